@@ -1,0 +1,263 @@
+/*
+ * fp64 CPU oracle for the Inkling attention block.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the benchmark's
+ * CPU-baseline leg may load this library.  It shares no code, header, table or helper
+ * with the CUDA library: it is the plain definition of what the block computes, written
+ * out with no blocking, fusion or reordering, so that a reader can check it by eye.
+ *
+ * Sources (the vLLM "Day-0 support for TML Inkling" blog and the Inkling serving
+ * recipes):
+ *  - Sconv: "Model Architecture / Sconv" (a window-4 short convolution applied to the
+ *    attention keys and values, per channel) and "vLLM Integration & Optimization /
+ *    Managing the sconv cache" (the cache keeps the last W-1 = 3 tokens).
+ *  - Relative attention: "Model Architecture / Attention" (GQA, head size 128, full and
+ *    sliding-window layers; a learned relative-position term added to the pre-softmax
+ *    logits instead of RoPE).  The pages do not fix the term's parameterisation; this
+ *    oracle uses a per-query-head table b[h, min(q-k, R-1)].
+ *  - MTP verify: "Model Architecture / MTP" (up to 9 query tokens per decode step);
+ *    decode and prefill share one definition and differ only in the number of new
+ *    tokens per sequence.
+ *
+ * Readings taken where the pages are silent (each listed in the design notes):
+ *  tap order w[c,3] * current token + ... + w[c,0] * token three back; no bias, no
+ *  activation, no residual in the sconv; zero history at sequence start; the cache
+ *  holds raw (pre-conv) rows; conv output rounded to bf16 (round to nearest even) before
+ *  it enters the bf16 KV cache; logit = scale * q.k + b[h, min(p_q - p_k, R-1)]; key
+ *  allowed iff 0 <= p_q - p_k and (window == 0 or p_q - p_k <= window - 1); query head h
+ *  reads KV head h / (Hq/Hkv); query token t of sequence b sits at position
+ *  seq_len[b] - n_b + t.
+ *
+ * Storage: the KV cache is paged, [num_blocks][Hkv][128 slots][128 dims] bf16; logical
+ * key j of sequence b lives in page block_table[b][j / 128], slot j % 128.  bf16 values
+ * are passed as their 16-bit patterns.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define OR_D 128
+#define OR_PAGE 128
+#define OR_TAPS 4
+
+enum { OR_OK = 0, OR_ERR_ARG = 1, OR_ERR_BLOCK = 2, OR_ERR_NOMEM = 3 };
+
+/* bf16 -> double: the 16 bits are the top half of an IEEE binary32; exact. */
+double oracle_bf16_to_double(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* double -> bf16, round to nearest, ties to even, in one step (no detour through
+ * binary32, which would round twice).  bf16 keeps 8 significant bits and the binary32
+ * exponent range, so the spacing of bf16 values around y is 2^(e-7) with
+ * e = max(floor(log2|y|), -126); subnormals share the spacing 2^-133. */
+uint16_t oracle_bf16_round(double y)
+{
+    uint32_t u;
+    float f;
+    if (isnan(y)) return 0x7fc0;
+    if (y == 0.0) {
+        f = (float)y; /* keeps the sign of zero */
+        memcpy(&u, &f, sizeof u);
+        return (uint16_t)(u >> 16);
+    }
+    int e;
+    frexp(y, &e); /* |y| = m * 2^e, m in [0.5, 1): floor(log2|y|) = e - 1 */
+    int ex = e - 1;
+    if (ex < -126) ex = -126;
+    double ulp = ldexp(1.0, ex - 7);
+    double r = nearbyint(y / ulp) * ulp; /* default rounding mode: nearest-even */
+    /* largest finite bf16 is (2 - 2^-7) * 2^127; anything rounding past it is inf */
+    if (fabs(r) >= ldexp(1.0, 128)) r = y > 0 ? INFINITY : -INFINITY;
+    f = (float)r; /* exact: r has at most 8 significant bits */
+    memcpy(&u, &f, sizeof u);
+    return (uint16_t)(u >> 16);
+}
+
+/*
+ * Sconv on K and on V for the new tokens of every sequence, written into the paged
+ * cache, then the sconv state moved forward.
+ *
+ *   x~ = [state rows 0..2 (oldest first) ; the n_b new raw rows]
+ *   y[t, c] = sum_{j=0..3} w[c, j] * x~[t + j, c]          (x~[t + 3] = new row t)
+ *   cache[slot_mapping[t]] <- bf16(y[t])   (slot -1: not stored)
+ *   state <- x~[n_b], x~[n_b + 1], x~[n_b + 2]
+ *
+ * k_raw, v_raw [T][C]; w_k, w_v [C][4]; state [B][2][3][C] (index 0 = K, 1 = V);
+ * caches [num_blocks][Hkv][128][128]; C = Hkv * 128.
+ */
+int oracle_sconv_kv(const uint16_t *k_raw, const uint16_t *v_raw, const float *w_k,
+                    const float *w_v, uint16_t *state, const int32_t *cu_q_lens,
+                    const int64_t *slot_mapping, uint16_t *k_cache, uint16_t *v_cache,
+                    int B, int T, int Hkv, int64_t num_blocks)
+{
+    if (B < 0 || T < 0 || Hkv <= 0 || num_blocks < 0) return OR_ERR_ARG;
+    if (cu_q_lens[0] != 0 || cu_q_lens[B] != T) return OR_ERR_ARG;
+    const int C = Hkv * OR_D;
+    for (int b = 0; b < B; ++b) {
+        const int t0 = cu_q_lens[b];
+        const int n = cu_q_lens[b + 1] - t0;
+        if (n < 0) return OR_ERR_ARG;
+        for (int which = 0; which < 2; ++which) {
+            const uint16_t *x = which == 0 ? k_raw : v_raw;
+            const float *w = which == 0 ? w_k : w_v;
+            uint16_t *cache = which == 0 ? k_cache : v_cache;
+            uint16_t *st = state + ((size_t)b * 2 + which) * 3 * C;
+            /* x~ rows as bit patterns: rows 0..2 from the state, rows 3.. from x */
+            uint16_t *ext = malloc(sizeof(uint16_t) * (size_t)(n + 3) * C);
+            if (!ext) return OR_ERR_NOMEM;
+            memcpy(ext, st, sizeof(uint16_t) * 3 * (size_t)C);
+            memcpy(ext + 3 * (size_t)C, x + (size_t)t0 * C, sizeof(uint16_t) * (size_t)n * C);
+            for (int t = 0; t < n; ++t) {
+                const int64_t slot = slot_mapping[t0 + t];
+                if (slot < 0) continue;
+                if (slot >= num_blocks * OR_PAGE) { free(ext); return OR_ERR_BLOCK; }
+                const int64_t blk = slot / OR_PAGE, off = slot % OR_PAGE;
+                for (int c = 0; c < C; ++c) {
+                    double y = 0.0;
+                    for (int j = 0; j < OR_TAPS; ++j)
+                        y += (double)w[(size_t)c * OR_TAPS + j] *
+                             oracle_bf16_to_double(ext[(size_t)(t + j) * C + c]);
+                    const int h = c / OR_D, d = c % OR_D;
+                    cache[(((size_t)blk * Hkv + h) * OR_PAGE + off) * OR_D + d] =
+                        oracle_bf16_round(y);
+                }
+            }
+            memcpy(st, ext + (size_t)n * C, sizeof(uint16_t) * 3 * (size_t)C);
+            free(ext);
+        }
+    }
+    return OR_OK;
+}
+
+/* ---------------------------------------------------------------- attention ---- */
+
+typedef struct {
+    const uint16_t *q, *k_cache, *v_cache;
+    const int32_t *block_table, *cu_q_lens, *seq_lens, *rows;
+    const float *bias;
+    int max_blocks, R, window, B, T, Hq, Hkv, n_rows;
+    int64_t num_blocks;
+    double scale;
+    double *out, *lse;
+    long next;  /* shared work counter over (row, head) items */
+    int status;
+} attn_job;
+
+static int seq_of_token(const int32_t *cu, int B, int t)
+{
+    for (int b = 0; b < B; ++b)
+        if (t >= cu[b] && t < cu[b + 1]) return b;
+    return -1;
+}
+
+/* One query row (token t, head h):
+ *   s_j = scale * sum_d q[t,h,d] K[j,kv,d] + b[h, min(p - j, R - 1)]  for allowed j
+ *   o   = sum_j softmax(s)_j V[j,kv,:],   lse = log sum_j exp(s_j)
+ * softmax is evaluated as exp(s_j - max s) / sum exp(s_k - max s), the same quantity. */
+static int attend_one(attn_job *jb, int item, double *s)
+{
+    const int ri = item / jb->Hq, h = item % jb->Hq;
+    const int t = jb->rows[ri];
+    const int b = seq_of_token(jb->cu_q_lens, jb->B, t);
+    if (b < 0) return OR_ERR_ARG;
+    const int n = jb->cu_q_lens[b + 1] - jb->cu_q_lens[b];
+    const int L = jb->seq_lens[b];
+    const int p = L - n + (t - jb->cu_q_lens[b]);
+    const int G = jb->Hq / jb->Hkv, kv = h / G;
+    const uint16_t *qrow = jb->q + ((size_t)t * jb->Hq + h) * OR_D;
+    double qd[OR_D];
+    for (int d = 0; d < OR_D; ++d) qd[d] = oracle_bf16_to_double(qrow[d]);
+
+    /* allowed keys: 0 <= p - j, and p - j <= window - 1 when a window is set */
+    const int j_lo = (jb->window > 0 && p - jb->window + 1 > 0) ? p - jb->window + 1 : 0;
+    const int j_hi = p; /* p <= L - 1 */
+    double smax = -INFINITY;
+    for (int j = j_lo; j <= j_hi; ++j) {
+        const int32_t blk = jb->block_table[(size_t)b * jb->max_blocks + j / OR_PAGE];
+        if (blk < 0 || blk >= jb->num_blocks) return OR_ERR_BLOCK;
+        const uint16_t *krow =
+            jb->k_cache + (((size_t)blk * jb->Hkv + kv) * OR_PAGE + j % OR_PAGE) * OR_D;
+        double dot = 0.0;
+        for (int d = 0; d < OR_D; ++d) dot += qd[d] * oracle_bf16_to_double(krow[d]);
+        const int dist = p - j;
+        const int bi = dist < jb->R - 1 ? dist : jb->R - 1;
+        s[j - j_lo] = jb->scale * dot + (double)jb->bias[(size_t)h * jb->R + bi];
+        if (s[j - j_lo] > smax) smax = s[j - j_lo];
+    }
+    double denom = 0.0, acc[OR_D];
+    for (int d = 0; d < OR_D; ++d) acc[d] = 0.0;
+    for (int j = j_lo; j <= j_hi; ++j) {
+        const double e = exp(s[j - j_lo] - smax);
+        denom += e;
+        const int32_t blk = jb->block_table[(size_t)b * jb->max_blocks + j / OR_PAGE];
+        const uint16_t *vrow =
+            jb->v_cache + (((size_t)blk * jb->Hkv + kv) * OR_PAGE + j % OR_PAGE) * OR_D;
+        for (int d = 0; d < OR_D; ++d) acc[d] += e * oracle_bf16_to_double(vrow[d]);
+    }
+    double *o = jb->out + ((size_t)ri * jb->Hq + h) * OR_D;
+    for (int d = 0; d < OR_D; ++d) o[d] = acc[d] / denom;
+    if (jb->lse) jb->lse[(size_t)ri * jb->Hq + h] = smax + log(denom);
+    return OR_OK;
+}
+
+static void *attn_worker(void *arg)
+{
+    attn_job *jb = (attn_job *)arg;
+    int maxL = 1;
+    for (int b = 0; b < jb->B; ++b)
+        if (jb->seq_lens[b] > maxL) maxL = jb->seq_lens[b];
+    double *s = malloc(sizeof(double) * (size_t)maxL);
+    if (!s) { __atomic_store_n(&jb->status, OR_ERR_NOMEM, __ATOMIC_RELAXED); return NULL; }
+    const long total = (long)jb->n_rows * jb->Hq;
+    for (;;) {
+        const long item = __atomic_fetch_add(&jb->next, 1, __ATOMIC_RELAXED);
+        if (item >= total) break;
+        const int rc = attend_one(jb, (int)item, s);
+        if (rc != OR_OK) { __atomic_store_n(&jb->status, rc, __ATOMIC_RELAXED); break; }
+    }
+    free(s);
+    return NULL;
+}
+
+/*
+ * Attention rows for the listed query tokens (global token indices into q), all heads.
+ * q [T][Hq][128]; block_table [B][max_blocks]; bias [Hq][R] fp32;
+ * out [n_rows][Hq][128] fp64; lse [n_rows][Hq] fp64 (natural log; may be NULL).
+ */
+int oracle_rel_attn(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                    const int32_t *block_table, int max_blocks, const int32_t *cu_q_lens,
+                    const int32_t *seq_lens, const float *bias, int R, double scale,
+                    int window, int B, int T, int Hq, int Hkv, int64_t num_blocks,
+                    const int32_t *rows, int n_rows, double *out, double *lse, int n_threads)
+{
+    if (B <= 0 || T < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || R < 1 || window < 0 ||
+        n_rows < 0 || max_blocks <= 0)
+        return OR_ERR_ARG;
+    for (int b = 0; b < B; ++b) {
+        const int n = cu_q_lens[b + 1] - cu_q_lens[b];
+        if (n < 0 || seq_lens[b] < n || seq_lens[b] > max_blocks * OR_PAGE) return OR_ERR_ARG;
+    }
+    for (int i = 0; i < n_rows; ++i)
+        if (rows[i] < 0 || rows[i] >= T) return OR_ERR_ARG;
+    attn_job jb = {q, k_cache, v_cache, block_table, cu_q_lens, seq_lens, rows, bias,
+                   max_blocks, R, window, B, T, Hq, Hkv, n_rows, num_blocks, scale,
+                   out, lse, 0, OR_OK};
+    if (n_threads < 1) n_threads = 1;
+    if (n_threads > 512) n_threads = 512;
+    pthread_t th[512];
+    int started = 0;
+    for (int i = 0; i < n_threads; ++i) {
+        if (pthread_create(&th[i], NULL, attn_worker, &jb) != 0) break;
+        ++started;
+    }
+    if (started == 0) attn_worker(&jb);
+    for (int i = 0; i < started; ++i) pthread_join(th[i], NULL);
+    return jb.status;
+}
