@@ -1,0 +1,169 @@
+/*
+ * inkling.h — C ABI of the Inkling attention-block library (sm_103a / GB300).
+ *
+ * The block, as the vLLM "Day-0 support for TML Inkling" blog describes it:
+ *   - "Model Architecture / Sconv": a short convolution of window 4, per channel, on the
+ *     attention keys and on the attention values;
+ *   - "vLLM Integration & Optimization / Managing the sconv cache": the conv keeps the
+ *     last W-1 = 3 tokens of its input per sequence;
+ *   - "Model Architecture / Attention": grouped-query attention, head size 128, full and
+ *     sliding-window layers, with a learned relative-position term added to the
+ *     pre-softmax logits in place of RoPE;
+ *   - "Model Architecture / MTP": up to 9 tokens per decode step (speculative verify);
+ *   - "vLLM Integration & Optimization / FA4 with sheared bias": a per-configuration
+ *     split factor for the KV dimension ("num_splits");
+ *   - the Inkling serving recipe ("Client Usage"): paged KV cache with --block-size 128.
+ * The pages do not fix the relative term's form; this library uses a per-query-head
+ * table b[h][min(q_pos - k_pos, R - 1)] (fp32, R entries per head).
+ *
+ * Conventions shared by every entry point
+ *   Layouts (row-major, densely packed, element sizes in brackets):
+ *     q          [T][Hq][128]                     bf16  (T = all new tokens of the batch)
+ *     k_raw,v_raw[T][C]                           bf16  (C = Hkv * 128, c = kv_head*128 + d)
+ *     w_k, w_v   [C][4]                           fp32  (w[c][3] multiplies the current
+ *                                                        token, w[c][0] the token 3 back)
+ *     sconv_state[B][2][3][C]                     bf16  (index 0 = K, 1 = V; raw pre-conv
+ *                                                        rows, oldest first)
+ *     k_cache, v_cache [num_blocks][Hkv][128][128] bf16 (page, kv head, slot, dim)
+ *     block_table[B][max_blocks]                  int32 (logical page -> physical page)
+ *     cu_q_lens  [B+1]                            int32 (prefix sums of new tokens)
+ *     seq_lens   [B]                              int32 (KV length incl. the new tokens)
+ *     slot_mapping[T]                             int64 (page*128 + slot, -1 = skip)
+ *     bias       [Hq][R]                          fp32
+ *     out        [T][Hq][128]                     bf16 or fp32 (out_dtype)
+ *     lse        [T][Hq]                          fp32, natural log (may be NULL)
+ *   Positions: query token t of sequence b sits at seq_lens[b] - n_b + t, n_b =
+ *   cu_q_lens[b+1] - cu_q_lens[b].  Key j is allowed for a query at p iff 0 <= p - j and
+ *   (window == 0 or p - j <= window - 1).  Logit = scale * q.k + bias[h][min(p-j, R-1)].
+ *   Query head h reads KV head h / (Hq / Hkv).
+ *   Pointers: every array pointer is a DEVICE pointer unless stated otherwise.  The
+ *   caller allocates and owns all memory; the library allocates no device memory and
+ *   keeps no per-call state.  All work is enqueued on `stream` and never synchronised.
+ *   Alignment: q, k_cache, v_cache, k_raw, v_raw and out must be 16-byte aligned.
+ *   Errors: argument problems found on the host return a nonzero inkling_status_t and
+ *   launch nothing.  Problems found on the device (a physical page id outside
+ *   [0, num_blocks), inconsistent lengths, a wait that ran out of time) are written to
+ *   `dev_status` (a device int32, first error wins; may be NULL), readable after the
+ *   stream is synchronised; the affected rows are left unwritten.  Kernels never trap.
+ *   Ordering: inkling_sconv_kv for a step's new tokens must precede, on the same stream,
+ *   the attention call that reads them.  The caller zeroes the sconv state rows of a
+ *   sequence that starts from nothing.
+ */
+#ifndef INKLING_H
+#define INKLING_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define INKLING_API __attribute__((visibility("default")))
+#else
+#define INKLING_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *inkling_stream_t; /* same object as cudaStream_t; NULL = legacy default stream */
+
+typedef enum {
+  INKLING_OK = 0,
+  INKLING_ERR_INVALID_ARG = 1, /* host-side argument check failed; nothing launched */
+  INKLING_ERR_UNSUPPORTED = 2, /* shape outside what the kernels implement */
+  INKLING_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed */
+  INKLING_ERR_TIMEOUT = 4,     /* device: a bounded wait ran out (written to dev_status) */
+  INKLING_ERR_BAD_BLOCK = 5,   /* device: page id or slot outside the cache */
+  INKLING_ERR_BAD_INPUT = 6,   /* device: lengths inconsistent with the host-side limits */
+  INKLING_ERR_WORKSPACE = 7    /* workspace missing or too small */
+} inkling_status_t;
+
+enum { INKLING_HEAD_DIM = 128, INKLING_BLOCK_SIZE = 128, INKLING_SCONV_WIDTH = 4,
+       INKLING_MAX_DECODE_Q = 9 };
+enum { INKLING_OUT_BF16 = 0, INKLING_OUT_F32 = 1 };
+
+/* Human-readable name of a status code (static storage, never NULL). */
+INKLING_API const char *inkling_status_string(int status);
+
+/* Library version, e.g. 0x000100 = 0.1.0. */
+INKLING_API int inkling_version(void);
+
+/*
+ * inkling_sconv_kv — the window-4 causal short convolution on K and on V (blog, "Model
+ * Architecture / Sconv") for the new tokens of every sequence, written straight into the
+ * paged KV cache, then the sconv cache moved forward ("Managing the sconv cache").
+ *
+ *   x~ = [sconv_state[b][kv] rows 0..2 ; new raw rows of b]
+ *   y[t][c] = sum_{j=0..3} w[c][j] * x~[t + j][c]        (fp32 arithmetic)
+ *   cache[slot_mapping[t]] = bf16_rne(y[t])   (skipped when slot_mapping[t] == -1)
+ *   sconv_state[b][kv] = the last 3 rows of x~ (raw, pre-conv)
+ *
+ * B sequences, T = cu_q_lens[B] new tokens in total, max_q_len >= every n_b (host-side
+ * bound used to size the launch).  num_blocks = pages in each cache.  The raw rows never
+ * round-trip through HBM: they are read once and the conv output lands in the cache.
+ * Device errors: slot >= num_blocks*128 -> INKLING_ERR_BAD_BLOCK; n_b > max_q_len or
+ * cu_q_lens not monotone -> INKLING_ERR_BAD_INPUT.
+ */
+INKLING_API int inkling_sconv_kv(const void *k_raw, const void *v_raw, const float *w_k, const float *w_v,
+                     void *sconv_state, const int32_t *cu_q_lens, const int64_t *slot_mapping,
+                     void *k_cache, void *v_cache, int32_t B, int32_t T, int32_t Hkv,
+                     int64_t num_blocks, int32_t max_q_len, int32_t *dev_status,
+                     inkling_stream_t stream);
+
+/*
+ * inkling_rel_attn_prefill — relative-bias GQA attention (blog, "Model Architecture /
+ * Attention") for every new token of every sequence, reading keys and values from the
+ * paged cache (so a cached prefix is attended to as well: chunked prefill).
+ *
+ *   out[t][h] = sum_j softmax_j(scale * q[t][h].K[j] + bias[h][min(p - j, R-1)]) V[j]
+ *
+ * Hq % Hkv == 0, head size 128, R >= 1, window >= 0 (0 = full causal), out_dtype
+ * INKLING_OUT_BF16 or INKLING_OUT_F32.  max_q_len >= every n_b (sizes the grid).
+ * lse (nullable) receives log(sum_j exp(logit_j)).
+ */
+INKLING_API int inkling_rel_attn_prefill(const void *q, const void *k_cache, const void *v_cache,
+                             const int32_t *block_table, int32_t max_blocks,
+                             const int32_t *cu_q_lens, const int32_t *seq_lens,
+                             const float *bias, int32_t R, float scale, int32_t window,
+                             void *out, int32_t out_dtype, float *lse, int32_t B, int32_t T,
+                             int32_t Hq, int32_t Hkv, int64_t num_blocks, int32_t max_q_len,
+                             int32_t *dev_status, inkling_stream_t stream);
+
+/*
+ * inkling_rel_attn_decode_workspace_size — bytes of device workspace that
+ * inkling_rel_attn_decode needs for these limits (0 when no split is needed).
+ * num_splits: 0 = the library's choice for this device (same rule as the decode call).
+ */
+INKLING_API size_t inkling_rel_attn_decode_workspace_size(int32_t B, int32_t Hq, int32_t Hkv,
+                                              int32_t max_q_len, int32_t max_seq_len,
+                                              int32_t window, int32_t num_splits);
+
+/*
+ * inkling_rel_attn_decode — the same attention for decode steps of up to
+ * INKLING_MAX_DECODE_Q (9) new tokens per sequence (MTP verify, blog "Model Architecture /
+ * MTP"), with the keys of each sequence split into `num_splits` page ranges processed in
+ * parallel and merged exactly (the blog's FA4 "num_splits", "FA4 with sheared bias").
+ * The G = Hq/Hkv query heads and n_b tokens that share a KV head are packed into one
+ * tile, so every K/V page is read once per KV head.
+ *
+ * max_q_len <= 9; max_seq_len >= every seq_lens[b] (host bound used to size the split).
+ * num_splits: 0 = automatic.  workspace: device memory of at least
+ * inkling_rel_attn_decode_workspace_size(...) bytes with the same arguments (may be NULL
+ * when that size is 0); owned by the caller, contents need no initialisation and are
+ * scratch after the call.  Concurrent calls must not share a workspace.
+ */
+INKLING_API int inkling_rel_attn_decode(const void *q, const void *k_cache, const void *v_cache,
+                            const int32_t *block_table, int32_t max_blocks,
+                            const int32_t *cu_q_lens, const int32_t *seq_lens,
+                            const float *bias, int32_t R, float scale, int32_t window,
+                            void *out, int32_t out_dtype, float *lse, int32_t B, int32_t T,
+                            int32_t Hq, int32_t Hkv, int64_t num_blocks, int32_t max_q_len,
+                            int32_t max_seq_len, int32_t num_splits, void *workspace,
+                            size_t workspace_bytes, int32_t *dev_status,
+                            inkling_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* INKLING_H */

@@ -1,0 +1,127 @@
+"""Inkling attention block on GB300: sconv on K/V into a paged cache, and relative-bias
+GQA prefill / paged decode, as a C-ABI CUDA library (include/inkling.h) for sm_103a.
+
+This module only marshals torch tensors into the C calls: every step of the computation
+runs in the library's CUDA kernels.  It raises if the library has not been built; there
+is no CPU or PyTorch fallback.
+"""
+from __future__ import annotations
+
+from typing import Optional
+
+import torch
+
+from . import _lib
+
+HEAD_DIM = 128
+BLOCK_SIZE = 128
+MAX_DECODE_Q = 9
+OUT_BF16, OUT_F32 = 0, 1
+
+InklingError = _lib.InklingError
+status_string = _lib.status_string
+library_path = _lib.library_path
+
+
+def _check_cuda(*ts):
+    dev = None
+    for t in ts:
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise ValueError("all tensors must be on a CUDA device")
+        if not t.is_contiguous():
+            raise ValueError("all tensors must be contiguous")
+        if dev is None:
+            dev = t.device
+        elif t.device != dev:
+            raise ValueError("all tensors must be on the same device")
+    return dev
+
+
+def _stream(stream):
+    return (stream if stream is not None else torch.cuda.current_stream()).cuda_stream
+
+
+def sconv_kv(k_raw: torch.Tensor, v_raw: torch.Tensor, w_k: torch.Tensor, w_v: torch.Tensor,
+             sconv_state: torch.Tensor, cu_q_lens: torch.Tensor, slot_mapping: torch.Tensor,
+             k_cache: torch.Tensor, v_cache: torch.Tensor, *, max_q_len: int,
+             dev_status: Optional[torch.Tensor] = None, stream=None) -> None:
+    """inkling_sconv_kv: conv on the new raw K/V rows straight into the paged caches, and
+    the in-place sconv-state update.  Shapes as in include/inkling.h."""
+    dev = _check_cuda(k_raw, v_raw, w_k, w_v, sconv_state, cu_q_lens, slot_mapping, k_cache,
+                      v_cache, dev_status)
+    assert k_raw.dtype == v_raw.dtype == sconv_state.dtype == k_cache.dtype == torch.bfloat16
+    assert w_k.dtype == w_v.dtype == torch.float32
+    assert cu_q_lens.dtype == torch.int32 and slot_mapping.dtype == torch.int64
+    B = cu_q_lens.shape[0] - 1
+    T = k_raw.shape[0]
+    hkv = k_cache.shape[1]
+    with torch.cuda.device(dev):
+        _lib.call("inkling_sconv_kv", k_raw, v_raw, w_k, w_v, sconv_state, cu_q_lens,
+                  slot_mapping, k_cache, v_cache, B, T, hkv, k_cache.shape[0], int(max_q_len),
+                  dev_status, _stream(stream))
+
+
+def _attn_common(q, k_cache, v_cache, block_table, cu_q_lens, seq_lens, bias, out, lse,
+                 dev_status):
+    dev = _check_cuda(q, k_cache, v_cache, block_table, cu_q_lens, seq_lens, bias, out, lse,
+                      dev_status)
+    assert q.dtype == k_cache.dtype == v_cache.dtype == torch.bfloat16
+    assert block_table.dtype == cu_q_lens.dtype == seq_lens.dtype == torch.int32
+    assert bias.dtype == torch.float32
+    if out.dtype == torch.bfloat16:
+        out_dtype = OUT_BF16
+    elif out.dtype == torch.float32:
+        out_dtype = OUT_F32
+    else:
+        raise ValueError("out must be bf16 or fp32")
+    if lse is not None:
+        assert lse.dtype == torch.float32
+    return dev, out_dtype
+
+
+def rel_attn_prefill(q, k_cache, v_cache, block_table, cu_q_lens, seq_lens, bias, *,
+                     scale: float, window: int, max_q_len: int, out: torch.Tensor,
+                     lse: Optional[torch.Tensor] = None, dev_status=None, stream=None) -> None:
+    """inkling_rel_attn_prefill into `out` ([T, Hq, 128], bf16 or fp32)."""
+    dev, out_dtype = _attn_common(q, k_cache, v_cache, block_table, cu_q_lens, seq_lens, bias,
+                                  out, lse, dev_status)
+    T, hq = q.shape[0], q.shape[1]
+    with torch.cuda.device(dev):
+        _lib.call("inkling_rel_attn_prefill", q, k_cache, v_cache, block_table,
+                  block_table.shape[1], cu_q_lens, seq_lens, bias, bias.shape[1], float(scale),
+                  int(window), out, out_dtype, lse, cu_q_lens.shape[0] - 1, T, hq,
+                  k_cache.shape[1], k_cache.shape[0], int(max_q_len), dev_status,
+                  _stream(stream))
+
+
+def decode_workspace_size(B: int, hq: int, hkv: int, max_q_len: int, max_seq_len: int,
+                          window: int, num_splits: int = 0, device=None) -> int:
+    with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
+        return _lib.workspace_size(B, hq, hkv, max_q_len, max_seq_len, window, num_splits)
+
+
+def rel_attn_decode(q, k_cache, v_cache, block_table, cu_q_lens, seq_lens, bias, *,
+                    scale: float, window: int, max_q_len: int, max_seq_len: int,
+                    out: torch.Tensor, lse: Optional[torch.Tensor] = None, num_splits: int = 0,
+                    workspace: Optional[torch.Tensor] = None, dev_status=None,
+                    stream=None) -> None:
+    """inkling_rel_attn_decode into `out`.  `workspace` is a caller-owned device buffer of
+    at least decode_workspace_size(...) bytes (allocated here when omitted)."""
+    dev, out_dtype = _attn_common(q, k_cache, v_cache, block_table, cu_q_lens, seq_lens, bias,
+                                  out, lse, dev_status)
+    T, hq = q.shape[0], q.shape[1]
+    B = cu_q_lens.shape[0] - 1
+    hkv = k_cache.shape[1]
+    with torch.cuda.device(dev):
+        need = _lib.workspace_size(B, hq, hkv, int(max_q_len), int(max_seq_len), int(window),
+                                   int(num_splits))
+        if workspace is None and need > 0:
+            workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+        ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+        _lib.call("inkling_rel_attn_decode", q, k_cache, v_cache, block_table,
+                  block_table.shape[1], cu_q_lens, seq_lens, bias, bias.shape[1], float(scale),
+                  int(window), out, out_dtype, lse, B, T, hq, hkv, k_cache.shape[0],
+                  int(max_q_len), int(max_seq_len), int(num_splits), workspace, ws_bytes,
+                  dev_status, _stream(stream))

@@ -1,0 +1,590 @@
+// Split-KV paged decode for relative-bias GQA with up to 9 new tokens per sequence
+// (vLLM Day-0 Inkling blog: "Model Architecture / MTP" for the 9-token verify step,
+// "FA4 with sheared bias" for the per-configuration num_splits).
+//
+// One CTA = (split, KV head, sequence).  The n_b new tokens x G query heads that share
+// the KV head are packed as rows r = t*G + g of one 128-row tile (72 rows for 9 tokens
+// and G = 8), so each K/V page is read from HBM once per KV head.  The packed Q lives in
+// tensor memory (64 columns of bf16 pairs) and both contractions run on the tensor core:
+// S = Q K^T with Q from TMEM (TS form), O += P V with P from TMEM.
+//   warp 4      TMA producer: K/V pages of the split (three-stage ring of 64 KB).
+//   warp 5      MMA issuer; S is double-buffered so S(i+1) overlaps softmax(i).
+//   warps 0-3   thread r owns packed row r: bias, mask, online softmax, P, epilogue.
+// TMEM columns: Q [0,64), S0 [128,256), S1 [256,384), O [384,512).
+// A sequence whose key range fits one split writes its output directly; otherwise every
+// split writes (m, l, unnormalised O) to the workspace and combine_kernel merges them:
+//   O = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s,  M = max_s m_s   (log2 domain).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace ink {
+namespace decode {
+
+constexpr int kStages = 3;
+constexpr int kThreads = 192;
+constexpr int kMaxG = 16;
+constexpr int kBiasStride = 144;  // floats per staged head (>= 127 + 9)
+constexpr uint32_t kIdescQK = idesc_bf16(128, 128, false, false);
+constexpr uint32_t kIdescPV = idesc_bf16(128, 128, false, true);
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;
+constexpr uint32_t kColQ = 0, kColS0 = 128, kColO = 384;
+
+struct __align__(1024) Smem {
+  uint8_t k[kStages][2][16384];
+  uint8_t v[kStages][2][16384];
+  float bias[2][kMaxG * kBiasStride];
+  uint64_t k_full[kStages], v_full[kStages], kv_empty[kStages];
+  uint64_t q_ready, s_full[2], p_full, pv_done, o_full, drain;
+  uint32_t tmem_base;
+  int abort_flag;
+  int bad_block;
+};
+
+struct Params {
+  const uint16_t* q;
+  const int32_t* block_table;
+  const int32_t* cu_q_lens;
+  const int32_t* seq_lens;
+  const float* bias;
+  void* out;
+  float* lse;
+  float* part_o;   // [B][Hkv][S][rmax][128]
+  float* part_ml;  // [B][Hkv][S][rmax][2]
+  int* status;
+  int max_blocks, R, window, out_dtype;
+  int B, T, Hq, Hkv, G, max_q_len, rmax, num_splits, pages_per_split;
+  long long num_blocks;
+  float scale_log2;
+};
+
+// Key pages a sequence's decode rows can see: [kt_lo, kt_hi].
+__device__ __forceinline__ void page_range(int L, int n, int window, int& kt_lo, int& kt_hi) {
+  const int k_lo = window > 0 ? max(0, L - n - window + 1) : 0;
+  kt_lo = k_lo >> 7;
+  kt_hi = (L - 1) >> 7;
+}
+
+__device__ __forceinline__ uint64_t desc_k(const uint8_t (*atoms)[16384], int ks) {
+  return sdesc_sw128(smem_u32(atoms[ks >> 2]) + (ks & 3) * 32, 16, 1024);
+}
+__device__ __forceinline__ uint64_t desc_v(const uint8_t (*atoms)[16384], int ks) {
+  return sdesc_sw128(smem_u32(atoms[0]) + ks * 2048, 16384, 1024);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+decode_kernel(const __grid_constant__ CUtensorMap map_k,
+              const __grid_constant__ CUtensorMap map_v, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  Smem& s = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                     ~uintptr_t(1023));
+  const int warp = warp_id(), lane = lane_id();
+  const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int t_seq0 = p.cu_q_lens[b];
+  const int n = p.cu_q_lens[b + 1] - t_seq0;
+  if (n == 0) return;
+  const int L = p.seq_lens[b];
+  if (n < 0 || n > p.max_q_len || n > L || L > p.max_blocks * 128) {
+    if (split == 0 && kvh == 0 && threadIdx.x == 0) report(p.status, kErrBadInput);
+    return;
+  }
+  int kt_lo, kt_hi;
+  page_range(L, n, p.window, kt_lo, kt_hi);
+  const int npages_seq = kt_hi - kt_lo + 1;
+  const int nsplit_b = (npages_seq + p.pages_per_split - 1) / p.pages_per_split;
+  if (split >= nsplit_b) return;
+  if (nsplit_b > p.num_splits) {  // host-side max_seq_len was too small
+    if (split == 0 && threadIdx.x == 0) report(p.status, kErrBadInput);
+    return;
+  }
+  const int pg0 = kt_lo + split * p.pages_per_split;
+  const int np = min(p.pages_per_split, kt_hi + 1 - pg0);
+  const int rows = n * p.G;
+  const int32_t* table = p.block_table + (size_t)b * p.max_blocks;
+
+  if (threadIdx.x == 0) {
+    s.abort_flag = 0;
+    s.bad_block = 0;
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < np; i += kThreads) {
+    const int32_t blk = table[pg0 + i];
+    if (blk < 0 || (long long)blk >= p.num_blocks) s.bad_block = 1;
+  }
+  __syncthreads();
+  if (s.bad_block) {
+    if (threadIdx.x == 0) report(p.status, kErrBadBlock);
+    return;
+  }
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&s.k_full[i], 1);
+      mbar_init(&s.v_full[i], 1);
+      mbar_init(&s.kv_empty[i], 1);
+    }
+    mbar_init(&s.q_ready, 128);
+    mbar_init(&s.s_full[0], 1);
+    mbar_init(&s.s_full[1], 1);
+    mbar_init(&s.p_full, 128);
+    mbar_init(&s.pv_done, 1);
+    mbar_init(&s.o_full, 1);
+    mbar_init(&s.drain, 1);
+    fence_barrier_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(&s.tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s.tmem_base;
+  volatile int* abort_flag = &s.abort_flag;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ TMA producer ---
+    if (lane == 0) {
+      tma_prefetch_desc(&map_k);
+      tma_prefetch_desc(&map_v);
+      const uint64_t pol = l2_policy_evict_first();
+      int issued = 0;
+      for (int i = 0; i < np; ++i) {
+        const int st = i % kStages;
+        if (i >= kStages && !mbar_wait(&s.kv_empty[st], ((i / kStages) - 1) & 1, abort_flag)) {
+          report(p.status, kErrTimeout);
+          s.abort_flag = 1;
+          break;
+        }
+        const int page = table[pg0 + i] * p.Hkv + kvh;
+        mbar_arrive_expect_tx(&s.k_full[st], 32768u);
+        tma_load_3d_hint(s.k[st][0], &map_k, &s.k_full[st], 0, 0, page, pol);
+        tma_load_3d_hint(s.k[st][1], &map_k, &s.k_full[st], 64, 0, page, pol);
+        mbar_arrive_expect_tx(&s.v_full[st], 32768u);
+        tma_load_3d_hint(s.v[st][0], &map_v, &s.v_full[st], 0, 0, page, pol);
+        tma_load_3d_hint(s.v[st][1], &map_v, &s.v_full[st], 64, 0, page, pol);
+        issued = i + 1;
+      }
+      if (*abort_flag) {
+        for (int i = max(0, issued - kStages); i < issued; ++i) {
+          const int st = i % kStages;
+          const uint32_t ph = (i / kStages) & 1;
+          volatile int never = 0;
+          mbar_wait(&s.k_full[st], ph, &never);
+          mbar_wait(&s.v_full[st], ph, &never);
+        }
+      }
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------- MMA issuer ---
+    bool ok = mbar_wait(&s.q_ready, 0, abort_flag) && mbar_wait(&s.k_full[0], 0, abort_flag);
+    bool issued_any = false;
+    if (ok) {
+      tc_fence_after();
+      if (lane == 0) {
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+          umma_ts(tmem + kColS0, tmem + kColQ + ks * 8, desc_k(s.k[0], ks), kIdescQK, ks > 0);
+        umma_commit(&s.s_full[0]);
+      }
+      issued_any = true;
+      __syncwarp();
+    }
+    for (int i = 0; ok && i < np; ++i) {
+      const int st = i % kStages;
+      if (i + 1 < np) {
+        const int st1 = (i + 1) % kStages;
+        ok = mbar_wait(&s.k_full[st1], ((i + 1) / kStages) & 1, abort_flag);
+        if (!ok) break;
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t dS = tmem + kColS0 + ((i + 1) & 1) * 128;
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            umma_ts(dS, tmem + kColQ + ks * 8, desc_k(s.k[st1], ks), kIdescQK, ks > 0);
+          umma_commit(&s.s_full[(i + 1) & 1]);
+        }
+        __syncwarp();
+      }
+      ok = mbar_wait(&s.p_full, i & 1, abort_flag) &&
+           mbar_wait(&s.v_full[st], (i / kStages) & 1, abort_flag);
+      if (!ok) break;
+      const int kt = pg0 + i;
+      if ((kt + 1) * 128 > L) {
+        // slots past the end of the sequence: P is 0 there but the stale V could be NaN
+        const int r0 = L - kt * 128;
+        const int chunks = (128 - r0) * 8;
+        for (int c = lane; c < 2 * chunks; c += 32) {
+          const int half = c / chunks, cc = c % chunks;
+          *reinterpret_cast<uint4*>(s.v[st][half] + (size_t)(r0 + cc / 8) * 128 + (cc % 8) * 16) =
+              make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t aP = tmem + kColS0 + (i & 1) * 128;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+          umma_ts(tmem + kColO, aP + ks * 8, desc_v(s.v[st], ks), kIdescPV, (i > 0 || ks > 0));
+        umma_commit(&s.kv_empty[st]);
+        umma_commit(&s.pv_done);
+      }
+      __syncwarp();
+    }
+    if (ok) {
+      if (lane == 0) umma_commit(&s.o_full);
+    } else {
+      report(p.status, kErrTimeout);
+      s.abort_flag = 1;
+      if (issued_any) {
+        if (lane == 0) umma_commit(&s.drain);
+        __syncwarp();
+        volatile int never = 0;
+        mbar_wait(&s.drain, 0, &never);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax group ---
+    const int r = threadIdx.x;  // 0..127
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const bool warp_active = warp * 32 < rows;
+    const bool valid = r < rows;
+    const int t = valid ? r / p.G : 0;
+    const int g = valid ? r % p.G : 0;
+    const int h = kvh * p.G + g;
+
+    // packed Q rows into TMEM columns [0, 64)
+    {
+      uint32_t qr[64];
+      if (valid) {
+        const uint4* src = reinterpret_cast<const uint4*>(p.q + ((size_t)(t_seq0 + t) * p.Hq + h) * 128);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const uint4 w = __ldg(src + j);
+          qr[4 * j] = w.x; qr[4 * j + 1] = w.y; qr[4 * j + 2] = w.z; qr[4 * j + 3] = w.w;
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 64; ++j) qr[j] = 0u;
+      }
+      tmem_st32(tmem + lane_base + kColQ, qr);
+      tmem_st32(tmem + lane_base + kColQ + 32, qr + 32);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&s.q_ready);
+    }
+
+    const float* brow = p.bias + (size_t)h * p.R;
+    const int R = p.R, W = p.window;
+    const float bconst = __ldg(brow + R - 1) * kLog2e;
+    const int pq = L - n + t;  // position of this row's token
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int i = 0; i < np; ++i) {
+      const int k0 = (pg0 + i) * 128;
+      const int dmin = (L - n) - k0 - 127;  // smallest distance in the page over all rows
+      const int dmax = (L - 1) - k0;
+      const bool clamped = dmin >= R - 1;
+      const bool masked = dmin < 0 || (W > 0 && dmax > W - 1);
+      float* bias_buf = s.bias[i & 1];
+      if (!clamped) {
+        // head g': rev[j] = b[kvh*G + g'][clamp(dmax - j)] * log2 e, j < 127 + n
+        const int span = 127 + n;
+        for (int e = r; e < p.G * span; e += 128) {
+          const int gg = e / span, j = e % span;
+          int d = dmax - j;
+          d = d < 0 ? 0 : (d > R - 1 ? R - 1 : d);
+          bias_buf[gg * kBiasStride + j] = __ldg(p.bias + (size_t)(kvh * p.G + gg) * R + d) * kLog2e;
+        }
+        named_bar_sync(1, 128);
+      }
+      if (!mbar_wait(&s.s_full[i & 1], (i >> 1) & 1, abort_flag)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t tS = tmem + lane_base + kColS0 + (i & 1) * 128;
+      if (warp_active) {
+        uint32_t sr[128];  // S row, then x = logit * log2 e, then packed bf16 P pairs
+        tmem_ld32(tS + 0, sr);
+        tmem_ld32(tS + 32, sr + 32);
+        tmem_ld32(tS + 64, sr + 64);
+        tmem_ld32(tS + 96, sr + 96);
+        tmem_wait_ld();
+        reg_fence<128>(sr);
+        if (clamped) {
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            sr[c] = __float_as_uint(fmaf(__uint_as_float(sr[c]), p.scale_log2, bconst));
+        } else {
+          const float* bp = bias_buf + g * kBiasStride + (n - 1 - t);
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            sr[c] = __float_as_uint(fmaf(__uint_as_float(sr[c]), p.scale_log2, bp[c]));
+        }
+        if (masked) {
+          const int d0 = pq - k0;
+#pragma unroll
+          for (int c = 0; c < 128; ++c) {
+            const int d = d0 - c;
+            const bool allowed = d >= 0 && (W == 0 || d <= W - 1);
+            sr[c] = allowed ? sr[c] : __float_as_uint(-INFINITY);
+          }
+        }
+        float mx0 = __uint_as_float(sr[0]), mx1 = __uint_as_float(sr[1]);
+        float mx2 = __uint_as_float(sr[2]), mx3 = __uint_as_float(sr[3]);
+#pragma unroll
+        for (int c = 4; c < 128; c += 4) {
+          mx0 = fmaxf(mx0, __uint_as_float(sr[c]));
+          mx1 = fmaxf(mx1, __uint_as_float(sr[c + 1]));
+          mx2 = fmaxf(mx2, __uint_as_float(sr[c + 2]));
+          mx3 = fmaxf(mx3, __uint_as_float(sr[c + 3]));
+        }
+        const float m_new = fmaxf(m, fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)));
+        const bool need = m_new > m + kRescaleThreshold || (m == -INFINITY && m_new > -INFINITY);
+        const float alpha = need ? ex2(m - m_new) : 1.f;
+        if (need) {
+          l *= alpha;
+          m = m_new;
+        }
+        const float m_use = m == -INFINITY ? 0.f : m;
+        float l0 = 0.f, l1 = 0.f;
+        // P pairs overwrite the registers they came from (index c/2 <= c)
+#pragma unroll
+        for (int c = 0; c < 128; c += 2) {
+          const float e0 = ex2(__uint_as_float(sr[c]) - m_use);
+          const float e1 = ex2(__uint_as_float(sr[c + 1]) - m_use);
+          l0 += e0;
+          l1 += e1;
+          sr[c / 2] = pack_bf16(e0, e1);
+        }
+        l += l0 + l1;
+        // rescale O (warp-wide, only when some row's max grew past the threshold)
+        if (__any_sync(0xffffffffu, need) && i > 0) {
+          // O must hold PV(i-1) before it is scaled
+          if (!mbar_wait(&s.pv_done, (i - 1) & 1, abort_flag)) ok = false;
+          tc_fence_after();
+          uint32_t orr[32];
+          const uint32_t tO = tmem + lane_base + kColO;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            tmem_ld32(tO + c * 32, orr);
+            tmem_wait_ld();
+            reg_fence<32>(orr);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) orr[j] = __float_as_uint(__uint_as_float(orr[j]) * alpha);
+            tmem_st32(tO + c * 32, orr);
+          }
+        }
+        tmem_st32(tS + 0, sr);
+        tmem_st32(tS + 32, sr + 32);
+        tmem_wait_st();
+      }
+      tc_fence_before();
+      mbar_arrive(&s.p_full);
+      if (!ok) break;
+    }
+    if (ok) ok = mbar_wait(&s.o_full, 0, abort_flag);
+    if (!ok) {
+      report(p.status, kErrTimeout);
+      s.abort_flag = 1;
+    } else if (warp_active) {
+      tc_fence_after();
+      const uint32_t tO = tmem + lane_base + kColO;
+      const bool direct = nsplit_b == 1;
+      const float inv_l = direct ? 1.f / l : 1.f;
+      const size_t prow = (((size_t)b * p.Hkv + kvh) * p.num_splits + split) * p.rmax + r;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t orr[32];
+        tmem_ld32(tO + c * 32, orr);
+        tmem_wait_ld();
+        reg_fence<32>(orr);
+        if (!valid) continue;
+        if (!direct) {
+          float4* dst = reinterpret_cast<float4*>(p.part_o + prow * 128 + c * 32);
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            dst[j] = make_float4(__uint_as_float(orr[4 * j]), __uint_as_float(orr[4 * j + 1]),
+                                 __uint_as_float(orr[4 * j + 2]), __uint_as_float(orr[4 * j + 3]));
+        } else {
+          const size_t obase = ((size_t)(t_seq0 + t) * p.Hq + h) * 128 + c * 32;
+          if (p.out_dtype == 0) {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + obase);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              uint4 w;
+              w.x = pack_bf16(__uint_as_float(orr[8 * j + 0]) * inv_l, __uint_as_float(orr[8 * j + 1]) * inv_l);
+              w.y = pack_bf16(__uint_as_float(orr[8 * j + 2]) * inv_l, __uint_as_float(orr[8 * j + 3]) * inv_l);
+              w.z = pack_bf16(__uint_as_float(orr[8 * j + 4]) * inv_l, __uint_as_float(orr[8 * j + 5]) * inv_l);
+              w.w = pack_bf16(__uint_as_float(orr[8 * j + 6]) * inv_l, __uint_as_float(orr[8 * j + 7]) * inv_l);
+              dst[j] = w;
+            }
+          } else {
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + obase);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              dst[j] = make_float4(__uint_as_float(orr[4 * j + 0]) * inv_l, __uint_as_float(orr[4 * j + 1]) * inv_l,
+                                   __uint_as_float(orr[4 * j + 2]) * inv_l, __uint_as_float(orr[4 * j + 3]) * inv_l);
+          }
+        }
+      }
+      if (valid) {
+        if (nsplit_b == 1) {
+          if (p.lse != nullptr) p.lse[(size_t)(t_seq0 + t) * p.Hq + h] = (m + __log2f(l)) * kLn2;
+        } else {
+          p.part_ml[prow * 2 + 0] = m;
+          p.part_ml[prow * 2 + 1] = l;
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// Merge the split partials of every (sequence, KV head) that needed more than one split.
+// One warp per packed row; each lane owns 4 of the 128 output columns.
+__global__ void __launch_bounds__(256)
+combine_kernel(const Params p) {
+  const int kvh = blockIdx.x, b = blockIdx.y;
+  const int t_seq0 = p.cu_q_lens[b];
+  const int n = p.cu_q_lens[b + 1] - t_seq0;
+  if (n <= 0 || n > p.max_q_len) return;
+  const int L = p.seq_lens[b];
+  if (n > L || L > p.max_blocks * 128) return;
+  int kt_lo, kt_hi;
+  page_range(L, n, p.window, kt_lo, kt_hi);
+  const int nsp = (kt_hi - kt_lo + 1 + p.pages_per_split - 1) / p.pages_per_split;
+  if (nsp <= 1 || nsp > p.num_splits) return;
+  const int rows = n * p.G;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const size_t base = ((size_t)b * p.Hkv + kvh) * p.num_splits;
+  for (int r = warp; r < rows; r += 8) {
+    float M = -INFINITY;
+    for (int sp = lane; sp < nsp; sp += 32) M = fmaxf(M, p.part_ml[((base + sp) * p.rmax + r) * 2]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float lsum = 0.f;
+    for (int sp = 0; sp < nsp; ++sp) {
+      const size_t prow = (base + sp) * p.rmax + r;
+      const float ms = p.part_ml[prow * 2], ls = p.part_ml[prow * 2 + 1];
+      const float wgt = ms == -INFINITY ? 0.f : ex2(ms - M);
+      if (wgt == 0.f) continue;
+      const float4 o = reinterpret_cast<const float4*>(p.part_o + prow * 128)[lane];
+      acc.x = fmaf(wgt, o.x, acc.x);
+      acc.y = fmaf(wgt, o.y, acc.y);
+      acc.z = fmaf(wgt, o.z, acc.z);
+      acc.w = fmaf(wgt, o.w, acc.w);
+      lsum = fmaf(wgt, ls, lsum);
+    }
+    const float inv = 1.f / lsum;
+    const int t = r / p.G, h = kvh * p.G + r % p.G;
+    const size_t obase = ((size_t)(t_seq0 + t) * p.Hq + h) * 128 + lane * 4;
+    if (p.out_dtype == 0) {
+      uint2 w;
+      w.x = pack_bf16(acc.x * inv, acc.y * inv);
+      w.y = pack_bf16(acc.z * inv, acc.w * inv);
+      *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.out) + obase) = w;
+    } else {
+      *reinterpret_cast<float4*>(static_cast<float*>(p.out) + obase) =
+          make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    }
+    if (lane == 0 && p.lse != nullptr) p.lse[(size_t)(t_seq0 + t) * p.Hq + h] = (M + __log2f(lsum)) * kLn2;
+  }
+}
+
+}  // namespace decode
+
+DecodeSplit decode_split(int B, int Hkv, int max_q_len, int max_seq_len, int window,
+                         int num_splits_req, int num_sms) {
+  // pages a sequence's decode rows can span (a window range may straddle one more page)
+  long long range_pages = ((long long)max_seq_len + 127) / 128;
+  if (window > 0) {
+    const long long w_pages = ((long long)window + max_q_len - 1 + 127) / 128 + 1;
+    if (w_pages < range_pages) range_pages = w_pages;
+  }
+  if (range_pages < 1) range_pages = 1;
+  long long ns;
+  if (num_splits_req > 0) {
+    ns = num_splits_req;
+  } else {
+    // enough CTAs to balance ragged lengths over the SMs, but >= 16 pages per split
+    const long long pairs = (long long)B * Hkv;
+    ns = (8LL * num_sms + pairs - 1) / (pairs > 0 ? pairs : 1);
+    const long long cap = (range_pages + 15) / 16;
+    if (ns > cap) ns = cap;
+  }
+  if (ns < 1) ns = 1;
+  if (ns > range_pages) ns = range_pages;
+  const long long pps = (range_pages + ns - 1) / ns;
+  ns = (range_pages + pps - 1) / pps;
+  return DecodeSplit{(int)ns, (int)pps};
+}
+
+size_t decode_workspace_bytes(int B, int Hq, int Hkv, int max_q_len, int num_splits) {
+  if (num_splits <= 1) return 0;
+  const size_t rmax = (size_t)max_q_len * (Hq / Hkv);
+  const size_t rows = (size_t)B * Hkv * num_splits * rmax;
+  return rows * 128 * sizeof(float) + rows * 2 * sizeof(float) + 256;
+}
+
+cudaError_t launch_decode(const AttnArgs& a, const AttnMaps& maps, cudaStream_t stream) {
+  using namespace decode;
+  Params p;
+  p.q = static_cast<const uint16_t*>(a.q);
+  p.block_table = a.block_table;
+  p.cu_q_lens = a.cu_q_lens;
+  p.seq_lens = a.seq_lens;
+  p.bias = a.bias;
+  p.out = a.out;
+  p.lse = a.lse;
+  p.status = a.dev_status;
+  p.max_blocks = a.max_blocks;
+  p.R = a.R;
+  p.window = a.window;
+  p.out_dtype = a.out_dtype;
+  p.B = a.B;
+  p.T = a.T;
+  p.Hq = a.Hq;
+  p.Hkv = a.Hkv;
+  p.G = a.Hq / a.Hkv;
+  p.max_q_len = a.max_q_len;
+  p.rmax = a.max_q_len * p.G;
+  p.num_splits = a.num_splits;
+  p.pages_per_split = a.pages_per_split;
+  p.num_blocks = a.num_blocks;
+  p.scale_log2 = a.scale * kLog2e;
+  p.part_o = nullptr;
+  p.part_ml = nullptr;
+  if (a.num_splits > 1) {
+    const size_t rows = (size_t)a.B * a.Hkv * a.num_splits * p.rmax;
+    uintptr_t w = (reinterpret_cast<uintptr_t>(a.workspace) + 255) & ~uintptr_t(255);
+    p.part_o = reinterpret_cast<float*>(w);
+    p.part_ml = p.part_o + rows * 128;
+  }
+  if (a.B == 0) return cudaSuccess;
+  const size_t smem = sizeof(Smem) + 1024;
+  cudaError_t e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(a.num_splits, a.Hkv, a.B);
+  decode_kernel<<<grid, kThreads, smem, stream>>>(maps.k, maps.v, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || a.num_splits <= 1) return e;
+  combine_kernel<<<dim3(a.Hkv, a.B), 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace ink

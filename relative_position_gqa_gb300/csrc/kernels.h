@@ -1,0 +1,75 @@
+// Private launch interface between the C ABI (api.cu) and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+namespace ink {
+
+struct SconvArgs {
+  const void* k_raw;
+  const void* v_raw;
+  const float* w_k;
+  const float* w_v;
+  void* state;
+  const int32_t* cu_q_lens;
+  const int64_t* slot_mapping;
+  void* k_cache;
+  void* v_cache;
+  int B, T, Hkv;
+  long long num_blocks;
+  int max_q_len;
+  int* dev_status;
+};
+
+struct AttnArgs {
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_table;
+  int max_blocks;
+  const int32_t* cu_q_lens;
+  const int32_t* seq_lens;
+  const float* bias;
+  int R;
+  float scale;
+  int window;
+  void* out;
+  int out_dtype;  // 0 = bf16, 1 = fp32
+  float* lse;
+  int B, T, Hq, Hkv;
+  long long num_blocks;
+  int max_q_len;
+  int* dev_status;
+  // decode only
+  int max_seq_len;
+  int num_splits;
+  int pages_per_split;
+  void* workspace;
+  size_t workspace_bytes;
+};
+
+// Tensor maps built by the host for the attention kernels.
+struct AttnMaps {
+  CUtensorMap q;  // (d=128, head=Hq, token=T), box (64, 1, 128), 128-byte swizzle
+  CUtensorMap k;  // (d=128, slot=128, page*Hkv+head), box (64, 128, 1), 128-byte swizzle
+  CUtensorMap v;
+};
+
+cudaError_t launch_sconv_kv(const SconvArgs& a, cudaStream_t stream);
+cudaError_t launch_prefill(const AttnArgs& a, const AttnMaps& maps, cudaStream_t stream);
+cudaError_t launch_decode(const AttnArgs& a, const AttnMaps& maps, cudaStream_t stream);
+
+// Decode split rule shared by the workspace query and the launch.
+struct DecodeSplit {
+  int num_splits;
+  int pages_per_split;
+};
+DecodeSplit decode_split(int B, int Hkv, int max_q_len, int max_seq_len, int window,
+                         int num_splits_req, int num_sms);
+size_t decode_workspace_bytes(int B, int Hq, int Hkv, int max_q_len, int num_splits);
+
+}  // namespace ink

@@ -1,0 +1,509 @@
+// Relative-bias GQA prefill attention on the fifth-generation tensor core (sm_103a).
+//
+// What it computes (vLLM Day-0 Inkling blog, "Model Architecture / Attention"): for each
+// new token at position p and query head h,
+//   out = sum_j softmax_j(scale * q.K[j] + b[h][min(p - j, R-1)]) V[j]
+// over keys j with 0 <= p - j (and p - j <= window - 1 for sliding-window layers), keys
+// and values read from the paged bf16 cache.
+//
+// Design (one CTA = 128 query tokens x two query heads of one KV group):
+//   warp 8      TMA producer: Q tiles once, then K and V pages (two-stage ring).
+//   warp 9      MMA issuer (one thread): S = Q K^T (SS form), O += P V (P read from
+//               tensor memory, TS form), commits to mbarriers.  Owns the TMEM allocation.
+//   warps 0-3   softmax for head A, warps 4-7 softmax for head B: thread r owns query row
+//               r (= TMEM lane r).  It loads its S row, adds the relative bias, masks,
+//               keeps a running max / sum (rescaling O in TMEM only when the max grew by
+//               more than 2^8), writes P as bf16 over the S columns, and finally
+//               normalises O and stores it.
+// Tensor memory (512 columns): S_A [0,128) S_B [128,256) O_A [256,384) O_B [384,512);
+// P_X overlays the first 64 columns of S_X.  The MMA thread issues
+//   S_A0 S_B0 | PV_A0 S_A1 | PV_B0 S_B1 | PV_A1 S_A2 | ...
+// so each softmax group works while the tensor core serves the other (ping-pong).
+//
+// The relative bias ("sheared" along the tile diagonals): within a 128x128 tile the
+// distance is delta + r - c with delta = p0 - k0, so row r needs a contiguous run of the
+// table, reversed.  Per tile the softmax group stages the 255 values it needs (times
+// log2 e) in shared memory, in four copies shifted by one float each, so that every
+// thread reads its run with aligned 16-byte loads.  Tiles whose smallest distance is
+// already past R-1 use the single clamped value instead (no loads).  Key tiles are
+// visited from the diagonal backwards; only tiles that overlap the causal diagonal, the
+// window edge or the end of the sequence pay for masking; tiles outside the window are
+// never visited.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace ink {
+namespace prefill {
+
+constexpr int kTile = 128;
+constexpr int kStages = 2;
+constexpr int kThreads = 320;
+constexpr int kBiasCopy = 264;  // floats per shifted copy; 264/4 = 66 = 2 (mod 8) spreads banks
+constexpr uint32_t kIdescQK = idesc_bf16(128, 128, false, false);
+constexpr uint32_t kIdescPV = idesc_bf16(128, 128, false, true);
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only past a 256x growth
+
+struct __align__(1024) Smem {
+  uint8_t q[2][2][16384];        // [head slot][d half][128 rows x 128 B], swizzled
+  uint8_t k[kStages][2][16384];  // [stage][d half][128 keys x 128 B]
+  uint8_t v[kStages][2][16384];
+  float bias[2][2][4][kBiasCopy];  // [head slot][buffer][shift][index]
+  uint64_t q_full;
+  uint64_t k_full[kStages], v_full[kStages], kv_empty[kStages];
+  uint64_t s_full[2], p_full[2], o_full, drain;
+  uint32_t tmem_base;
+  int abort_flag;
+  int bad_block;
+};
+
+struct Params {
+  const int32_t* block_table;
+  const int32_t* cu_q_lens;
+  const int32_t* seq_lens;
+  const float* bias;
+  void* out;
+  float* lse;
+  int* status;
+  int max_blocks, R, window, out_dtype;
+  int B, T, Hq, Hkv, G, pairs_per_group, head_pairs, q_tiles, max_q_len;
+  long long num_blocks;
+  float scale_log2;
+};
+
+__device__ __forceinline__ uint64_t desc_kmajor(const uint8_t (*atoms)[16384], int ks) {
+  return sdesc_sw128(smem_u32(atoms[ks >> 2]) + (ks & 3) * 32, 16, 1024);
+}
+__device__ __forceinline__ uint64_t desc_v(const uint8_t (*atoms)[16384], int ks) {
+  // V tile [128 keys][128 d] as two 64-wide d halves: MN-major B operand,
+  // 16 keys per MMA = 2048 bytes, the two d halves 16 KB apart.
+  return sdesc_sw128(smem_u32(atoms[0]) + ks * 2048, 16384, 1024);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+prefill_kernel(const __grid_constant__ CUtensorMap map_q,
+               const __grid_constant__ CUtensorMap map_k,
+               const __grid_constant__ CUtensorMap map_v, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  Smem& s = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                     ~uintptr_t(1023));
+  const int warp = warp_id(), lane = lane_id();
+
+  // ---- work item: heavy (late) query tiles first, head pairs fastest ----
+  const int idx = blockIdx.x;
+  const int hp = idx % p.head_pairs;
+  const int rest = idx / p.head_pairs;
+  const int b = rest % p.B;
+  const int qt = p.q_tiles - 1 - rest / p.B;
+  const int t_seq0 = p.cu_q_lens[b];
+  const int n = p.cu_q_lens[b + 1] - t_seq0;
+  if (qt * kTile >= n) return;  // whole CTA, before any barrier
+  const int L = p.seq_lens[b];
+  if (n > L || n > p.max_q_len || L > p.max_blocks * kTile) {
+    if (threadIdx.x == 0) report(p.status, kErrBadInput);
+    return;
+  }
+  const int P0 = L - n + qt * kTile;  // position of row 0
+  const int rows = min(kTile, n - qt * kTile);
+  const int lo = p.window > 0 ? max(0, P0 - p.window + 1) : 0;
+  const int hi = P0 + rows - 1;
+  const int kt_lo = lo / kTile, kt_hi = hi / kTile;
+  const int ntiles = kt_hi - kt_lo + 1;
+  const int kvh = hp / p.pairs_per_group;
+  const int h0 = kvh * p.G + 2 * (hp % p.pairs_per_group);
+  const bool has_b = (2 * (hp % p.pairs_per_group) + 1) < p.G;
+  const int t_glob0 = t_seq0 + qt * kTile;
+  const int32_t* table = p.block_table + (size_t)b * p.max_blocks;
+
+  if (threadIdx.x == 0) {
+    s.abort_flag = 0;
+    s.bad_block = 0;
+  }
+  __syncthreads();
+  for (int kt = kt_lo + (int)threadIdx.x; kt <= kt_hi; kt += kThreads) {
+    const int32_t blk = table[kt];
+    if (blk < 0 || (long long)blk >= p.num_blocks) s.bad_block = 1;
+  }
+  __syncthreads();
+  if (s.bad_block) {
+    if (threadIdx.x == 0) report(p.status, kErrBadBlock);
+    return;
+  }
+
+  if (threadIdx.x == 0) {
+    mbar_init(&s.q_full, 1);
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&s.k_full[i], 1);
+      mbar_init(&s.v_full[i], 1);
+      mbar_init(&s.kv_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s.s_full[i], 1);
+      mbar_init(&s.p_full[i], 128);
+    }
+    mbar_init(&s.o_full, 1);
+    mbar_init(&s.drain, 1);
+    fence_barrier_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(&s.tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s.tmem_base;
+  volatile int* abort_flag = &s.abort_flag;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ TMA producer ---
+    if (lane == 0) {
+      tma_prefetch_desc(&map_q);
+      tma_prefetch_desc(&map_k);
+      tma_prefetch_desc(&map_v);
+      mbar_arrive_expect_tx(&s.q_full, has_b ? 65536u : 32768u);
+      tma_load_3d(s.q[0][0], &map_q, &s.q_full, 0, h0, t_glob0);
+      tma_load_3d(s.q[0][1], &map_q, &s.q_full, 64, h0, t_glob0);
+      if (has_b) {
+        tma_load_3d(s.q[1][0], &map_q, &s.q_full, 0, h0 + 1, t_glob0);
+        tma_load_3d(s.q[1][1], &map_q, &s.q_full, 64, h0 + 1, t_glob0);
+      }
+      int issued = 0;
+      for (int i = 0; i < ntiles; ++i) {
+        const int st = i % kStages;
+        if (i >= kStages && !mbar_wait(&s.kv_empty[st], ((i / kStages) - 1) & 1, abort_flag)) {
+          report(p.status, kErrTimeout);
+          s.abort_flag = 1;
+          break;
+        }
+        const int page = table[kt_hi - i] * p.Hkv + kvh;
+        mbar_arrive_expect_tx(&s.k_full[st], 32768u);
+        tma_load_3d(s.k[st][0], &map_k, &s.k_full[st], 0, 0, page);
+        tma_load_3d(s.k[st][1], &map_k, &s.k_full[st], 64, 0, page);
+        mbar_arrive_expect_tx(&s.v_full[st], 32768u);
+        tma_load_3d(s.v[st][0], &map_v, &s.v_full[st], 0, 0, page);
+        tma_load_3d(s.v[st][1], &map_v, &s.v_full[st], 64, 0, page);
+        issued = i + 1;
+      }
+      if (*abort_flag) {
+        // let the copies already in flight land before the CTA goes away
+        for (int i = max(0, issued - kStages); i < issued; ++i) {
+          const int st = i % kStages;
+          const uint32_t ph = (i / kStages) & 1;
+          volatile int never = 0;
+          mbar_wait(&s.k_full[st], ph, &never);
+          mbar_wait(&s.v_full[st], ph, &never);
+        }
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------- MMA issuer ---
+    bool ok = mbar_wait(&s.q_full, 0, abort_flag) && mbar_wait(&s.k_full[0], 0, abort_flag);
+    bool issued_any = false;
+    if (ok) {
+      tc_fence_after();
+      if (lane == 0) {
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+          umma_ss(tmem + 0, desc_kmajor(s.q[0], ks), desc_kmajor(s.k[0], ks), kIdescQK, ks > 0);
+        umma_commit(&s.s_full[0]);
+        if (has_b) {
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            umma_ss(tmem + 128, desc_kmajor(s.q[1], ks), desc_kmajor(s.k[0], ks), kIdescQK,
+                    ks > 0);
+          umma_commit(&s.s_full[1]);
+        }
+      }
+      issued_any = true;
+      __syncwarp();
+    }
+    for (int i = 0; ok && i < ntiles; ++i) {
+      const int st = i % kStages;
+      const uint32_t ph = (i / kStages) & 1;
+      ok = mbar_wait(&s.p_full[0], i & 1, abort_flag) && mbar_wait(&s.v_full[st], ph, abort_flag);
+      if (!ok) break;
+      if (i == 0 && (kt_hi + 1) * kTile > L) {
+        // keys past the end of the sequence: their P is 0, but junk V could be NaN
+        const int r0 = L - kt_hi * kTile;
+        const int chunks = (kTile - r0) * 8;  // 16-byte chunks per d half
+        for (int c = lane; c < 2 * chunks; c += 32) {
+          const int half = c / chunks, cc = c % chunks;
+          *reinterpret_cast<uint4*>(s.v[st][half] + (size_t)(r0 + cc / 8) * 128 + (cc % 8) * 16) =
+              make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
+      tc_fence_after();
+      if (lane == 0) {
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+          umma_ts(tmem + 256, tmem + 0 + ks * 8, desc_v(s.v[st], ks), kIdescPV, (i > 0 || ks > 0));
+      }
+      __syncwarp();
+      const bool more = i + 1 < ntiles;
+      const int st1 = (i + 1) % kStages;
+      if (more) {
+        ok = mbar_wait(&s.k_full[st1], ((i + 1) / kStages) & 1, abort_flag);
+        if (!ok) break;
+        tc_fence_after();
+        if (lane == 0) {
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            umma_ss(tmem + 0, desc_kmajor(s.q[0], ks), desc_kmajor(s.k[st1], ks), kIdescQK, ks > 0);
+          umma_commit(&s.s_full[0]);
+        }
+        __syncwarp();
+      }
+      if (has_b) {
+        ok = mbar_wait(&s.p_full[1], i & 1, abort_flag);
+        if (!ok) break;
+        tc_fence_after();
+        if (lane == 0) {
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            umma_ts(tmem + 384, tmem + 128 + ks * 8, desc_v(s.v[st], ks), kIdescPV,
+                    (i > 0 || ks > 0));
+        }
+        __syncwarp();
+      }
+      if (lane == 0) umma_commit(&s.kv_empty[st]);
+      if (has_b && more) {
+        if (lane == 0) {
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            umma_ss(tmem + 128, desc_kmajor(s.q[1], ks), desc_kmajor(s.k[st1], ks), kIdescQK,
+                    ks > 0);
+          umma_commit(&s.s_full[1]);
+        }
+      }
+      __syncwarp();
+    }
+    if (ok) {
+      if (lane == 0) umma_commit(&s.o_full);
+    } else {
+      report(p.status, kErrTimeout);
+      s.abort_flag = 1;
+      if (issued_any) {
+        // wait for the tensor core to finish whatever was issued before freeing TMEM
+        if (lane == 0) umma_commit(&s.drain);
+        __syncwarp();
+        volatile int never = 0;
+        mbar_wait(&s.drain, 0, &never);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax groups ---
+    const int grp = warp >> 2;  // 0 = head A, 1 = head B
+    const int r = threadIdx.x & 127;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_base + grp * 128;
+    const uint32_t tO = tmem + lane_base + 256 + grp * 128;
+    const int h = h0 + grp;
+    if (grp == 0 || has_b) {
+      const float* brow = p.bias + (size_t)h * p.R;
+      const float bconst = __ldg(brow + p.R - 1) * kLog2e;
+      const int R = p.R, W = p.window;
+      const int sh = (127 - r) & 3;
+      const int base = (127 - r) - sh;
+      float m = -INFINITY, l = 0.f;
+      bool ok = true;
+      for (int i = 0; i < ntiles; ++i) {
+        const int k0 = (kt_hi - i) * kTile;
+        const int delta = P0 - k0;
+        const bool clamped = delta - 127 >= R - 1;
+        const bool masked = (delta < 127) || (W > 0 && delta + 127 > W - 1) || (k0 + 127 >= L);
+        float* bias_buf = &s.bias[grp][i & 1][0][0];
+        if (!clamped) {
+          // rev[j] = b[h][clamp(delta + 127 - j)] * log2 e, j = 0..255;  copy_q[j - q] = rev[j]
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int j = r + 128 * u;
+            int d = delta + 127 - j;
+            d = d < 0 ? 0 : (d > R - 1 ? R - 1 : d);
+            const float v = __ldg(brow + d) * kLog2e;
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              if (j - q >= 0) bias_buf[q * kBiasCopy + j - q] = v;
+          }
+          named_bar_sync(1 + grp, 128);
+        }
+        if (!mbar_wait(&s.s_full[grp], i & 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t sr[128];  // S row, then x = logit * log2 e, then packed bf16 P pairs
+        tmem_ld32(tS + 0, sr);
+        tmem_ld32(tS + 32, sr + 32);
+        tmem_ld32(tS + 64, sr + 64);
+        tmem_ld32(tS + 96, sr + 96);
+        tmem_wait_ld();
+        reg_fence<128>(sr);
+        if (clamped) {
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            sr[c] = __float_as_uint(fmaf(__uint_as_float(sr[c]), p.scale_log2, bconst));
+        } else {
+          const float4* bp = reinterpret_cast<const float4*>(bias_buf + sh * kBiasCopy + base);
+#pragma unroll
+          for (int g = 0; g < 32; ++g) {
+            const float4 bv = bp[g];
+            sr[4 * g + 0] = __float_as_uint(fmaf(__uint_as_float(sr[4 * g + 0]), p.scale_log2, bv.x));
+            sr[4 * g + 1] = __float_as_uint(fmaf(__uint_as_float(sr[4 * g + 1]), p.scale_log2, bv.y));
+            sr[4 * g + 2] = __float_as_uint(fmaf(__uint_as_float(sr[4 * g + 2]), p.scale_log2, bv.z));
+            sr[4 * g + 3] = __float_as_uint(fmaf(__uint_as_float(sr[4 * g + 3]), p.scale_log2, bv.w));
+          }
+        }
+        if (masked) {
+          const int dr = delta + r;  // distance at column 0
+          const int kend = L - k0;   // columns >= kend are past the sequence
+#pragma unroll
+          for (int c = 0; c < 128; ++c) {
+            const int d = dr - c;
+            const bool allowed = d >= 0 && (W == 0 || d <= W - 1) && c < kend;
+            sr[c] = allowed ? sr[c] : __float_as_uint(-INFINITY);
+          }
+        }
+        float mx0 = __uint_as_float(sr[0]), mx1 = __uint_as_float(sr[1]);
+        float mx2 = __uint_as_float(sr[2]), mx3 = __uint_as_float(sr[3]);
+#pragma unroll
+        for (int c = 4; c < 128; c += 4) {
+          mx0 = fmaxf(mx0, __uint_as_float(sr[c]));
+          mx1 = fmaxf(mx1, __uint_as_float(sr[c + 1]));
+          mx2 = fmaxf(mx2, __uint_as_float(sr[c + 2]));
+          mx3 = fmaxf(mx3, __uint_as_float(sr[c + 3]));
+        }
+        const float m_new = fmaxf(m, fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)));
+        const bool need = m_new > m + kRescaleThreshold || (m == -INFINITY && m_new > -INFINITY);
+        const float alpha = need ? ex2(m - m_new) : 1.f;
+        if (need) {
+          l *= alpha;
+          m = m_new;
+        }
+        const float m_use = m == -INFINITY ? 0.f : m;
+        float l0 = 0.f, l1 = 0.f;
+        // P pairs overwrite the registers they came from (index c/2 <= c)
+#pragma unroll
+        for (int c = 0; c < 128; c += 2) {
+          const float e0 = ex2(__uint_as_float(sr[c]) - m_use);
+          const float e1 = ex2(__uint_as_float(sr[c + 1]) - m_use);
+          l0 += e0;
+          l1 += e1;
+          sr[c / 2] = pack_bf16(e0, e1);
+        }
+        l += l0 + l1;
+        // rescale O (warp-wide, only when some row's max grew past the threshold)
+        if (__any_sync(0xffffffffu, need) && i > 0) {
+          // PV(i-1) was issued before S(i), so it is complete here
+          uint32_t orr[32];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            tmem_ld32(tO + c * 32, orr);
+            tmem_wait_ld();
+            reg_fence<32>(orr);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) orr[j] = __float_as_uint(__uint_as_float(orr[j]) * alpha);
+            tmem_st32(tO + c * 32, orr);
+          }
+        }
+        tmem_st32(tS + 0, sr);
+        tmem_st32(tS + 32, sr + 32);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&s.p_full[grp]);
+      }
+      if (ok) ok = mbar_wait(&s.o_full, 0, abort_flag);
+      if (!ok) {
+        report(p.status, kErrTimeout);
+        s.abort_flag = 1;
+      } else {
+        tc_fence_after();
+        const float inv_l = 1.f / l;
+        const int t = t_glob0 + r;
+        const bool store = r < rows;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t orr[32];
+          tmem_ld32(tO + c * 32, orr);
+          tmem_wait_ld();
+          reg_fence<32>(orr);
+          if (store) {
+            const size_t obase = ((size_t)t * p.Hq + h) * 128 + c * 32;
+            if (p.out_dtype == 0) {
+              uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + obase);
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                uint4 w;
+                w.x = pack_bf16(__uint_as_float(orr[8 * j + 0]) * inv_l, __uint_as_float(orr[8 * j + 1]) * inv_l);
+                w.y = pack_bf16(__uint_as_float(orr[8 * j + 2]) * inv_l, __uint_as_float(orr[8 * j + 3]) * inv_l);
+                w.z = pack_bf16(__uint_as_float(orr[8 * j + 4]) * inv_l, __uint_as_float(orr[8 * j + 5]) * inv_l);
+                w.w = pack_bf16(__uint_as_float(orr[8 * j + 6]) * inv_l, __uint_as_float(orr[8 * j + 7]) * inv_l);
+                dst[j] = w;
+              }
+            } else {
+              float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + obase);
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                dst[j] = make_float4(__uint_as_float(orr[4 * j + 0]) * inv_l, __uint_as_float(orr[4 * j + 1]) * inv_l,
+                                     __uint_as_float(orr[4 * j + 2]) * inv_l, __uint_as_float(orr[4 * j + 3]) * inv_l);
+            }
+          }
+        }
+        if (store && p.lse != nullptr) p.lse[(size_t)t * p.Hq + h] = (m + __log2f(l)) * kLn2;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace prefill
+
+cudaError_t launch_prefill(const AttnArgs& a, const AttnMaps& maps, cudaStream_t stream) {
+  using namespace prefill;
+  Params p;
+  p.block_table = a.block_table;
+  p.cu_q_lens = a.cu_q_lens;
+  p.seq_lens = a.seq_lens;
+  p.bias = a.bias;
+  p.out = a.out;
+  p.lse = a.lse;
+  p.status = a.dev_status;
+  p.max_blocks = a.max_blocks;
+  p.R = a.R;
+  p.window = a.window;
+  p.out_dtype = a.out_dtype;
+  p.B = a.B;
+  p.T = a.T;
+  p.Hq = a.Hq;
+  p.Hkv = a.Hkv;
+  p.G = a.Hq / a.Hkv;
+  p.pairs_per_group = (p.G + 1) / 2;
+  p.head_pairs = a.Hkv * p.pairs_per_group;
+  p.q_tiles = (a.max_q_len + kTile - 1) / kTile;
+  p.max_q_len = a.max_q_len;
+  p.num_blocks = a.num_blocks;
+  p.scale_log2 = a.scale * kLog2e;
+  const long long grid = (long long)p.q_tiles * p.B * p.head_pairs;
+  if (grid == 0) return cudaSuccess;
+  if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  const size_t smem = sizeof(Smem) + 1024;
+  cudaError_t e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  prefill_kernel<<<(unsigned)grid, kThreads, smem, stream>>>(maps.q, maps.k, maps.v, p);
+  return cudaGetLastError();
+}
+
+}  // namespace ink

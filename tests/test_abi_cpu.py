@@ -1,0 +1,93 @@
+"""The C-ABI library builds, loads without a GPU, exports every entry point that
+include/inkling.h declares, and rejects bad arguments on the host before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "inkling.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from relative_position_gqa_gb300 import build, _lib
+    build.build()
+    return _lib.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(inkling_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_three_calls():
+    names = declared_functions()
+    for n in ("inkling_sconv_kv", "inkling_rel_attn_prefill", "inkling_rel_attn_decode",
+              "inkling_rel_attn_decode_workspace_size", "inkling_status_string"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    from relative_position_gqa_gb300 import _lib
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert name in _lib.SIGNATURES, f"binding lacks {name}"
+
+
+def test_status_strings(lib):
+    from relative_position_gqa_gb300 import _lib
+    assert _lib.status_string(0) == "ok"
+    assert "page" in _lib.status_string(5)
+    assert _lib.status_string(12345) == "unknown status"
+
+
+FAKE = 0x10000  # a 16-byte aligned non-null value: the checks below fail before any use
+
+
+def _prefill(lib, **over):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, bt=FAKE, maxb=4, cu=FAKE, sl=FAKE, bias=FAKE, R=64,
+             scale=0.1, window=0, out=FAKE, odt=0, lse=None, B=1, T=10, Hq=4, Hkv=2, nb=4,
+             mq=10, st=None, stream=None)
+    a.update(over)
+    return lib.inkling_rel_attn_prefill(*a.values())
+
+
+@pytest.mark.parametrize("over", [dict(window=-1), dict(Hq=5), dict(R=0), dict(odt=3),
+                                  dict(q=None), dict(out=FAKE + 2), dict(B=-1), dict(nb=0)])
+def test_prefill_host_checks(lib, over):
+    assert _prefill(lib, **over) == 1
+
+
+def _decode(lib, **over):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, bt=FAKE, maxb=4, cu=FAKE, sl=FAKE, bias=FAKE, R=64,
+             scale=0.1, window=0, out=FAKE, odt=0, lse=None, B=1, T=10, Hq=8, Hkv=1, nb=4,
+             mq=9, msl=500, ns=2, ws=None, wsb=0, st=None, stream=None)
+    a.update(over)
+    return lib.inkling_rel_attn_decode(*a.values())
+
+
+def test_decode_host_checks(lib):
+    assert _decode(lib, mq=10) == 1              # more than 9 tokens
+    assert _decode(lib, Hq=32, Hkv=1) == 2       # G = 32: packed rows exceed one tile
+    assert _decode(lib, ns=-1) == 1
+    assert _decode(lib, ws=None, wsb=0) == 7     # two splits need a workspace
+
+
+def test_sconv_host_checks(lib):
+    f = lib.inkling_sconv_kv
+    assert f(None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 4, 1, 4, 4, None, None) == 1
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 4, 0, 4, 4, None, None) == 1
+    assert f(FAKE + 8, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 4, 1, 4, 4, None, None) == 1
+    # nothing to do is not an error
+    assert f(None, None, None, None, None, None, None, None, None, 0, 0, 1, 4, 0, None, None) == 0
+
+
+def test_workspace_size_rule(lib):
+    ws = lib.inkling_rel_attn_decode_workspace_size
+    assert ws(1, 8, 1, 9, 100000, 0, 1) == 0
+    two = ws(1, 8, 1, 9, 100000, 0, 2)
+    assert two >= 2 * 72 * 130 * 4
+    assert ws(1, 8, 1, 9, 100000, 0, 8) > two

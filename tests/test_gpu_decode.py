@@ -1,0 +1,123 @@
+"""GPU parity of inkling_rel_attn_decode: paged KV, up to 9 query tokens per sequence (MTP
+verify, vLLM Day-0 Inkling blog "Model Architecture / MTP"), split over pages and merged
+("FA4 with sheared bias": num_splits), full or sliding window."""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from harness import compare_out, gpu_attn, gpu_sconv, run_oracle, snapshot
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ink():
+    import relative_position_gqa_gb300 as m
+    m._lib.load()
+    return m
+
+
+def _status():
+    return torch.zeros(1, dtype=torch.int32, device="cuda")
+
+
+CASES = {
+    "mtp9_gqa8": W.small(q_lens=(9, 9, 9), seq_lens=(1000, 129, 9), hq=8, hkv=1, r=300),
+    "n1_gqa8": W.small(q_lens=(1, 1, 1, 1), seq_lens=(2000, 1, 128, 129), hq=16, hkv=2, r=500),
+    "mixed_n": W.small(q_lens=(1, 5, 9, 2, 0), seq_lens=(700, 5, 300, 1200, 40), hq=8, hkv=2, r=1000),
+    "window_300": W.small(q_lens=(9, 3, 9), seq_lens=(1500, 200, 301), hq=8, hkv=1, r=2000, window=300),
+    "window_1": W.small(q_lens=(9, 4), seq_lens=(500, 4), hq=4, hkv=2, r=64, window=1),
+    "g16_n8": W.small(q_lens=(8, 8), seq_lens=(900, 8), hq=16, hkv=1, r=128),
+    "g1_n9": W.small(q_lens=(9,), seq_lens=(777,), hq=2, hkv=2, r=50),
+    "g3_odd": W.small(q_lens=(7, 9), seq_lens=(400, 260), hq=9, hkv=3, r=8192),
+}
+
+
+def _run(ink, spec, seed, num_splits=0, out_dtype=torch.float32):
+    g = W.make_case(spec, seed=seed, device="cuda")
+    snap = snapshot(g)
+    st = _status()
+    gpu_sconv(ink, g, st)
+    out, lse = gpu_attn(ink, g, st, decode=True, num_splits=num_splits, out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0, ink.status_string(int(st.item()))
+    _, _, _, ref, ref_lse = run_oracle(snap)
+    return compare_out(out, lse, ref, ref_lse, snap.tok_index), out
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+@pytest.mark.parametrize("num_splits", [0, 1, 3])
+def test_decode_matches_oracle(ink, name, num_splits):
+    _run(ink, CASES[name], seed=61, num_splits=num_splits)
+
+
+def test_decode_bf16_output(ink):
+    _run(ink, CASES["mixed_n"], seed=62, out_dtype=torch.bfloat16, num_splits=2)
+
+
+def test_split_count_invariance(ink):
+    spec = W.small(q_lens=(9, 1), seq_lens=(3000, 2500), hq=8, hkv=1, r=4000)
+    outs = [_run(ink, spec, seed=63, num_splits=n)[1] for n in (1, 2, 5, 24, 0)]
+    for o in outs[1:]:
+        assert (o - outs[0]).abs().max().item() <= 2e-3
+
+
+def test_token_by_token_decode_equals_prefill(ink):
+    """Prefill 200 tokens, then decode steps of 1, 9, 9, 1, 5 tokens (sconv each step)
+    against one prefill of all 225 tokens."""
+    total = 225
+    spec = W.small(q_lens=(total,), seq_lens=(total,), hq=8, hkv=1, r=150, window=100)
+    full = W.make_case(spec, seed=64, device="cuda")
+    st = _status()
+    ref_case = W.make_case(spec, seed=64, device="cuda")
+    gpu_sconv(ink, ref_case, st)
+    ref, ref_lse = gpu_attn(ink, ref_case, st, decode=False)
+    start = 0
+    for n in (200, 1, 9, 9, 1, 5):
+        sl = slice(start, start + n)
+        cu = torch.tensor([0, n], dtype=torch.int32, device="cuda")
+        L = torch.tensor([start + n], dtype=torch.int32, device="cuda")
+        ink.sconv_kv(full.k_raw[sl], full.v_raw[sl], full.w_k, full.w_v, full.state, cu,
+                     full.slot_mapping[sl], full.k_cache, full.v_cache, max_q_len=n, dev_status=st)
+        out = torch.empty(n, spec.hq, 128, device="cuda")
+        lse = torch.empty(n, spec.hq, device="cuda")
+        if n <= 9:
+            ink.rel_attn_decode(full.q[sl], full.k_cache, full.v_cache, full.block_table, cu, L,
+                                full.bias, scale=spec.scale, window=spec.window, max_q_len=n,
+                                max_seq_len=start + n, out=out, lse=lse, dev_status=st)
+        else:
+            ink.rel_attn_prefill(full.q[sl], full.k_cache, full.v_cache, full.block_table, cu, L,
+                                 full.bias, scale=spec.scale, window=spec.window, max_q_len=n,
+                                 out=out, lse=lse, dev_status=st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        assert (out - ref[sl]).abs().max().item() <= 2e-3
+        assert (lse - ref_lse[sl]).abs().max().item() <= 1e-3
+        start += n
+    assert torch.equal(full.k_cache.view(torch.int16), ref_case.k_cache.view(torch.int16))
+
+
+def test_decode_workspace_too_small(ink):
+    spec = CASES["mtp9_gqa8"]
+    g = W.make_case(spec, seed=65, device="cuda")
+    need = ink.decode_workspace_size(spec.batch, spec.hq, spec.hkv, 9, spec.max_seq_len, 0, 4)
+    assert need > 0
+    ws = torch.empty(need - 1, dtype=torch.uint8, device="cuda")
+    out = torch.empty(spec.total_q, spec.hq, 128, device="cuda")
+    with pytest.raises(ink.InklingError) as e:
+        ink.rel_attn_decode(g.q, g.k_cache, g.v_cache, g.block_table, g.cu_q_lens, g.seq_lens,
+                            g.bias, scale=spec.scale, window=0, max_q_len=9,
+                            max_seq_len=spec.max_seq_len, num_splits=4, out=out, workspace=ws)
+    assert e.value.code == 7
+
+
+def test_decode_rejects_more_than_nine_tokens(ink):
+    spec = W.small(q_lens=(10,), seq_lens=(100,), hq=2, hkv=1)
+    g = W.make_case(spec, seed=66, device="cuda")
+    out = torch.empty(10, 2, 128, device="cuda")
+    with pytest.raises(ink.InklingError) as e:
+        ink.rel_attn_decode(g.q, g.k_cache, g.v_cache, g.block_table, g.cu_q_lens, g.seq_lens,
+                            g.bias, scale=spec.scale, window=0, max_q_len=10, max_seq_len=100,
+                            out=out)
+    assert e.value.code == 1
