@@ -45,6 +45,9 @@
  *   [0, num_blocks), inconsistent lengths, a wait that ran out of time) are written to
  *   `dev_status` (a device int32, first error wins; may be NULL), readable after the
  *   stream is synchronised; the affected rows are left unwritten.  Kernels never trap.
+ *   dev_status must hold 0 when a call is enqueued: the attention kernels poll it and
+ *   stop waiting once any CTA has reported an error, so that one failure ends the launch
+ *   quickly instead of every CTA running into its own time limit.
  *   Ordering: inkling_sconv_kv for a step's new tokens must precede, on the same stream,
  *   the attention call that reads them.  The caller zeroes the sconv state rows of a
  *   sequence that starts from nothing.

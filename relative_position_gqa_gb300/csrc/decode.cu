@@ -156,7 +156,7 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
       int issued = 0;
       for (int i = 0; i < np; ++i) {
         const int st = i % kStages;
-        if (i >= kStages && !mbar_wait(&s.kv_empty[st], ((i / kStages) - 1) & 1, abort_flag)) {
+        if (i >= kStages && !mbar_wait(&s.kv_empty[st], ((i / kStages) - 1) & 1, abort_flag, p.status)) {
           report(p.status, kErrTimeout);
           s.abort_flag = 1;
           break;
@@ -182,7 +182,7 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
     }
   } else if (warp == 5) {
     // ------------------------------------------------------------- MMA issuer ---
-    bool ok = mbar_wait(&s.q_ready, 0, abort_flag) && mbar_wait(&s.k_full[0], 0, abort_flag);
+    bool ok = mbar_wait(&s.q_ready, 0, abort_flag, p.status) && mbar_wait(&s.k_full[0], 0, abort_flag, p.status);
     bool issued_any = false;
     if (ok) {
       tc_fence_after();
@@ -199,7 +199,7 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
       const int st = i % kStages;
       if (i + 1 < np) {
         const int st1 = (i + 1) % kStages;
-        ok = mbar_wait(&s.k_full[st1], ((i + 1) / kStages) & 1, abort_flag);
+        ok = mbar_wait(&s.k_full[st1], ((i + 1) / kStages) & 1, abort_flag, p.status);
         if (!ok) break;
         tc_fence_after();
         if (lane == 0) {
@@ -211,8 +211,8 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
         }
         __syncwarp();
       }
-      ok = mbar_wait(&s.p_full, i & 1, abort_flag) &&
-           mbar_wait(&s.v_full[st], (i / kStages) & 1, abort_flag);
+      ok = mbar_wait(&s.p_full, i & 1, abort_flag, p.status) &&
+           mbar_wait(&s.v_full[st], (i / kStages) & 1, abort_flag, p.status);
       if (!ok) break;
       const int kt = pg0 + i;
       if ((kt + 1) * 128 > L) {
@@ -306,7 +306,7 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
         }
         named_bar_sync(1, 128);
       }
-      if (!mbar_wait(&s.s_full[i & 1], (i >> 1) & 1, abort_flag)) { ok = false; break; }
+      if (!mbar_wait(&s.s_full[i & 1], (i >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
       tc_fence_after();
       const uint32_t tS = tmem + lane_base + kColS0 + (i & 1) * 128;
       if (warp_active) {
@@ -367,7 +367,7 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
         // rescale O (warp-wide, only when some row's max grew past the threshold)
         if (__any_sync(0xffffffffu, need) && i > 0) {
           // O must hold PV(i-1) before it is scaled
-          if (!mbar_wait(&s.pv_done, (i - 1) & 1, abort_flag)) ok = false;
+          if (!mbar_wait(&s.pv_done, (i - 1) & 1, abort_flag, p.status)) ok = false;
           tc_fence_after();
           uint32_t orr[32];
           const uint32_t tO = tmem + lane_base + kColO;
@@ -389,7 +389,7 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
       mbar_arrive(&s.p_full);
       if (!ok) break;
     }
-    if (ok) ok = mbar_wait(&s.o_full, 0, abort_flag);
+    if (ok) ok = mbar_wait(&s.o_full, 0, abort_flag, p.status);
     if (!ok) {
       report(p.status, kErrTimeout);
       s.abort_flag = 1;

@@ -177,7 +177,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_q,
       int issued = 0;
       for (int i = 0; i < ntiles; ++i) {
         const int st = i % kStages;
-        if (i >= kStages && !mbar_wait(&s.kv_empty[st], ((i / kStages) - 1) & 1, abort_flag)) {
+        if (i >= kStages && !mbar_wait(&s.kv_empty[st], ((i / kStages) - 1) & 1, abort_flag, p.status)) {
           report(p.status, kErrTimeout);
           s.abort_flag = 1;
           break;
@@ -204,7 +204,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_q,
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------- MMA issuer ---
-    bool ok = mbar_wait(&s.q_full, 0, abort_flag) && mbar_wait(&s.k_full[0], 0, abort_flag);
+    bool ok = mbar_wait(&s.q_full, 0, abort_flag, p.status) && mbar_wait(&s.k_full[0], 0, abort_flag, p.status);
     bool issued_any = false;
     if (ok) {
       tc_fence_after();
@@ -227,7 +227,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_q,
     for (int i = 0; ok && i < ntiles; ++i) {
       const int st = i % kStages;
       const uint32_t ph = (i / kStages) & 1;
-      ok = mbar_wait(&s.p_full[0], i & 1, abort_flag) && mbar_wait(&s.v_full[st], ph, abort_flag);
+      ok = mbar_wait(&s.p_full[0], i & 1, abort_flag, p.status) && mbar_wait(&s.v_full[st], ph, abort_flag, p.status);
       if (!ok) break;
       if (i == 0 && (kt_hi + 1) * kTile > L) {
         // keys past the end of the sequence: their P is 0, but junk V could be NaN
@@ -251,7 +251,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_q,
       const bool more = i + 1 < ntiles;
       const int st1 = (i + 1) % kStages;
       if (more) {
-        ok = mbar_wait(&s.k_full[st1], ((i + 1) / kStages) & 1, abort_flag);
+        ok = mbar_wait(&s.k_full[st1], ((i + 1) / kStages) & 1, abort_flag, p.status);
         if (!ok) break;
         tc_fence_after();
         if (lane == 0) {
@@ -263,7 +263,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_q,
         __syncwarp();
       }
       if (has_b) {
-        ok = mbar_wait(&s.p_full[1], i & 1, abort_flag);
+        ok = mbar_wait(&s.p_full[1], i & 1, abort_flag, p.status);
         if (!ok) break;
         tc_fence_after();
         if (lane == 0) {
@@ -336,7 +336,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_q,
           }
           named_bar_sync(1 + grp, 128);
         }
-        if (!mbar_wait(&s.s_full[grp], i & 1, abort_flag)) { ok = false; break; }
+        if (!mbar_wait(&s.s_full[grp], i & 1, abort_flag, p.status)) { ok = false; break; }
         tc_fence_after();
         uint32_t sr[128];  // S row, then x = logit * log2 e, then packed bf16 P pairs
         tmem_ld32(tS + 0, sr);
@@ -418,7 +418,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_q,
         tc_fence_before();
         mbar_arrive(&s.p_full[grp]);
       }
-      if (ok) ok = mbar_wait(&s.o_full, 0, abort_flag);
+      if (ok) ok = mbar_wait(&s.o_full, 0, abort_flag, p.status);
       if (!ok) {
         report(p.status, kErrTimeout);
         s.abort_flag = 1;

@@ -59,14 +59,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 // Wait for the phase with the given parity to complete.  Gives up (returns false) when
-// `abort_flag` is raised by another warp or after kWaitBudgetCycles.
+// `abort_flag` is raised by another warp of the CTA, when the launch's global status word
+// (nullable) shows that some CTA has already failed, or after kWaitBudgetCycles.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
-                                          volatile int* abort_flag) {
+                                          volatile int* abort_flag,
+                                          const int* global_status = nullptr) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
+  uint32_t spins = 0;
   while (!mbar_try_wait(bar, parity)) {
     if (*abort_flag) return false;
-    if (clock64() - t0 > kWaitBudgetCycles) return false;
+    if ((++spins & 255u) == 0) {
+      if (global_status != nullptr && *reinterpret_cast<const volatile int*>(global_status) != 0)
+        return false;
+      if (clock64() - t0 > kWaitBudgetCycles) return false;
+    }
   }
   return true;
 }
