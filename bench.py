@@ -1,0 +1,423 @@
+"""Benchmark of the Inkling attention block on GB300.
+
+Default workload (one step = the whole hot path over one batch):
+  sliding-window prefill, B=4 sequences x 8192 new tokens, 32 query / 4 KV heads, head
+  dim 128, window 4096, relative-bias table [32 x 8192]:
+    inkling_sconv_kv      (K and V sconv into the paged bf16 cache, 512 channels)
+    inkling_rel_attn_prefill  (bf16 output)
+Metric: attention TFLOP/s counting only allowed (query, key) pairs, 4*D flops per pair
+per head (QK^T and PV).  Other workloads (--workload 1..5) print the same line shape;
+the decode ones report KV-read GB/s (algorithmic K/V bytes inside the causal/window range).
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload 2]
+Under torchrun (N > 1) every rank runs an independent replica (the path has no exchange
+step); value = work of all ranks / max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+METRIC = "prefill attn TFLOP/s and decode KV-read GB/s on 1 GB300; % of roofline"
+L2_FLUSH_BYTES = 512 << 20
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# --------------------------------------------------------------- algorithmic work ----
+def allowed_pairs(n: int, L: int, window: int) -> int:
+    """Number of (query, key) pairs with 0 <= p - j (<= window-1) for queries at
+    positions L-n .. L-1 (closed form per query, summed)."""
+    total = 0
+    for p in range(L - n, L):
+        keys = p + 1 if window <= 0 else min(p + 1, window)
+        total += keys
+    return total
+
+
+def attn_flops(spec: W.Spec) -> float:
+    pairs = sum(allowed_pairs(n, L, spec.window) for n, L in zip(spec.q_lens, spec.seq_lens))
+    return 4.0 * 128 * spec.hq * pairs
+
+
+def decode_kv_bytes(spec: W.Spec) -> float:
+    """K+V bytes of the keys any query of the step may see (union over the n new tokens),
+    per KV head: 2 * 128 * 2 bytes per key."""
+    total = 0
+    for n, L in zip(spec.q_lens, spec.seq_lens):
+        if n == 0:
+            continue
+        lo = 0 if spec.window <= 0 else max(0, L - n - spec.window + 1)
+        total += (L - lo) * spec.hkv * 2 * 128 * 2
+    return float(total)
+
+
+def is_decode(n: int) -> bool:
+    return n in (4, 5)
+
+
+def workload_spec(n: int, variant=None) -> W.Spec:
+    return W.config(n, variant=variant)
+
+
+def workload_name(spec: W.Spec) -> str:
+    return (f"{spec.name}: B={spec.batch} new={spec.max_q_len} L<={spec.max_seq_len} "
+            f"Hq={spec.hq} Hkv={spec.hkv} D=128 window={spec.window} R={spec.r}")
+
+
+# --------------------------------------------------------------------- clocks -------
+class ClockSampler:
+    """nvidia-smi clocks/throttle reasons sampled every 200 ms during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.gpu = str(device_index)
+        try:  # the physical GPU behind this process's device, whatever the visible-set order
+            self.gpu = "GPU-" + str(torch.cuda.get_device_properties(device_index).uuid)
+        except Exception:
+            pass
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+# ------------------------------------------------------------------ our arm ---------
+def run_ours(args, ws, rank, local):
+    import relative_position_gqa_gb300 as ink
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    ink._lib.load()  # raises if the CUDA library is missing: no fallback
+    spec = workload_spec(args.workload, args.variant)
+    decode = is_decode(args.workload)
+    g = W.make_case(spec, seed=args.workload + 1000 * rank, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = torch.empty(spec.total_q, spec.hq, 128, dtype=torch.bfloat16, device=dev)
+    state0 = g.state.clone()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    ws_bytes = 0
+    workspace = None
+    if decode:
+        ws_bytes = ink.decode_workspace_size(spec.batch, spec.hq, spec.hkv, spec.max_q_len,
+                                             spec.max_seq_len, spec.window)
+        workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def attn(q, o):
+        if decode:
+            ink.rel_attn_decode(q, g.k_cache, g.v_cache, g.block_table, g.cu_q_lens, g.seq_lens,
+                                g.bias, scale=spec.scale, window=spec.window,
+                                max_q_len=spec.max_q_len, max_seq_len=spec.max_seq_len, out=o,
+                                workspace=workspace, dev_status=status)
+        else:
+            ink.rel_attn_prefill(q, g.k_cache, g.v_cache, g.block_table, g.cu_q_lens,
+                                 g.seq_lens, g.bias, scale=spec.scale, window=spec.window,
+                                 max_q_len=spec.max_q_len, out=o, dev_status=status)
+
+    def sconv(kr, vr):
+        ink.sconv_kv(kr, vr, g.w_k, g.w_v, g.state, g.cu_q_lens, g.slot_mapping, g.k_cache,
+                     g.v_cache, max_q_len=spec.max_q_len, dev_status=status)
+
+    def reset():
+        g.state.copy_(state0)
+        flush.fill_(1.0)  # evict the previous step's data from L2
+
+    # ---- device-resident timing: per step, events around the step and around attention
+    for _ in range(args.warmup):
+        reset()
+        sconv(g.k_raw, g.v_raw)
+        attn(g.q, out)
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {ink.status_string(int(status.item()))}")
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        for i in range(args.steps):
+            reset()
+            ev[i][0].record(stream)
+            sconv(g.k_raw, g.v_raw)
+            ev[i][1].record(stream)
+            attn(g.q, out)
+            ev[i][2].record(stream)
+        torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {ink.status_string(int(status.item()))}")
+    step_ms = sum(a.elapsed_time(c) for a, _, c in ev) / args.steps
+    attn_ms = sum(b.elapsed_time(c) for _, b, c in ev) / args.steps
+    sconv_ms = sum(a.elapsed_time(b) for a, b, _ in ev) / args.steps
+
+    # ---- end to end through the public API with host buffers
+    host_in = [t.cpu().pin_memory() for t in (g.q, g.k_raw, g.v_raw)]
+    dev_in = [torch.empty_like(t, device=dev) for t in host_in]
+    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = host_out.numel() * host_out.element_size()
+    e2e_ev = []
+    for i in range(args.warmup + args.steps):
+        reset()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for d, h in zip(dev_in, host_in):
+            d.copy_(h, non_blocking=True)
+        sconv(dev_in[1], dev_in[2])
+        attn(dev_in[0], out)
+        host_out.copy_(out, non_blocking=True)
+        b.record(stream)
+        if i >= args.warmup:
+            e2e_ev.append((a, b))
+    torch.cuda.synchronize()
+    e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_ev) / len(e2e_ev)
+
+    # max over ranks
+    t = torch.tensor([step_ms, attn_ms, e2e_ms, sconv_ms], dtype=torch.float64, device=dev)
+    if ws > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    step_ms, attn_ms, e2e_ms, sconv_ms = t.tolist()
+
+    peaks, peak_src = measured_peaks()
+    if decode:
+        work = decode_kv_bytes(spec)
+        unit = "GB/s"
+        value = ws * work / (step_ms * 1e-3) / 1e9
+        e2e_value = ws * work / (e2e_ms * 1e-3) / 1e9
+        achieved = work / (attn_ms * 1e-3) / 1e9
+        peak = float(peaks["hbm_gbs"])
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": None,
+                "peak_source": f"{peak_src} hbm_gbs", "kernel": "decode_kernel (+combine)"}
+    else:
+        work = attn_flops(spec)
+        unit = "TFLOP/s"
+        value = ws * work / (step_ms * 1e-3) / 1e12
+        e2e_value = ws * work / (e2e_ms * 1e-3) / 1e12
+        achieved = work / (attn_ms * 1e-3) / 1e12
+        peak = float(peaks["bf16_tflops"])
+        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
+                "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
+                "peak_source": f"{peak_src} bf16_tflops (burst; kernel timed per launch)",
+                "kernel": "prefill_kernel"}
+    roof["traffic"] = args.traffic
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": unit, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) Q/K/V, N(0,0.5) sconv taps, N(0,sd) bias)",
+        "config": {"workload": workload_name(spec), "global_batch": spec.batch * ws,
+                   "seq_len": spec.max_seq_len, "parallelism": f"replicas x{ws}",
+                   "l2": "flushed (512 MB write) between timed steps",
+                   "attn_ms": round(attn_ms, 4), "sconv_ms": round(sconv_ms, 4)},
+        "e2e": {"value": round(e2e_value, 3), "unit": unit, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps * (2 + (1 if decode and ws_bytes > 0 else 0)),
+        "roofline": roof,
+        "clocks": clocks.summary(),
+    }
+    return line
+
+
+# ------------------------------------------------------------- oracle (CPU) arm -----
+def oracle_sample(spec: W.Spec, budget_s: float, seed: int):
+    """Time the fp64 oracle on a bounded sample of the workload: the sconv of every new
+    token of one sequence plus attention for a spread of query rows.  Returns
+    (work units done, seconds, description, cores)."""
+    import oracle
+    small_enough = (not spec.history_random) and spec.total_q * spec.hq < 3_000_000
+    case = W.make_case(spec, seed=seed, device="cpu") if small_enough else None
+    if case is None:
+        # only one sequence's worth, generated on the CPU
+        sub = W.Spec(**{**spec.__dict__, "batch": 1, "q_lens": [spec.q_lens[-1]],
+                        "seq_lens": [spec.seq_lens[-1]]})
+        case = W.make_case(sub, seed=seed, device="cpu")
+        spec = sub
+    cores = oracle.host_cores()
+    kc, vc, st = case.k_cache.clone(), case.v_cache.clone(), case.state.clone()
+    t0 = time.perf_counter()
+    oracle.sconv_kv(case.k_raw, case.v_raw, case.w_k, case.w_v, st, case.cu_q_lens,
+                    case.slot_mapping, kc, vc)
+    t_sconv = time.perf_counter() - t0
+    # attention rows: grow the sample until the time budget is used
+    T = spec.total_q
+    rows, done_pairs, t_attn = [], 0, 0.0
+    cu = case.cu_q_lens.tolist()
+    sl = case.seq_lens.tolist()
+    rng = torch.Generator().manual_seed(seed)
+    batch = max(cores, 8)
+    while t_attn < budget_s and len(rows) < T:
+        pick = torch.randint(0, T, (batch,), generator=rng).tolist()
+        t0 = time.perf_counter()
+        oracle.rel_attn(case.q, kc, vc, case.block_table, case.cu_q_lens, case.seq_lens,
+                        case.bias, scale=spec.scale, window=spec.window, rows=pick)
+        t_attn += time.perf_counter() - t0
+        for t in pick:
+            b = max(i for i in range(len(cu) - 1) if cu[i] <= t)
+            n, L = cu[b + 1] - cu[b], sl[b]
+            p = L - n + (t - cu[b])
+            done_pairs += (p + 1) if spec.window <= 0 else min(p + 1, spec.window)
+        rows += pick
+    return (done_pairs, t_attn, t_sconv, len(rows), cores, spec)
+
+
+def run_reference(args, ws, rank):
+    spec = workload_spec(args.workload, args.variant)
+    decode = is_decode(args.workload)
+    per_step = []
+    desc = None
+    for i in range(args.warmup + args.steps):
+        pairs, t_attn, t_sconv, nrows, cores, sspec = oracle_sample(
+            spec, budget_s=args.ref_seconds, seed=args.workload + i)
+        if i >= args.warmup:
+            per_step.append((pairs, t_attn, nrows))
+        desc = (f"fp64 C oracle on {cores} host threads: {nrows} random query rows x "
+                f"{sspec.hq} heads of the workload (plus one sequence's sconv, "
+                f"{t_sconv:.2f} s, not counted)")
+    pairs = sum(p for p, _, _ in per_step)
+    secs = sum(t for _, t, _ in per_step)
+    if decode:
+        # bytes of K/V the sampled rows read, per the same accounting as our arm
+        work = pairs * 2 * 128 * 2 / (spec.hq // spec.hkv)
+        unit = "GB/s"
+        value = work / secs / 1e9
+    else:
+        work = 4.0 * 128 * pairs
+        unit = "TFLOP/s"
+        value = work / secs / 1e12
+    ms = secs / len(per_step) * 1e3
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": unit, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": workload_name(spec)},
+        "cpu_baseline": {"value": value, "unit": unit, "cores": cores, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--variant", default=None, help="mtp_decode: swa|full; decode_1m: n1|n9")
+    ap.add_argument("--ref-seconds", type=float, default=6.0,
+                    help="oracle seconds per reference step / for the cpu_baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="DRAM bytes per launch of the dominant kernel from an ncu capture")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        if args.impl == "ours":
+            torch.cuda.set_device(local)
+        torch.distributed.init_process_group(backend=backend)
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, ws, rank)), flush=True)
+        if ws > 1:
+            torch.distributed.destroy_process_group()
+        return
+
+    line = run_ours(args, ws, rank, local)
+    if rank == 0 and not args.no_cpu_baseline:
+        spec = workload_spec(args.workload, args.variant)
+        pairs, t_attn, t_sconv, nrows, cores, sspec = oracle_sample(spec, args.ref_seconds,
+                                                                    seed=99)
+        if is_decode(args.workload):
+            v = pairs * 2 * 128 * 2 / (spec.hq // spec.hkv) / t_attn / 1e9
+            unit = "GB/s"
+        else:
+            v = 4.0 * 128 * pairs / t_attn / 1e12
+            unit = "TFLOP/s"
+        line["cpu_baseline"] = {
+            "value": v, "unit": unit, "cores": cores, "kind": "oracle",
+            "sample": f"{nrows} random query rows x {sspec.hq} heads (all allowed keys each), "
+                      f"fp64 C oracle, {t_attn:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -8,7 +8,10 @@
 // tensor memory (64 columns of bf16 pairs) and both contractions run on the tensor core:
 // S = Q K^T with Q from TMEM (TS form), O += P V with P from TMEM.
 //   warp 4      TMA producer: K/V pages of the split (three-stage ring of 64 KB).
-//   warp 5      MMA issuer; S is double-buffered so S(i+1) overlaps softmax(i).
+//   warp 5      MMA issuer; S is double-buffered so S(i+1) overlaps softmax(i).  Page i's
+//               "P ready" barrier is p_full[i & 1]: S(i+1) is issued before P(i) is
+//               consumed, so a fast warp may finish page i+1 while a slow one is still on
+//               page i, and one barrier for both pages would complete too early.
 //   warps 0-3   thread r owns packed row r: bias, mask, online softmax, P, epilogue.
 // TMEM columns: Q [0,64), S0 [128,256), S1 [256,384), O [384,512).
 // A sequence whose key range fits one split writes its output directly; otherwise every
@@ -41,7 +44,7 @@ struct __align__(1024) Smem {
   uint8_t v[kStages][2][16384];
   float bias[2][kMaxG * kBiasStride];
   uint64_t k_full[kStages], v_full[kStages], kv_empty[kStages];
-  uint64_t q_ready, s_full[2], p_full, pv_done, o_full, drain;
+  uint64_t q_ready, s_full[2], p_full[2], pv_done, o_full, drain;
   uint32_t tmem_base;
   int abort_flag;
   int bad_block;
@@ -106,6 +109,9 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
   const int pg0 = kt_lo + split * p.pages_per_split;
   const int np = min(p.pages_per_split, kt_hi + 1 - pg0);
   const int rows = n * p.G;
+  // softmax warps that own packed rows; the others sit out (their TMEM lanes hold rows
+  // nobody reads, and the MMA rows are independent of each other)
+  const int nact = ((rows + 31) / 32) * 32;
   const int32_t* table = p.block_table + (size_t)b * p.max_blocks;
 
   if (threadIdx.x == 0) {
@@ -128,10 +134,11 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
       mbar_init(&s.v_full[i], 1);
       mbar_init(&s.kv_empty[i], 1);
     }
-    mbar_init(&s.q_ready, 128);
+    mbar_init(&s.q_ready, nact);
     mbar_init(&s.s_full[0], 1);
     mbar_init(&s.s_full[1], 1);
-    mbar_init(&s.p_full, 128);
+    mbar_init(&s.p_full[0], nact);
+    mbar_init(&s.p_full[1], nact);
     mbar_init(&s.pv_done, 1);
     mbar_init(&s.o_full, 1);
     mbar_init(&s.drain, 1);
@@ -211,7 +218,7 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
         }
         __syncwarp();
       }
-      ok = mbar_wait(&s.p_full, i & 1, abort_flag, p.status) &&
+      ok = mbar_wait(&s.p_full[i & 1], (i >> 1) & 1, abort_flag, p.status) &&
            mbar_wait(&s.v_full[st], (i / kStages) & 1, abort_flag, p.status);
       if (!ok) break;
       const int kt = pg0 + i;
@@ -251,11 +258,10 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
       }
     }
     __syncwarp();
-  } else {
+  } else if (warp * 32 < rows) {
     // ------------------------------------------------------------ softmax group ---
-    const int r = threadIdx.x;  // 0..127
+    const int r = threadIdx.x;  // 0..nact-1
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    const bool warp_active = warp * 32 < rows;
     const bool valid = r < rows;
     const int t = valid ? r / p.G : 0;
     const int g = valid ? r % p.G : 0;
@@ -298,102 +304,100 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
       if (!clamped) {
         // head g': rev[j] = b[kvh*G + g'][clamp(dmax - j)] * log2 e, j < 127 + n
         const int span = 127 + n;
-        for (int e = r; e < p.G * span; e += 128) {
+        for (int e = r; e < p.G * span; e += nact) {
           const int gg = e / span, j = e % span;
           int d = dmax - j;
           d = d < 0 ? 0 : (d > R - 1 ? R - 1 : d);
           bias_buf[gg * kBiasStride + j] = __ldg(p.bias + (size_t)(kvh * p.G + gg) * R + d) * kLog2e;
         }
-        named_bar_sync(1, 128);
+        named_bar_sync(1, nact);
       }
       if (!mbar_wait(&s.s_full[i & 1], (i >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
       tc_fence_after();
       const uint32_t tS = tmem + lane_base + kColS0 + (i & 1) * 128;
-      if (warp_active) {
-        uint32_t sr[128];  // S row, then x = logit * log2 e, then packed bf16 P pairs
-        tmem_ld32(tS + 0, sr);
-        tmem_ld32(tS + 32, sr + 32);
-        tmem_ld32(tS + 64, sr + 64);
-        tmem_ld32(tS + 96, sr + 96);
-        tmem_wait_ld();
-        reg_fence<128>(sr);
-        if (clamped) {
+      uint32_t sr[128];  // S row, then x = logit * log2 e, then packed bf16 P pairs
+      tmem_ld32(tS + 0, sr);
+      tmem_ld32(tS + 32, sr + 32);
+      tmem_ld32(tS + 64, sr + 64);
+      tmem_ld32(tS + 96, sr + 96);
+      tmem_wait_ld();
+      reg_fence<128>(sr);
+      if (clamped) {
 #pragma unroll
-          for (int c = 0; c < 128; ++c)
-            sr[c] = __float_as_uint(fmaf(__uint_as_float(sr[c]), p.scale_log2, bconst));
-        } else {
-          const float* bp = bias_buf + g * kBiasStride + (n - 1 - t);
+        for (int c = 0; c < 128; ++c)
+          sr[c] = __float_as_uint(fmaf(__uint_as_float(sr[c]), p.scale_log2, bconst));
+      } else {
+        const float* bp = bias_buf + g * kBiasStride + (n - 1 - t);
 #pragma unroll
-          for (int c = 0; c < 128; ++c)
-            sr[c] = __float_as_uint(fmaf(__uint_as_float(sr[c]), p.scale_log2, bp[c]));
-        }
-        if (masked) {
-          const int d0 = pq - k0;
-#pragma unroll
-          for (int c = 0; c < 128; ++c) {
-            const int d = d0 - c;
-            const bool allowed = d >= 0 && (W == 0 || d <= W - 1);
-            sr[c] = allowed ? sr[c] : __float_as_uint(-INFINITY);
-          }
-        }
-        float mx0 = __uint_as_float(sr[0]), mx1 = __uint_as_float(sr[1]);
-        float mx2 = __uint_as_float(sr[2]), mx3 = __uint_as_float(sr[3]);
-#pragma unroll
-        for (int c = 4; c < 128; c += 4) {
-          mx0 = fmaxf(mx0, __uint_as_float(sr[c]));
-          mx1 = fmaxf(mx1, __uint_as_float(sr[c + 1]));
-          mx2 = fmaxf(mx2, __uint_as_float(sr[c + 2]));
-          mx3 = fmaxf(mx3, __uint_as_float(sr[c + 3]));
-        }
-        const float m_new = fmaxf(m, fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)));
-        const bool need = m_new > m + kRescaleThreshold || (m == -INFINITY && m_new > -INFINITY);
-        const float alpha = need ? ex2(m - m_new) : 1.f;
-        if (need) {
-          l *= alpha;
-          m = m_new;
-        }
-        const float m_use = m == -INFINITY ? 0.f : m;
-        float l0 = 0.f, l1 = 0.f;
-        // P pairs overwrite the registers they came from (index c/2 <= c)
-#pragma unroll
-        for (int c = 0; c < 128; c += 2) {
-          const float e0 = ex2(__uint_as_float(sr[c]) - m_use);
-          const float e1 = ex2(__uint_as_float(sr[c + 1]) - m_use);
-          l0 += e0;
-          l1 += e1;
-          sr[c / 2] = pack_bf16(e0, e1);
-        }
-        l += l0 + l1;
-        // rescale O (warp-wide, only when some row's max grew past the threshold)
-        if (__any_sync(0xffffffffu, need) && i > 0) {
-          // O must hold PV(i-1) before it is scaled
-          if (!mbar_wait(&s.pv_done, (i - 1) & 1, abort_flag, p.status)) ok = false;
-          tc_fence_after();
-          uint32_t orr[32];
-          const uint32_t tO = tmem + lane_base + kColO;
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            tmem_ld32(tO + c * 32, orr);
-            tmem_wait_ld();
-            reg_fence<32>(orr);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) orr[j] = __float_as_uint(__uint_as_float(orr[j]) * alpha);
-            tmem_st32(tO + c * 32, orr);
-          }
-        }
-        tmem_st32(tS + 0, sr);
-        tmem_st32(tS + 32, sr + 32);
-        tmem_wait_st();
+        for (int c = 0; c < 128; ++c)
+          sr[c] = __float_as_uint(fmaf(__uint_as_float(sr[c]), p.scale_log2, bp[c]));
       }
+      if (masked) {
+        const int d0 = pq - k0;
+#pragma unroll
+        for (int c = 0; c < 128; ++c) {
+          const int d = d0 - c;
+          const bool allowed = d >= 0 && (W == 0 || d <= W - 1);
+          sr[c] = allowed ? sr[c] : __float_as_uint(-INFINITY);
+        }
+      }
+      float mx0 = __uint_as_float(sr[0]), mx1 = __uint_as_float(sr[1]);
+      float mx2 = __uint_as_float(sr[2]), mx3 = __uint_as_float(sr[3]);
+#pragma unroll
+      for (int c = 4; c < 128; c += 4) {
+        mx0 = fmaxf(mx0, __uint_as_float(sr[c]));
+        mx1 = fmaxf(mx1, __uint_as_float(sr[c + 1]));
+        mx2 = fmaxf(mx2, __uint_as_float(sr[c + 2]));
+        mx3 = fmaxf(mx3, __uint_as_float(sr[c + 3]));
+      }
+      const float m_new = fmaxf(m, fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)));
+      const bool need = m_new > m + kRescaleThreshold || (m == -INFINITY && m_new > -INFINITY);
+      const float alpha = need ? ex2(m - m_new) : 1.f;
+      if (need) {
+        l *= alpha;
+        m = m_new;
+      }
+      const float m_use = m == -INFINITY ? 0.f : m;
+      float l0 = 0.f, l1 = 0.f;
+      // P pairs overwrite the registers they came from (index c/2 <= c)
+#pragma unroll
+      for (int c = 0; c < 128; c += 2) {
+        const float e0 = ex2(__uint_as_float(sr[c]) - m_use);
+        const float e1 = ex2(__uint_as_float(sr[c + 1]) - m_use);
+        l0 += e0;
+        l1 += e1;
+        sr[c / 2] = pack_bf16(e0, e1);
+      }
+      l += l0 + l1;
+      // rescale O (warp-wide, only when some row's max grew past the threshold)
+      if (__any_sync(0xffffffffu, need) && i > 0) {
+        // O must hold PV(i-1) before it is scaled
+        if (!mbar_wait(&s.pv_done, (i - 1) & 1, abort_flag, p.status)) ok = false;
+        tc_fence_after();
+        uint32_t orr[32];
+        const uint32_t tO = tmem + lane_base + kColO;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          tmem_ld32(tO + c * 32, orr);
+          tmem_wait_ld();
+          reg_fence<32>(orr);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) orr[j] = __float_as_uint(__uint_as_float(orr[j]) * alpha);
+          tmem_st32(tO + c * 32, orr);
+        }
+      }
+      tmem_st32(tS + 0, sr);
+      tmem_st32(tS + 32, sr + 32);
+      tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&s.p_full);
+      mbar_arrive(&s.p_full[i & 1]);
       if (!ok) break;
     }
     if (ok) ok = mbar_wait(&s.o_full, 0, abort_flag, p.status);
     if (!ok) {
       report(p.status, kErrTimeout);
       s.abort_flag = 1;
-    } else if (warp_active) {
+    } else {
       tc_fence_after();
       const uint32_t tO = tmem + lane_base + kColO;
       const bool direct = nsplit_b == 1;
