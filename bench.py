@@ -291,19 +291,22 @@ def run_ours(args, ws, rank, local):
 
 
 # ------------------------------------------------------------- oracle (CPU) arm -----
-def oracle_sample(spec: W.Spec, budget_s: float, seed: int):
-    """Time the fp64 oracle on a bounded sample of the workload: the sconv of every new
-    token of one sequence plus attention for a spread of query rows.  Returns
-    (work units done, seconds, description, cores)."""
-    import oracle
+def oracle_case(spec: W.Spec, seed: int):
+    """The CPU input set the oracle is timed on: the whole workload when it is small and
+    has no random cache history, else its last sequence alone."""
     small_enough = (not spec.history_random) and spec.total_q * spec.hq < 3_000_000
-    case = W.make_case(spec, seed=seed, device="cpu") if small_enough else None
-    if case is None:
-        # only one sequence's worth, generated on the CPU
-        sub = W.Spec(**{**spec.__dict__, "batch": 1, "q_lens": [spec.q_lens[-1]],
-                        "seq_lens": [spec.seq_lens[-1]]})
-        case = W.make_case(sub, seed=seed, device="cpu")
-        spec = sub
+    if not small_enough:
+        spec = W.Spec(**{**spec.__dict__, "batch": 1, "q_lens": [spec.q_lens[-1]],
+                         "seq_lens": [spec.seq_lens[-1]]})
+    return spec, W.make_case(spec, seed=seed, device="cpu")
+
+
+def oracle_sample(spec: W.Spec, case, budget_s: float, seed: int):
+    """Time the fp64 oracle on a bounded sample of the workload: the sconv of every new
+    token of `case` plus attention for seeded random query rows until `budget_s` of
+    attention time is used.  Returns (allowed pairs done, attention seconds, sconv
+    seconds, rows, cores, spec)."""
+    import oracle
     cores = oracle.host_cores()
     kc, vc, st = case.k_cache.clone(), case.v_cache.clone(), case.state.clone()
     t0 = time.perf_counter()
@@ -337,9 +340,10 @@ def run_reference(args, ws, rank):
     decode = is_decode(args.workload)
     per_step = []
     desc = None
+    sspec, case = oracle_case(spec, seed=args.workload)
     for i in range(args.warmup + args.steps):
         pairs, t_attn, t_sconv, nrows, cores, sspec = oracle_sample(
-            spec, budget_s=args.ref_seconds, seed=args.workload + i)
+            sspec, case, budget_s=args.ref_seconds, seed=args.workload + i)
         if i >= args.warmup:
             per_step.append((pairs, t_attn, nrows))
         desc = (f"fp64 C oracle on {cores} host threads: {nrows} random query rows x "
@@ -401,8 +405,9 @@ def main():
     line = run_ours(args, ws, rank, local)
     if rank == 0 and not args.no_cpu_baseline:
         spec = workload_spec(args.workload, args.variant)
-        pairs, t_attn, t_sconv, nrows, cores, sspec = oracle_sample(spec, args.ref_seconds,
-                                                                    seed=99)
+        sspec, case = oracle_case(spec, seed=args.workload)
+        pairs, t_attn, t_sconv, nrows, cores, sspec = oracle_sample(sspec, case,
+                                                                    args.ref_seconds, seed=99)
         if is_decode(args.workload):
             v = pairs * 2 * 128 * 2 / (spec.hq // spec.hkv) / t_attn / 1e9
             unit = "GB/s"

@@ -60,7 +60,8 @@ def test_split_count_invariance(ink):
     spec = W.small(q_lens=(9, 1), seq_lens=(3000, 2500), hq=8, hkv=1, r=4000)
     outs = [_run(ink, spec, seed=63, num_splits=n)[1] for n in (1, 2, 5, 24, 0)]
     for o in outs[1:]:
-        assert (o - outs[0]).abs().max().item() <= 2e-3
+        d = (o - outs[0]).abs()
+        assert d.max().item() <= 1e-2 and d.mean().item() <= 1e-3
 
 
 def test_token_by_token_decode_equals_prefill(ink):
@@ -92,10 +93,16 @@ def test_token_by_token_decode_equals_prefill(ink):
                                  out=out, lse=lse, dev_status=st)
         torch.cuda.synchronize()
         assert int(st.item()) == 0
-        assert (out - ref[sl]).abs().max().item() <= 2e-3
+        # both sides carry their own bf16 rounding of P: hold them to the parity bar
+        d = (out - ref[sl]).abs()
+        assert d.max().item() <= 1e-2 and d.mean().item() <= 1e-3
         assert (lse - ref_lse[sl]).abs().max().item() <= 1e-3
         start += n
     assert torch.equal(full.k_cache.view(torch.int16), ref_case.k_cache.view(torch.int16))
+    # and the one-shot rows against the oracle
+    snap = snapshot(W.make_case(spec, seed=64, device="cuda"))
+    _, _, _, o_ref, o_lse = run_oracle(snap)
+    compare_out(ref, ref_lse, o_ref, o_lse, snap.tok_index)
 
 
 def test_decode_workspace_too_small(ink):
