@@ -42,7 +42,17 @@ namespace prefill {
 
 constexpr int kTile = 128;
 constexpr int kStages = 2;
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;  // three warpgroups: softmax A, softmax B, producer/MMA
+// Register split (setmaxnreg): the kernel is built for 168 registers a thread at launch
+// (65536 / 384, rounded down to 8), i.e. 64512 for the CTA.  The producer/MMA warpgroup
+// gives back down to 64 and each softmax warpgroup grows to 216: 2*128*216 + 128*64 =
+// 63488 <= 64512.  The host refuses to launch unless the built register count is 168,
+// since an increase that the launch cannot cover would wait forever.
+constexpr int kLaunchRegs = 168;
+constexpr int kSoftmaxRegs = 216;
+constexpr int kOtherRegs = 64;
+static_assert(2 * 128 * kSoftmaxRegs + 128 * kOtherRegs <= kThreads * kLaunchRegs,
+              "register split exceeds the launch allocation");
 constexpr int kBiasCopy = 264;  // floats per shifted copy; 264/4 = 66 = 2 (mod 8) spreads banks
 constexpr uint32_t kIdescQK = idesc_bf16(128, 128, false, false);
 constexpr uint32_t kIdescPV = idesc_bf16(128, 128, false, true);
@@ -161,7 +171,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_q,
   const uint32_t tmem = s.tmem_base;
   volatile int* abort_flag = &s.abort_flag;
 
-  if (warp == 8) {
+  if (warp >= 8) {
+   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kOtherRegs));
+   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer ---
     if (lane == 0) {
       tma_prefetch_desc(&map_q);
@@ -300,7 +312,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_q,
       }
     }
     __syncwarp();
+   }
   } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
     // ------------------------------------------------------------ softmax groups ---
     const int grp = warp >> 2;  // 0 = head A, 1 = head B
     const int r = threadIdx.x & 127;
@@ -314,90 +328,120 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_q,
       const int R = p.R, W = p.window;
       const int sh = (127 - r) & 3;
       const int base = (127 - r) - sh;
-      float m = -INFINITY, l = 0.f;
+      float m = -INFINITY;
+      float2 l2 = make_float2(0.f, 0.f);
+      const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
       bool ok = true;
+      // this thread's two staged bias values for a tile: rev[j], j = r and r + 128, with
+      // rev[j] = b[h][clamp(delta + 127 - j)] * log2 e.  Loaded one tile ahead.
+      auto load_rev = [&](int i, float& v0, float& v1) {
+        const int delta = P0 - (kt_hi - i) * kTile;
+        int d0 = delta + 127 - r, d1 = d0 - 128;
+        d0 = d0 < 0 ? 0 : (d0 > R - 1 ? R - 1 : d0);
+        d1 = d1 < 0 ? 0 : (d1 > R - 1 ? R - 1 : d1);
+        v0 = __ldg(brow + d0);
+        v1 = __ldg(brow + d1);
+      };
+      float nv0 = 0.f, nv1 = 0.f;
+      if (ntiles > 0 && !(P0 - kt_hi * kTile - 127 >= R - 1)) load_rev(0, nv0, nv1);
       for (int i = 0; i < ntiles; ++i) {
         const int k0 = (kt_hi - i) * kTile;
         const int delta = P0 - k0;
+        // tiles are visited with growing distance, so clamped tiles form a suffix and
+        // every unclamped tile stages (and synchronises) before any clamped one
         const bool clamped = delta - 127 >= R - 1;
         const bool masked = (delta < 127) || (W > 0 && delta + 127 > W - 1) || (k0 + 127 >= L);
         float* bias_buf = &s.bias[grp][i & 1][0][0];
         if (!clamped) {
-          // rev[j] = b[h][clamp(delta + 127 - j)] * log2 e, j = 0..255;  copy_q[j - q] = rev[j]
+          // four copies shifted by one float: copy_q[j - q] = rev[j]
+          const float v[2] = {nv0 * kLog2e, nv1 * kLog2e};
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
             const int j = r + 128 * u;
-            int d = delta + 127 - j;
-            d = d < 0 ? 0 : (d > R - 1 ? R - 1 : d);
-            const float v = __ldg(brow + d) * kLog2e;
 #pragma unroll
             for (int q = 0; q < 4; ++q)
-              if (j - q >= 0) bias_buf[q * kBiasCopy + j - q] = v;
+              if (j - q >= 0) bias_buf[q * kBiasCopy + j - q] = v[u];
           }
+          if (i + 1 < ntiles && !(delta + kTile - 127 >= R - 1)) load_rev(i + 1, nv0, nv1);
           named_bar_sync(1 + grp, 128);
         }
         if (!mbar_wait(&s.s_full[grp], i & 1, abort_flag, p.status)) { ok = false; break; }
         tc_fence_after();
-        uint32_t sr[128];  // S row, then x = logit * log2 e, then packed bf16 P pairs
+        // S row in two halves: the second half's TMEM load overlaps work on the first
+        uint32_t sr[128];
         tmem_ld32(tS + 0, sr);
         tmem_ld32(tS + 32, sr + 32);
+        tmem_wait_ld();
+        reg_fence<64>(sr);
         tmem_ld32(tS + 64, sr + 64);
         tmem_ld32(tS + 96, sr + 96);
+        float2 x[64];  // logit * log2 e, pairs of columns
+        const float4* bp = reinterpret_cast<const float4*>(bias_buf + sh * kBiasCopy + base);
+        const float2 bc2 = make_float2(bconst, bconst);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          const float2 sv = make_float2(__uint_as_float(sr[2 * k]), __uint_as_float(sr[2 * k + 1]));
+          if (clamped) {
+            x[k] = __ffma2_rn(sv, sc2, bc2);
+          } else {
+            const float4 bv = bp[k >> 1];
+            x[k] = __ffma2_rn(sv, sc2, (k & 1) ? make_float2(bv.z, bv.w) : make_float2(bv.x, bv.y));
+          }
+        }
         tmem_wait_ld();
-        reg_fence<128>(sr);
-        if (clamped) {
+        reg_fence<64>(sr + 64);
 #pragma unroll
-          for (int c = 0; c < 128; ++c)
-            sr[c] = __float_as_uint(fmaf(__uint_as_float(sr[c]), p.scale_log2, bconst));
-        } else {
-          const float4* bp = reinterpret_cast<const float4*>(bias_buf + sh * kBiasCopy + base);
-#pragma unroll
-          for (int g = 0; g < 32; ++g) {
-            const float4 bv = bp[g];
-            sr[4 * g + 0] = __float_as_uint(fmaf(__uint_as_float(sr[4 * g + 0]), p.scale_log2, bv.x));
-            sr[4 * g + 1] = __float_as_uint(fmaf(__uint_as_float(sr[4 * g + 1]), p.scale_log2, bv.y));
-            sr[4 * g + 2] = __float_as_uint(fmaf(__uint_as_float(sr[4 * g + 2]), p.scale_log2, bv.z));
-            sr[4 * g + 3] = __float_as_uint(fmaf(__uint_as_float(sr[4 * g + 3]), p.scale_log2, bv.w));
+        for (int k = 32; k < 64; ++k) {
+          const float2 sv = make_float2(__uint_as_float(sr[2 * k]), __uint_as_float(sr[2 * k + 1]));
+          if (clamped) {
+            x[k] = __ffma2_rn(sv, sc2, bc2);
+          } else {
+            const float4 bv = bp[k >> 1];
+            x[k] = __ffma2_rn(sv, sc2, (k & 1) ? make_float2(bv.z, bv.w) : make_float2(bv.x, bv.y));
           }
         }
         if (masked) {
           const int dr = delta + r;  // distance at column 0
           const int kend = L - k0;   // columns >= kend are past the sequence
 #pragma unroll
-          for (int c = 0; c < 128; ++c) {
+          for (int k = 0; k < 64; ++k) {
+            const int c = 2 * k;
             const int d = dr - c;
-            const bool allowed = d >= 0 && (W == 0 || d <= W - 1) && c < kend;
-            sr[c] = allowed ? sr[c] : __float_as_uint(-INFINITY);
+            const bool a0 = d >= 0 && (W == 0 || d <= W - 1) && c < kend;
+            const bool a1 = d - 1 >= 0 && (W == 0 || d - 1 <= W - 1) && c + 1 < kend;
+            x[k].x = a0 ? x[k].x : -INFINITY;
+            x[k].y = a1 ? x[k].y : -INFINITY;
           }
         }
-        float mx0 = __uint_as_float(sr[0]), mx1 = __uint_as_float(sr[1]);
-        float mx2 = __uint_as_float(sr[2]), mx3 = __uint_as_float(sr[3]);
+        float mx0 = fmax3(x[0].x, x[0].y, x[1].x), mx1 = fmax3(x[1].y, x[2].x, x[2].y);
+        float mx2 = fmax3(x[3].x, x[3].y, x[4].x), mx3 = fmax3(x[4].y, x[5].x, x[5].y);
 #pragma unroll
-        for (int c = 4; c < 128; c += 4) {
-          mx0 = fmaxf(mx0, __uint_as_float(sr[c]));
-          mx1 = fmaxf(mx1, __uint_as_float(sr[c + 1]));
-          mx2 = fmaxf(mx2, __uint_as_float(sr[c + 2]));
-          mx3 = fmaxf(mx3, __uint_as_float(sr[c + 3]));
+        for (int k = 6; k < 62; k += 4) {
+          mx0 = fmax3(mx0, x[k].x, x[k].y);
+          mx1 = fmax3(mx1, x[k + 1].x, x[k + 1].y);
+          mx2 = fmax3(mx2, x[k + 2].x, x[k + 2].y);
+          mx3 = fmax3(mx3, x[k + 3].x, x[k + 3].y);
         }
-        const float m_new = fmaxf(m, fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)));
+        mx0 = fmax3(mx0, x[62].x, x[62].y);
+        mx1 = fmax3(mx1, x[63].x, x[63].y);
+        const float m_new = fmax3(m, fmaxf(mx0, mx1), fmaxf(mx2, mx3));
         const bool need = m_new > m + kRescaleThreshold || (m == -INFINITY && m_new > -INFINITY);
         const float alpha = need ? ex2(m - m_new) : 1.f;
         if (need) {
-          l *= alpha;
+          l2.x *= alpha;
+          l2.y *= alpha;
           m = m_new;
         }
         const float m_use = m == -INFINITY ? 0.f : m;
-        float l0 = 0.f, l1 = 0.f;
-        // P pairs overwrite the registers they came from (index c/2 <= c)
+        const float2 nm2 = make_float2(-m_use, -m_use);
+        // P as bf16 pairs, reusing the S registers
 #pragma unroll
-        for (int c = 0; c < 128; c += 2) {
-          const float e0 = ex2(__uint_as_float(sr[c]) - m_use);
-          const float e1 = ex2(__uint_as_float(sr[c + 1]) - m_use);
-          l0 += e0;
-          l1 += e1;
-          sr[c / 2] = pack_bf16(e0, e1);
+        for (int k = 0; k < 64; ++k) {
+          const float2 d2 = __fadd2_rn(x[k], nm2);
+          const float2 e2 = make_float2(ex2(d2.x), ex2(d2.y));
+          l2 = __fadd2_rn(l2, e2);
+          sr[k] = pack_bf16(e2.x, e2.y);
         }
-        l += l0 + l1;
         // rescale O (warp-wide, only when some row's max grew past the threshold)
         if (__any_sync(0xffffffffu, need) && i > 0) {
           // PV(i-1) was issued before S(i), so it is complete here
@@ -418,6 +462,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_q,
         tc_fence_before();
         mbar_arrive(&s.p_full[grp]);
       }
+      const float l = l2.x + l2.y;
       if (ok) ok = mbar_wait(&s.o_full, 0, abort_flag, p.status);
       if (!ok) {
         report(p.status, kErrTimeout);
@@ -502,6 +547,10 @@ cudaError_t launch_prefill(const AttnArgs& a, const AttnMaps& maps, cudaStream_t
   cudaError_t e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
+  cudaFuncAttributes fa;
+  e = cudaFuncGetAttributes(&fa, prefill_kernel);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;  // see kLaunchRegs
   prefill_kernel<<<(unsigned)grid, kThreads, smem, stream>>>(maps.q, maps.k, maps.v, p);
   return cudaGetLastError();
 }

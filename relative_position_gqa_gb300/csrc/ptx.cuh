@@ -240,6 +240,13 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// max of three floats in one instruction (sm_100+)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   uint32_t r;
   // cvt packs its first source into the upper half

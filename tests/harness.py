@@ -6,9 +6,9 @@ Parity bars (fixed by the block's specification: bf16 inputs, fp32 accumulation)
   attention output (bf16 out mode): |err| <= max(1e-2, half a bf16 ulp of the oracle
     value) + 1e-3 (the output rounding alone can exceed 1e-2 for |o| >= 4);
   lse: |err| <= 1e-3;
-  sconv output in the cache: within one bf16 ulp of the oracle (fp32 vs fp64 sums can
-    round to neighbouring bf16 values near a tie); every other cache slot and the sconv
-    state bit-exact.
+  sconv output in the cache: |gpu - oracle| <= ulp_bf16(oracle) + 2^-21 * sum_j |w_j x_j|
+    (the fp32 sum's rounding error; near-cancelling sums can differ by many ulps of their
+    small result); every other cache slot and the sconv state bit-exact.
 """
 from __future__ import annotations
 
@@ -120,15 +120,51 @@ def bf16_bits(t: torch.Tensor) -> np.ndarray:
     return t.contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
 
 
-def assert_cache_matches(gpu_cache: torch.Tensor, ora_cache: torch.Tensor, snap: Snapshot):
-    """The snapshot's pages of the GPU cache vs the oracle's: <= 1 ulp, mostly exact."""
-    g = bf16_bits(gpu_cache.index_select(0, snap.page_index.to(gpu_cache.device)))
-    o = bf16_bits(ora_cache)
-    d = np.abs(_order_key(g) - _order_key(o))
-    assert d.max() <= 1, f"cache differs by {d.max()} ulp"
-    frac = (d > 0).mean()
-    assert frac < 1e-3, f"{frac:.2e} of cache values differ by one ulp"
-    return frac
+def _sconv_magnitude(c: W.Case, which: int) -> torch.Tensor:
+    """S[t, c] = sum_j |w[c, j]| * |x~[t + j, c]| for every new token (snapshot order):
+    the scale of the fp32 rounding error of the conv sum."""
+    w = (c.w_k if which == 0 else c.w_v).abs().float()
+    raw = (c.k_raw if which == 0 else c.v_raw).float().abs()
+    cu = c.cu_q_lens.tolist()
+    out = []
+    for b in range(len(cu) - 1):
+        n = cu[b + 1] - cu[b]
+        ext = torch.cat([c.state[b, which].float().abs(), raw[cu[b]:cu[b + 1]]])
+        acc = torch.zeros(n, ext.shape[1])
+        for j in range(4):
+            acc += w[:, j] * ext[j:j + n]
+        out.append(acc)
+    return torch.cat(out) if out else torch.zeros(0, w.shape[0])
+
+
+def assert_cache_matches(gpu_cache: torch.Tensor, ora_cache: torch.Tensor, snap: Snapshot,
+                         which: int):
+    """The snapshot's pages of the GPU cache vs the oracle's.
+
+    Slots of the new tokens hold the conv output: the GPU sums four products in fp32
+    (four roundings, |error| <= 4 * 2^-24 * S with S = sum |w x|), the oracle in fp64, and
+    each result is rounded once to bf16, so |gpu - oracle| <= ulp_bf16(oracle) + 2^-21 * S.
+    Every other slot must be untouched: bit-exact."""
+    c = snap.case
+    g = gpu_cache.index_select(0, snap.page_index.to(gpu_cache.device)).cpu()
+    o = ora_cache.clone()
+    slots = c.slot_mapping
+    keep = slots >= 0
+    blk, off = slots[keep] // 128, slots[keep] % 128
+    n = int(keep.sum())
+    gv = g[blk, :, off, :].reshape(n, -1).double()
+    ov = o[blk, :, off, :].reshape(n, -1).double()
+    S = _sconv_magnitude(c, which)[keep].double()
+    ulp = torch.exp2(torch.floor(torch.log2(ov.abs().clamp_min(2.0 ** -126))) - 7)
+    bad = (gv - ov).abs() > ulp + 2.0 ** -21 * S
+    assert not bad.any(), f"{int(bad.sum())} conv outputs outside the fp32 rounding bound"
+    differ = float((gv != ov).double().mean()) if n else 0.0
+    assert differ < 1e-3, f"{differ:.2e} of conv outputs differ from the oracle"
+    # everything that is not a new token's slot: bit-exact
+    g[blk, :, off, :] = 0
+    o[blk, :, off, :] = 0
+    assert torch.equal(g.view(torch.int16), o.view(torch.int16)), "untouched cache slots differ"
+    return differ
 
 
 def assert_state_matches(gpu_state: torch.Tensor, ora_state: torch.Tensor, snap: Snapshot):

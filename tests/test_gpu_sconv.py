@@ -42,8 +42,8 @@ def test_sconv_matches_oracle(ink, kw):
     torch.cuda.synchronize()
     assert int(st.item()) == 0
     kc, vc, state, _, _ = run_oracle(snap, rows=[])
-    assert_cache_matches(g.k_cache, kc, snap)
-    assert_cache_matches(g.v_cache, vc, snap)
+    assert_cache_matches(g.k_cache, kc, snap, 0)
+    assert_cache_matches(g.v_cache, vc, snap, 1)
     assert_state_matches(g.state, state, snap)
 
 

@@ -42,8 +42,8 @@ def _check(ink, wl, seqs, per_seq, *, decode, variant=None, out_dtype=torch.floa
     assert int(st.item()) == 0, ink.status_string(int(st.item()))
     rows = _rows(snap, per_seq)
     kc, vc, state, ref, ref_lse = run_oracle(snap, rows=rows)
-    assert_cache_matches(g.k_cache, kc, snap)
-    assert_cache_matches(g.v_cache, vc, snap)
+    assert_cache_matches(g.k_cache, kc, snap, 0)
+    assert_cache_matches(g.v_cache, vc, snap, 1)
     assert_state_matches(g.state, state, snap)
     tok = snap.tok_index[torch.tensor(rows, dtype=torch.long)]
     return compare_out(out, lse, ref, ref_lse, tok)
