@@ -7,7 +7,8 @@
 // and G = 8), so each K/V page is read from HBM once per KV head.  The packed Q lives in
 // tensor memory (64 columns of bf16 pairs) and both contractions run on the tensor core:
 // S = Q K^T with Q from TMEM (TS form), O += P V with P from TMEM.
-//   warp 4      TMA producer: K/V pages of the split (three-stage ring of 64 KB).
+//   warp 4      TMA producer: K/V pages of the split (three-stage ring of 64 KB); its
+//               lanes also cp.async each page's bias slices (G heads) into the ring.
 //   warp 5      MMA issuer; S is double-buffered so S(i+1) overlaps softmax(i).  Page i's
 //               "P ready" barrier is p_full[i & 1]: S(i+1) is issued before P(i) is
 //               consumed, so a fast warp may finish page i+1 while a slow one is still on
@@ -16,7 +17,7 @@
 // TMEM columns: Q [0,64), S0 [128,256), S1 [256,384), O [384,512).
 // A sequence whose key range fits one split writes its output directly; otherwise every
 // split writes (m, l, unnormalised O) to the workspace and combine_kernel merges them:
-//   O = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s,  M = max_s m_s   (log2 domain).
+//   O = sum_s e^(m_s - M) O_s / sum_s e^(m_s - M) l_s,  M = max_s m_s.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -36,14 +37,14 @@ constexpr uint32_t kIdescQK = idesc_bf16(128, 128, false, false);
 constexpr uint32_t kIdescPV = idesc_bf16(128, 128, false, true);
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr float kRescaleThreshold = 8.0f;
+constexpr float kRescaleThreshold = 5.545177444479562f;  // 8 ln 2: rescale O past 256x growth
 constexpr uint32_t kColQ = 0, kColS0 = 128, kColO = 384;
 
 struct __align__(1024) Smem {
   uint8_t k[kStages][2][16384];
   uint8_t v[kStages][2][16384];
-  float bias[2][kMaxG * kBiasStride];
-  uint64_t k_full[kStages], v_full[kStages], kv_empty[kStages];
+  float bias[kStages][kMaxG * kBiasStride];  // raw table values, staged per page by the TMA warp
+  uint64_t k_full[kStages], v_full[kStages], kv_empty[kStages], b_full[kStages];
   uint64_t q_ready, s_full[2], p_full[2], pv_done, o_full, drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -64,7 +65,7 @@ struct Params {
   int max_blocks, R, window, out_dtype;
   int B, T, Hq, Hkv, G, max_q_len, rmax, num_splits, pages_per_split;
   long long num_blocks;
-  float scale_log2;
+  float scale;
 };
 
 // Key pages a sequence's decode rows can see: [kt_lo, kt_hi].
@@ -133,6 +134,7 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
       mbar_init(&s.k_full[i], 1);
       mbar_init(&s.v_full[i], 1);
       mbar_init(&s.kv_empty[i], 1);
+      mbar_init(&s.b_full[i], 32);
     }
     mbar_init(&s.q_ready, nact);
     mbar_init(&s.s_full[0], 1);
@@ -156,18 +158,30 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
 
   if (warp == 4) {
     // ------------------------------------------------------------ TMA producer ---
+    // Lane 0 issues the K/V page loads; all 32 lanes stage the page's bias slice with
+    // 4-byte cp.async copies (no register round trip) and arrive on b_full[stage] when
+    // their copies land.  The warp runs up to kStages pages ahead of the softmax.
+    const uint64_t pol = l2_policy_evict_first();
     if (lane == 0) {
       tma_prefetch_desc(&map_k);
       tma_prefetch_desc(&map_v);
-      const uint64_t pol = l2_policy_evict_first();
-      int issued = 0;
-      for (int i = 0; i < np; ++i) {
-        const int st = i % kStages;
-        if (i >= kStages && !mbar_wait(&s.kv_empty[st], ((i / kStages) - 1) & 1, abort_flag, p.status)) {
+    }
+    const int R = p.R, span = 127 + n;
+    int issued = 0;
+    for (int i = 0; i < np; ++i) {
+      const int st = i % kStages;
+      int ok = 1;
+      if (lane == 0 && i >= kStages)
+        ok = mbar_wait(&s.kv_empty[st], ((i / kStages) - 1) & 1, abort_flag, p.status);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) {
+        if (lane == 0) {
           report(p.status, kErrTimeout);
           s.abort_flag = 1;
-          break;
         }
+        break;
+      }
+      if (lane == 0) {
         const int page = table[pg0 + i] * p.Hkv + kvh;
         mbar_arrive_expect_tx(&s.k_full[st], 32768u);
         tma_load_3d_hint(s.k[st][0], &map_k, &s.k_full[st], 0, 0, page, pol);
@@ -175,16 +189,30 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
         mbar_arrive_expect_tx(&s.v_full[st], 32768u);
         tma_load_3d_hint(s.v[st][0], &map_v, &s.v_full[st], 0, 0, page, pol);
         tma_load_3d_hint(s.v[st][1], &map_v, &s.v_full[st], 64, 0, page, pol);
-        issued = i + 1;
       }
-      if (*abort_flag) {
-        for (int i = max(0, issued - kStages); i < issued; ++i) {
-          const int st = i % kStages;
-          const uint32_t ph = (i / kStages) & 1;
-          volatile int never = 0;
-          mbar_wait(&s.k_full[st], ph, &never);
-          mbar_wait(&s.v_full[st], ph, &never);
+      const int k0 = (pg0 + i) * 128;
+      const int dmax = (L - 1) - k0;                 // largest distance in the page
+      if ((L - n) - k0 - 127 < R - 1) {              // not every distance clamped
+        // head g: slot j holds b[kvh*G + g][clamp(dmax - j, 0, R-1)], j < 127 + n
+        float* dst = s.bias[st];
+        for (int e = lane; e < p.G * span; e += 32) {
+          const int gg = e / span, j = e % span;
+          int d = dmax - j;
+          d = d < 0 ? 0 : (d > R - 1 ? R - 1 : d);
+          cp_async_4(dst + gg * kBiasStride + j, p.bias + (size_t)(kvh * p.G + gg) * R + d);
         }
+      }
+      cp_async_mbar_arrive(&s.b_full[st]);
+      issued = i + 1;
+    }
+    if (lane == 0 && *abort_flag) {
+      for (int i = max(0, issued - kStages); i < issued; ++i) {
+        const int st = i % kStages;
+        const uint32_t ph = (i / kStages) & 1;
+        volatile int never = 0;
+        mbar_wait(&s.k_full[st], ph, &never);
+        mbar_wait(&s.v_full[st], ph, &never);
+        mbar_wait(&s.b_full[st], ph, &never);
       }
     }
   } else if (warp == 5) {
@@ -290,7 +318,7 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
 
     const float* brow = p.bias + (size_t)h * p.R;
     const int R = p.R, W = p.window;
-    const float bconst = __ldg(brow + R - 1) * kLog2e;
+    const float bconst = __ldg(brow + R - 1);
     const int pq = L - n + t;  // position of this row's token
     float m = -INFINITY, l = 0.f;
     bool ok = true;
@@ -300,17 +328,10 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
       const int dmax = (L - 1) - k0;
       const bool clamped = dmin >= R - 1;
       const bool masked = dmin < 0 || (W > 0 && dmax > W - 1);
-      float* bias_buf = s.bias[i & 1];
-      if (!clamped) {
-        // head g': rev[j] = b[kvh*G + g'][clamp(dmax - j)] * log2 e, j < 127 + n
-        const int span = 127 + n;
-        for (int e = r; e < p.G * span; e += nact) {
-          const int gg = e / span, j = e % span;
-          int d = dmax - j;
-          d = d < 0 ? 0 : (d > R - 1 ? R - 1 : d);
-          bias_buf[gg * kBiasStride + j] = __ldg(p.bias + (size_t)(kvh * p.G + gg) * R + d) * kLog2e;
-        }
-        named_bar_sync(1, nact);
+      const float* bias_buf = s.bias[i % kStages];
+      if (!clamped && !mbar_wait(&s.b_full[i % kStages], (i / kStages) & 1, abort_flag, p.status)) {
+        ok = false;
+        break;
       }
       if (!mbar_wait(&s.s_full[i & 1], (i >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
       tc_fence_after();
@@ -325,12 +346,12 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
       if (clamped) {
 #pragma unroll
         for (int c = 0; c < 128; ++c)
-          sr[c] = __float_as_uint(fmaf(__uint_as_float(sr[c]), p.scale_log2, bconst));
+          sr[c] = __float_as_uint(fmaf(__uint_as_float(sr[c]), p.scale, bconst));
       } else {
         const float* bp = bias_buf + g * kBiasStride + (n - 1 - t);
 #pragma unroll
         for (int c = 0; c < 128; ++c)
-          sr[c] = __float_as_uint(fmaf(__uint_as_float(sr[c]), p.scale_log2, bp[c]));
+          sr[c] = __float_as_uint(fmaf(__uint_as_float(sr[c]), p.scale, bp[c]));
       }
       if (masked) {
         const int d0 = pq - k0;
@@ -352,18 +373,18 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
       }
       const float m_new = fmaxf(m, fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)));
       const bool need = m_new > m + kRescaleThreshold || (m == -INFINITY && m_new > -INFINITY);
-      const float alpha = need ? ex2(m - m_new) : 1.f;
+      const float alpha = need ? ex2((m - m_new) * kLog2e) : 1.f;
       if (need) {
         l *= alpha;
         m = m_new;
       }
-      const float m_use = m == -INFINITY ? 0.f : m;
+      const float nm = m == -INFINITY ? 0.f : -m * kLog2e;  // p = 2^(x log2 e - m log2 e)
       float l0 = 0.f, l1 = 0.f;
       // P pairs overwrite the registers they came from (index c/2 <= c)
 #pragma unroll
       for (int c = 0; c < 128; c += 2) {
-        const float e0 = ex2(__uint_as_float(sr[c]) - m_use);
-        const float e1 = ex2(__uint_as_float(sr[c + 1]) - m_use);
+        const float e0 = ex2(fmaf(__uint_as_float(sr[c]), kLog2e, nm));
+        const float e1 = ex2(fmaf(__uint_as_float(sr[c + 1]), kLog2e, nm));
         l0 += e0;
         l1 += e1;
         sr[c / 2] = pack_bf16(e0, e1);
@@ -440,7 +461,7 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
       }
       if (valid) {
         if (nsplit_b == 1) {
-          if (p.lse != nullptr) p.lse[(size_t)(t_seq0 + t) * p.Hq + h] = (m + __log2f(l)) * kLn2;
+          if (p.lse != nullptr) p.lse[(size_t)(t_seq0 + t) * p.Hq + h] = m + __log2f(l) * kLn2;
         } else {
           p.part_ml[prow * 2 + 0] = m;
           p.part_ml[prow * 2 + 1] = l;
@@ -484,7 +505,7 @@ combine_kernel(const Params p) {
     for (int sp = 0; sp < nsp; ++sp) {
       const size_t prow = (base + sp) * p.rmax + r;
       const float ms = p.part_ml[prow * 2], ls = p.part_ml[prow * 2 + 1];
-      const float wgt = ms == -INFINITY ? 0.f : ex2(ms - M);
+      const float wgt = ms == -INFINITY ? 0.f : ex2((ms - M) * kLog2e);
       if (wgt == 0.f) continue;
       const float4 o = reinterpret_cast<const float4*>(p.part_o + prow * 128)[lane];
       acc.x = fmaf(wgt, o.x, acc.x);
@@ -505,7 +526,7 @@ combine_kernel(const Params p) {
       *reinterpret_cast<float4*>(static_cast<float*>(p.out) + obase) =
           make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
     }
-    if (lane == 0 && p.lse != nullptr) p.lse[(size_t)(t_seq0 + t) * p.Hq + h] = (M + __log2f(lsum)) * kLn2;
+    if (lane == 0 && p.lse != nullptr) p.lse[(size_t)(t_seq0 + t) * p.Hq + h] = M + __log2f(lsum) * kLn2;
   }
 }
 
@@ -569,7 +590,7 @@ cudaError_t launch_decode(const AttnArgs& a, const AttnMaps& maps, cudaStream_t 
   p.num_splits = a.num_splits;
   p.pages_per_split = a.pages_per_split;
   p.num_blocks = a.num_blocks;
-  p.scale_log2 = a.scale * kLog2e;
+  p.scale = a.scale;
   p.part_o = nullptr;
   p.part_ml = nullptr;
   if (a.num_splits > 1) {

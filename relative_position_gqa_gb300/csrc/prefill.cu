@@ -10,6 +10,8 @@
 //   warp 8      TMA producer: Q tiles once, then K and V pages (two-stage ring).
 //   warp 9      MMA issuer (one thread): S = Q K^T (SS form), O += P V (P read from
 //               tensor memory, TS form), commits to mbarriers.  Owns the TMEM allocation.
+//   warps 10-11 bias stagers (one per head): cp.async the tile's slice of the bias table
+//               into shared memory, one stage ahead.
 //   warps 0-3   softmax for head A, warps 4-7 softmax for head B: thread r owns query row
 //               r (= TMEM lane r).  It loads its S row, adds the relative bias, masks,
 //               keeps a running max / sum (rescaling O in TMEM only when the max grew by
@@ -22,10 +24,11 @@
 //
 // The relative bias ("sheared" along the tile diagonals): within a 128x128 tile the
 // distance is delta + r - c with delta = p0 - k0, so row r needs a contiguous run of the
-// table, reversed.  Per tile the softmax group stages the 255 values it needs (times
-// log2 e) in shared memory, in four copies shifted by one float each, so that every
-// thread reads its run with aligned 16-byte loads.  Tiles whose smallest distance is
-// already past R-1 use the single clamped value instead (no loads).  Key tiles are
+// table, reversed.  The stager warp puts the 255 values a tile needs in shared memory in
+// four copies shifted by one float each, so that every softmax thread reads its run with
+// aligned 16-byte loads.  Tiles whose smallest distance is already past R-1 use the single
+// clamped value instead (no copies, no loads).  Logits are kept in natural units
+// (x = scale * q.k + b) and log2 e is folded into the exponent's FMA.  Key tiles are
 // visited from the diagonal backwards; only tiles that overlap the causal diagonal, the
 // window edge or the end of the sequence pay for masking; tiles outside the window are
 // never visited.
@@ -58,16 +61,16 @@ constexpr uint32_t kIdescQK = idesc_bf16(128, 128, false, false);
 constexpr uint32_t kIdescPV = idesc_bf16(128, 128, false, true);
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only past a 256x growth
+constexpr float kRescaleThreshold = 5.545177444479562f;  // 8 ln 2: rescale O past 256x growth
 
 struct __align__(1024) Smem {
   uint8_t q[2][2][16384];        // [head slot][d half][128 rows x 128 B], swizzled
   uint8_t k[kStages][2][16384];  // [stage][d half][128 keys x 128 B]
   uint8_t v[kStages][2][16384];
-  float bias[2][2][4][kBiasCopy];  // [head slot][buffer][shift][index]
+  float bias[kStages][2][4][kBiasCopy];  // [stage][head slot][shift][index], raw values
   uint64_t q_full;
   uint64_t k_full[kStages], v_full[kStages], kv_empty[kStages];
-  uint64_t s_full[2], p_full[2], o_full, drain;
+  uint64_t s_full[2], p_full[2], o_full, drain, b_full[kStages];
   uint32_t tmem_base;
   int abort_flag;
   int bad_block;
@@ -84,7 +87,7 @@ struct Params {
   int max_blocks, R, window, out_dtype;
   int B, T, Hq, Hkv, G, pairs_per_group, head_pairs, q_tiles, max_q_len;
   long long num_blocks;
-  float scale_log2;
+  float scale;
 };
 
 __device__ __forceinline__ uint64_t desc_kmajor(const uint8_t (*atoms)[16384], int ks) {
@@ -152,6 +155,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_q,
       mbar_init(&s.k_full[i], 1);
       mbar_init(&s.v_full[i], 1);
       mbar_init(&s.kv_empty[i], 1);
+      mbar_init(&s.b_full[i], 64);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s.s_full[i], 1);
@@ -214,6 +218,41 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_q,
         }
       }
     }
+   } else if (warp >= 10) {
+    // ---------------------------------------------------------- bias stagers ---
+    // warp 10 stages head A's slices, warp 11 head B's, with 4-byte cp.async copies:
+    // copy_q[j - q] = rev[j] = b[h][clamp(delta + 127 - j, 0, R-1)], j < 256, q < 4,
+    // so every softmax thread can read its reversed diagonal run with aligned 16-byte
+    // loads.  Both warps arrive on b_full[stage] for every tile (count 64).
+    const int slot = warp - 10;
+    const bool mine = slot == 0 || has_b;
+    const float* brow = p.bias + (size_t)(h0 + slot) * p.R;
+    const int R = p.R;
+    for (int i = 0; i < ntiles; ++i) {
+      const int st = i % kStages;
+      int ok = 1;
+      if (lane == 0 && i >= kStages)
+        ok = mbar_wait(&s.kv_empty[st], ((i / kStages) - 1) & 1, abort_flag, p.status);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      const int delta = P0 - (kt_hi - i) * kTile;
+      if (mine && delta - 127 < R - 1) {
+        float* dst = &s.bias[st][slot][0][0];
+#pragma unroll 4
+        for (int e = lane; e < 4 * 256; e += 32) {
+          const int q = e >> 8, jj = e & 255;  // copy q, entry jj holds rev[jj + q]
+          const int j = jj + q;
+          if (j < 256) {
+            int d = delta + 127 - j;
+            d = d < 0 ? 0 : (d > R - 1 ? R - 1 : d);
+            cp_async_4(dst + q * kBiasCopy + jj, brow + d);
+          }
+        }
+      }
+      cp_async_mbar_arrive(&s.b_full[st]);
+    }
+    // let outstanding copies land before the CTA can exit
+    asm volatile("cp.async.wait_all;" ::: "memory");
   } else if (warp == 9) {
     // ------------------------------------------------------------- MMA issuer ---
     bool ok = mbar_wait(&s.q_full, 0, abort_flag, p.status) && mbar_wait(&s.k_full[0], 0, abort_flag, p.status);
@@ -324,46 +363,24 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_q,
     const int h = h0 + grp;
     if (grp == 0 || has_b) {
       const float* brow = p.bias + (size_t)h * p.R;
-      const float bconst = __ldg(brow + p.R - 1) * kLog2e;
+      const float bconst = __ldg(brow + p.R - 1);
       const int R = p.R, W = p.window;
       const int sh = (127 - r) & 3;
       const int base = (127 - r) - sh;
-      float m = -INFINITY;
+      float m = -INFINITY;  // running max of the logits, natural units
       float2 l2 = make_float2(0.f, 0.f);
-      const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
+      const float2 sc2 = make_float2(p.scale, p.scale);
+      const float2 lg2 = make_float2(kLog2e, kLog2e);
       bool ok = true;
-      // this thread's two staged bias values for a tile: rev[j], j = r and r + 128, with
-      // rev[j] = b[h][clamp(delta + 127 - j)] * log2 e.  Loaded one tile ahead.
-      auto load_rev = [&](int i, float& v0, float& v1) {
-        const int delta = P0 - (kt_hi - i) * kTile;
-        int d0 = delta + 127 - r, d1 = d0 - 128;
-        d0 = d0 < 0 ? 0 : (d0 > R - 1 ? R - 1 : d0);
-        d1 = d1 < 0 ? 0 : (d1 > R - 1 ? R - 1 : d1);
-        v0 = __ldg(brow + d0);
-        v1 = __ldg(brow + d1);
-      };
-      float nv0 = 0.f, nv1 = 0.f;
-      if (ntiles > 0 && !(P0 - kt_hi * kTile - 127 >= R - 1)) load_rev(0, nv0, nv1);
       for (int i = 0; i < ntiles; ++i) {
         const int k0 = (kt_hi - i) * kTile;
         const int delta = P0 - k0;
-        // tiles are visited with growing distance, so clamped tiles form a suffix and
-        // every unclamped tile stages (and synchronises) before any clamped one
-        const bool clamped = delta - 127 >= R - 1;
+        const bool clamped = delta - 127 >= R - 1;  // every distance past the table end
         const bool masked = (delta < 127) || (W > 0 && delta + 127 > W - 1) || (k0 + 127 >= L);
-        float* bias_buf = &s.bias[grp][i & 1][0][0];
-        if (!clamped) {
-          // four copies shifted by one float: copy_q[j - q] = rev[j]
-          const float v[2] = {nv0 * kLog2e, nv1 * kLog2e};
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int j = r + 128 * u;
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-              if (j - q >= 0) bias_buf[q * kBiasCopy + j - q] = v[u];
-          }
-          if (i + 1 < ntiles && !(delta + kTile - 127 >= R - 1)) load_rev(i + 1, nv0, nv1);
-          named_bar_sync(1 + grp, 128);
+        const float* bias_buf = &s.bias[i % kStages][grp][0][0];
+        if (!clamped && !mbar_wait(&s.b_full[i % kStages], (i / kStages) & 1, abort_flag, p.status)) {
+          ok = false;
+          break;
         }
         if (!mbar_wait(&s.s_full[grp], i & 1, abort_flag, p.status)) { ok = false; break; }
         tc_fence_after();
@@ -426,18 +443,18 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_q,
         mx1 = fmax3(mx1, x[63].x, x[63].y);
         const float m_new = fmax3(m, fmaxf(mx0, mx1), fmaxf(mx2, mx3));
         const bool need = m_new > m + kRescaleThreshold || (m == -INFINITY && m_new > -INFINITY);
-        const float alpha = need ? ex2(m - m_new) : 1.f;
+        const float alpha = need ? ex2((m - m_new) * kLog2e) : 1.f;
         if (need) {
           l2.x *= alpha;
           l2.y *= alpha;
           m = m_new;
         }
-        const float m_use = m == -INFINITY ? 0.f : m;
-        const float2 nm2 = make_float2(-m_use, -m_use);
+        const float nm = m == -INFINITY ? 0.f : -m * kLog2e;  // p = 2^(x log2 e - m log2 e)
+        const float2 nm2 = make_float2(nm, nm);
         // P as bf16 pairs, reusing the S registers
 #pragma unroll
         for (int k = 0; k < 64; ++k) {
-          const float2 d2 = __fadd2_rn(x[k], nm2);
+          const float2 d2 = __ffma2_rn(x[k], lg2, nm2);
           const float2 e2 = make_float2(ex2(d2.x), ex2(d2.y));
           l2 = __fadd2_rn(l2, e2);
           sr[k] = pack_bf16(e2.x, e2.y);
@@ -500,7 +517,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_q,
             }
           }
         }
-        if (store && p.lse != nullptr) p.lse[(size_t)t * p.Hq + h] = (m + __log2f(l)) * kLn2;
+        if (store && p.lse != nullptr) p.lse[(size_t)t * p.Hq + h] = m + __log2f(l) * kLn2;
       }
     }
   }
@@ -539,7 +556,7 @@ cudaError_t launch_prefill(const AttnArgs& a, const AttnMaps& maps, cudaStream_t
   p.q_tiles = (a.max_q_len + kTile - 1) / kTile;
   p.max_q_len = a.max_q_len;
   p.num_blocks = a.num_blocks;
-  p.scale_log2 = a.scale * kLog2e;
+  p.scale = a.scale;
   const long long grid = (long long)p.q_tiles * p.B * p.head_pairs;
   if (grid == 0) return cudaSuccess;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
