@@ -165,6 +165,33 @@ INKLING_API int inkling_rel_attn_decode(const void *q, const void *k_cache, cons
                             size_t workspace_bytes, int32_t *dev_status,
                             inkling_stream_t stream);
 
+/*
+ * inkling_rel_attn_decode_noalloc — inkling_rel_attn_decode for callers that cannot give
+ * the library a device buffer: a runtime that reserves all device memory at start-up and
+ * forbids cudaMalloc while serving (it can synchronise the device, and it is not allowed
+ * inside a stream that is being captured), or code that runs inside another framework's
+ * allocator and must not re-enter it.  The pages have no counterpart to this call.
+ *
+ * Arguments and results are those of inkling_rel_attn_decode without the workspace.
+ * The split partials go to a static device array of
+ * inkling_rel_attn_decode_noalloc_capacity() bytes (32 MiB) that is part of the library:
+ * every GPU that loads the library holds it until the process exits.  A request whose
+ * partials would not fit (inkling_rel_attn_decode_workspace_size(...) with the same
+ * arguments above the capacity) returns INKLING_ERR_WORKSPACE and launches nothing.
+ * The first call on a device looks up the array's device address (cudaGetSymbolAddress,
+ * with that device current); make that first call before any stream capture.  No device
+ * memory is allocated or freed.  All calls share the one array and it keeps the last
+ * call's contents (the kernels need none of it zeroed): calls whose work can overlap on
+ * the GPU (other streams, other threads) race on it and must be serialised by the caller.
+ */
+INKLING_API size_t inkling_rel_attn_decode_noalloc_capacity(void);
+INKLING_API int inkling_rel_attn_decode_noalloc(
+    const void *q, const void *k_cache, const void *v_cache, const int32_t *block_table,
+    int32_t max_blocks, const int32_t *cu_q_lens, const int32_t *seq_lens, const float *bias,
+    int32_t R, float scale, int32_t window, void *out, int32_t out_dtype, float *lse, int32_t B,
+    int32_t T, int32_t Hq, int32_t Hkv, int64_t num_blocks, int32_t max_q_len,
+    int32_t max_seq_len, int32_t num_splits, int32_t *dev_status, inkling_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

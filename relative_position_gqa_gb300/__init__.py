@@ -125,3 +125,27 @@ def rel_attn_decode(q, k_cache, v_cache, block_table, cu_q_lens, seq_lens, bias,
                   int(window), out, out_dtype, lse, B, T, hq, hkv, k_cache.shape[0],
                   int(max_q_len), int(max_seq_len), int(num_splits), workspace, ws_bytes,
                   dev_status, _stream(stream))
+
+
+def decode_noalloc_capacity() -> int:
+    """Bytes of the library's static decode scratch (per device)."""
+    return int(_lib.load().inkling_rel_attn_decode_noalloc_capacity())
+
+
+def rel_attn_decode_noalloc(q, k_cache, v_cache, block_table, cu_q_lens, seq_lens, bias, *,
+                            scale: float, window: int, max_q_len: int, max_seq_len: int,
+                            out: torch.Tensor, lse: Optional[torch.Tensor] = None,
+                            num_splits: int = 0, dev_status=None, stream=None) -> None:
+    """inkling_rel_attn_decode_noalloc: the same decode, with its split partials in the
+    library's static device scratch instead of a workspace, for callers that cannot
+    allocate device memory while they run.  Nothing is allocated here either.  Calls
+    that can overlap on the GPU share that scratch and must be serialised."""
+    dev, out_dtype = _attn_common(q, k_cache, v_cache, block_table, cu_q_lens, seq_lens, bias,
+                                  out, lse, dev_status)
+    T, hq = q.shape[0], q.shape[1]
+    with torch.cuda.device(dev):
+        _lib.call("inkling_rel_attn_decode_noalloc", q, k_cache, v_cache, block_table,
+                  block_table.shape[1], cu_q_lens, seq_lens, bias, bias.shape[1], float(scale),
+                  int(window), out, out_dtype, lse, cu_q_lens.shape[0] - 1, T, hq,
+                  k_cache.shape[1], k_cache.shape[0], int(max_q_len), int(max_seq_len),
+                  int(num_splits), dev_status, _stream(stream))

@@ -23,10 +23,14 @@ SIGNATURES = {
     "inkling_rel_attn_decode_workspace_size": [I32, I32, I32, I32, I32, I32, I32],
     "inkling_rel_attn_decode": [P, P, P, P, I32, P, P, P, I32, F32, I32, P, I32, P, I32, I32,
                                 I32, I32, I64, I32, I32, I32, P, SZ, P, P],
+    "inkling_rel_attn_decode_noalloc_capacity": [],
+    "inkling_rel_attn_decode_noalloc": [P, P, P, P, I32, P, P, P, I32, F32, I32, P, I32, P, I32,
+                                        I32, I32, I32, I64, I32, I32, I32, P, P],
     "inkling_status_string": [ctypes.c_int],
     "inkling_version": [],
 }
-RESTYPES = {"inkling_rel_attn_decode_workspace_size": SZ, "inkling_status_string": ctypes.c_char_p}
+RESTYPES = {"inkling_rel_attn_decode_workspace_size": SZ, "inkling_status_string": ctypes.c_char_p,
+            "inkling_rel_attn_decode_noalloc_capacity": SZ}
 
 _lib = None
 
