@@ -479,55 +479,58 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
 }
 
 // Merge the split partials of every (sequence, KV head) that needed more than one split.
-// One warp per packed row; each lane owns 4 of the 128 output columns.
-__global__ void __launch_bounds__(256)
+// One warp per packed row (grid: row groups x KV heads x sequences); each lane owns 4 of
+// the 128 output columns.  The split loop has no data-dependent branch, so the loads of
+// several splits are in flight at once (a row with no allowed key in a split has m = -inf,
+// l = 0 and O = 0 there, and gets weight 0).
+constexpr int kCombineWarps = 8;
+
+__global__ void __launch_bounds__(kCombineWarps * 32)
 combine_kernel(const Params p) {
-  const int kvh = blockIdx.x, b = blockIdx.y;
+  const int kvh = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = blockIdx.x * kCombineWarps + warp;
   const int t_seq0 = p.cu_q_lens[b];
   const int n = p.cu_q_lens[b + 1] - t_seq0;
-  if (n <= 0 || n > p.max_q_len) return;
+  if (n <= 0 || n > p.max_q_len || r >= n * p.G) return;
   const int L = p.seq_lens[b];
   if (n > L || L > p.max_blocks * 128) return;
   int kt_lo, kt_hi;
   page_range(L, n, p.window, kt_lo, kt_hi);
   const int nsp = (kt_hi - kt_lo + 1 + p.pages_per_split - 1) / p.pages_per_split;
   if (nsp <= 1 || nsp > p.num_splits) return;
-  const int rows = n * p.G;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const size_t base = ((size_t)b * p.Hkv + kvh) * p.num_splits;
-  for (int r = warp; r < rows; r += 8) {
-    float M = -INFINITY;
-    for (int sp = lane; sp < nsp; sp += 32) M = fmaxf(M, p.part_ml[((base + sp) * p.rmax + r) * 2]);
+  float M = -INFINITY;
+  for (int sp = lane; sp < nsp; sp += 32) M = fmaxf(M, p.part_ml[((base + sp) * p.rmax + r) * 2]);
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    float lsum = 0.f;
-    for (int sp = 0; sp < nsp; ++sp) {
-      const size_t prow = (base + sp) * p.rmax + r;
-      const float ms = p.part_ml[prow * 2], ls = p.part_ml[prow * 2 + 1];
-      const float wgt = ms == -INFINITY ? 0.f : ex2((ms - M) * kLog2e);
-      if (wgt == 0.f) continue;
-      const float4 o = reinterpret_cast<const float4*>(p.part_o + prow * 128)[lane];
-      acc.x = fmaf(wgt, o.x, acc.x);
-      acc.y = fmaf(wgt, o.y, acc.y);
-      acc.z = fmaf(wgt, o.z, acc.z);
-      acc.w = fmaf(wgt, o.w, acc.w);
-      lsum = fmaf(wgt, ls, lsum);
-    }
-    const float inv = 1.f / lsum;
-    const int t = r / p.G, h = kvh * p.G + r % p.G;
-    const size_t obase = ((size_t)(t_seq0 + t) * p.Hq + h) * 128 + lane * 4;
-    if (p.out_dtype == 0) {
-      uint2 w;
-      w.x = pack_bf16(acc.x * inv, acc.y * inv);
-      w.y = pack_bf16(acc.z * inv, acc.w * inv);
-      *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.out) + obase) = w;
-    } else {
-      *reinterpret_cast<float4*>(static_cast<float*>(p.out) + obase) =
-          make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-    }
-    if (lane == 0 && p.lse != nullptr) p.lse[(size_t)(t_seq0 + t) * p.Hq + h] = M + __log2f(lsum) * kLn2;
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float lsum = 0.f;
+#pragma unroll 8
+  for (int sp = 0; sp < nsp; ++sp) {
+    const size_t prow = (base + sp) * p.rmax + r;
+    const float2 ml = *reinterpret_cast<const float2*>(p.part_ml + prow * 2);
+    const float4 o = reinterpret_cast<const float4*>(p.part_o + prow * 128)[lane];
+    const float wgt = ex2((ml.x - M) * kLog2e);  // m = -inf gives 0
+    acc.x = fmaf(wgt, o.x, acc.x);
+    acc.y = fmaf(wgt, o.y, acc.y);
+    acc.z = fmaf(wgt, o.z, acc.z);
+    acc.w = fmaf(wgt, o.w, acc.w);
+    lsum = fmaf(wgt, ml.y, lsum);
   }
+  const float inv = 1.f / lsum;
+  const int t = r / p.G, h = kvh * p.G + r % p.G;
+  const size_t obase = ((size_t)(t_seq0 + t) * p.Hq + h) * 128 + lane * 4;
+  if (p.out_dtype == 0) {
+    uint2 w;
+    w.x = pack_bf16(acc.x * inv, acc.y * inv);
+    w.y = pack_bf16(acc.z * inv, acc.w * inv);
+    *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.out) + obase) = w;
+  } else {
+    *reinterpret_cast<float4*>(static_cast<float*>(p.out) + obase) =
+        make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+  }
+  if (lane == 0 && p.lse != nullptr) p.lse[(size_t)(t_seq0 + t) * p.Hq + h] = M + __log2f(lsum) * kLn2;
 }
 
 }  // namespace decode
@@ -608,7 +611,8 @@ cudaError_t launch_decode(const AttnArgs& a, const AttnMaps& maps, cudaStream_t 
   decode_kernel<<<grid, kThreads, smem, stream>>>(maps.k, maps.v, p);
   e = cudaGetLastError();
   if (e != cudaSuccess || a.num_splits <= 1) return e;
-  combine_kernel<<<dim3(a.Hkv, a.B), 256, 0, stream>>>(p);
+  combine_kernel<<<dim3((p.rmax + kCombineWarps - 1) / kCombineWarps, a.Hkv, a.B),
+                   kCombineWarps * 32, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -59,8 +59,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 // Wait for the phase with the given parity to complete.  Gives up (returns false) when
-// `abort_flag` is raised by another warp of the CTA, when the launch's global status word
-// (nullable) shows that some CTA has already failed, or after kWaitBudgetCycles.
+// `abort_flag` is raised by another warp of the CTA, after kWaitBudgetCycles, or, once the
+// wait has lasted kGlobalPollAfter cycles, when the launch's global status word
+// (nullable) shows that some CTA has already failed.  The slow checks only run every few
+// spins and global memory is not touched at all by a wait of normal length.
+constexpr long long kGlobalPollAfter = 1000000LL;
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
                                           volatile int* abort_flag,
                                           const int* global_status = nullptr) {
@@ -68,11 +71,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
   const long long t0 = clock64();
   uint32_t spins = 0;
   while (!mbar_try_wait(bar, parity)) {
+    if ((++spins & 15u) != 0) continue;
     if (*abort_flag) return false;
-    if ((++spins & 255u) == 0) {
-      if (global_status != nullptr && *reinterpret_cast<const volatile int*>(global_status) != 0)
+    if ((spins & 255u) == 0) {
+      const long long dt = clock64() - t0;
+      if (dt > kWaitBudgetCycles) return false;
+      if (dt > kGlobalPollAfter && global_status != nullptr &&
+          *reinterpret_cast<const volatile int*>(global_status) != 0)
         return false;
-      if (clock64() - t0 > kWaitBudgetCycles) return false;
     }
   }
   return true;
