@@ -47,14 +47,13 @@ constexpr int kTile = 128;
 constexpr int kStages = 2;
 constexpr int kThreads = 384;  // three warpgroups: softmax A, softmax B, producer/MMA
 // Register split (setmaxnreg): the kernel is built for 168 registers a thread at launch
-// (65536 / 384, rounded down to 8), i.e. 64512 for the CTA.  The producer/MMA/stager
-// warpgroup gives back down to 112 and each softmax warpgroup grows to 192:
-// 2*128*192 + 128*112 = 63488 <= 64512.  The host refuses to launch unless the built
-// register count is 168, since an increase that the launch cannot cover would wait
-// forever.
+// (65536 / 384, rounded down to 8), i.e. 64512 for the CTA.  The producer/MMA warpgroup
+// gives back down to 64 and each softmax warpgroup grows to 216: 2*128*216 + 128*64 =
+// 63488 <= 64512.  The host refuses to launch unless the built register count is 168,
+// since an increase that the launch cannot cover would wait forever.
 constexpr int kLaunchRegs = 168;
-constexpr int kSoftmaxRegs = 192;
-constexpr int kOtherRegs = 112;
+constexpr int kSoftmaxRegs = 216;
+constexpr int kOtherRegs = 64;
 static_assert(2 * 128 * kSoftmaxRegs + 128 * kOtherRegs <= kThreads * kLaunchRegs,
               "register split exceeds the launch allocation");
 constexpr int kBiasCopy = 264;  // floats per shifted copy; 264/4 = 66 = 2 (mod 8) spreads banks
@@ -69,7 +68,7 @@ struct __align__(1024) Smem {
   uint8_t k[kStages][2][16384];  // [stage][d half][128 keys x 128 B]
   uint8_t v[kStages][2][16384];
   float bias[kStages][2][4][kBiasCopy];  // [stage][head slot][shift][index], raw values
-  uint64_t q_full, q_empty, o_free;
+  uint64_t q_full;
   uint64_t k_full[kStages], v_full[kStages], kv_empty[kStages];
   uint64_t s_full[2], p_full[2], o_full, drain, b_full[kStages];
   uint32_t tmem_base;
@@ -86,7 +85,7 @@ struct Params {
   float* lse;
   int* status;
   int max_blocks, R, window, out_dtype;
-  int B, T, Hq, Hkv, G, pairs_per_group, head_pairs, q_tiles, max_q_len, num_items;
+  int B, T, Hq, Hkv, G, pairs_per_group, head_pairs, q_tiles, max_q_len;
   long long num_blocks;
   float scale;
 };
@@ -100,46 +99,6 @@ __device__ __forceinline__ uint64_t desc_v(const uint8_t (*atoms)[16384], int ks
   return sdesc_sw128(smem_u32(atoms[0]) + ks * 2048, 16384, 1024);
 }
 
-// Geometry of one work item (a 128-token query tile of one sequence x a pair of query
-// heads of one KV group).  Items are numbered heavy (late query tiles) first, head pairs
-// fastest; a CTA takes items blockIdx.x, blockIdx.x + gridDim.x, ...
-struct Item {
-  bool valid;   // the tile holds at least one new token
-  bool bad;     // lengths inconsistent with the limits
-  bool has_b;   // the pair has a second head
-  int b, n, L, P0, rows, kt_hi, ntiles, kvh, h0, t_glob0;
-};
-
-__device__ __forceinline__ Item item_geom(const Params& p, int idx) {
-  Item it;
-  const int hp = idx % p.head_pairs;
-  const int rest = idx / p.head_pairs;
-  it.b = rest % p.B;
-  const int qt = p.q_tiles - 1 - rest / p.B;
-  const int t_seq0 = p.cu_q_lens[it.b];
-  it.n = p.cu_q_lens[it.b + 1] - t_seq0;
-  it.L = p.seq_lens[it.b];
-  it.valid = qt * kTile < it.n;
-  it.bad = it.valid && (it.n > it.L || it.n > p.max_q_len || it.L > p.max_blocks * kTile);
-  if (!it.valid || it.bad) {
-    it.valid = false;
-    it.has_b = false;
-    it.P0 = it.rows = it.kt_hi = it.ntiles = it.kvh = it.h0 = it.t_glob0 = 0;
-    return it;
-  }
-  it.P0 = it.L - it.n + qt * kTile;  // position of row 0
-  it.rows = min(kTile, it.n - qt * kTile);
-  const int lo = p.window > 0 ? max(0, it.P0 - p.window + 1) : 0;
-  const int hi = it.P0 + it.rows - 1;
-  it.kt_hi = hi / kTile;
-  it.ntiles = it.kt_hi - lo / kTile + 1;
-  it.kvh = hp / p.pairs_per_group;
-  it.h0 = it.kvh * p.G + 2 * (hp % p.pairs_per_group);
-  it.has_b = (2 * (hp % p.pairs_per_group) + 1) < p.G;
-  it.t_glob0 = t_seq0 + qt * kTile;
-  return it;
-}
-
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap map_q,
                const __grid_constant__ CUtensorMap map_k,
@@ -148,34 +107,50 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_q,
   Smem& s = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                      ~uintptr_t(1023));
   const int warp = warp_id(), lane = lane_id();
-  const int first = blockIdx.x, stride = gridDim.x;
+
+  // ---- work item: heavy (late) query tiles first, head pairs fastest ----
+  const int idx = blockIdx.x;
+  const int hp = idx % p.head_pairs;
+  const int rest = idx / p.head_pairs;
+  const int b = rest % p.B;
+  const int qt = p.q_tiles - 1 - rest / p.B;
+  const int t_seq0 = p.cu_q_lens[b];
+  const int n = p.cu_q_lens[b + 1] - t_seq0;
+  if (qt * kTile >= n) return;  // whole CTA, before any barrier
+  const int L = p.seq_lens[b];
+  if (n > L || n > p.max_q_len || L > p.max_blocks * kTile) {
+    if (threadIdx.x == 0) report(p.status, kErrBadInput);
+    return;
+  }
+  const int P0 = L - n + qt * kTile;  // position of row 0
+  const int rows = min(kTile, n - qt * kTile);
+  const int lo = p.window > 0 ? max(0, P0 - p.window + 1) : 0;
+  const int hi = P0 + rows - 1;
+  const int kt_lo = lo / kTile, kt_hi = hi / kTile;
+  const int ntiles = kt_hi - kt_lo + 1;
+  const int kvh = hp / p.pairs_per_group;
+  const int h0 = kvh * p.G + 2 * (hp % p.pairs_per_group);
+  const bool has_b = (2 * (hp % p.pairs_per_group) + 1) < p.G;
+  const int t_glob0 = t_seq0 + qt * kTile;
+  const int32_t* table = p.block_table + (size_t)b * p.max_blocks;
 
   if (threadIdx.x == 0) {
     s.abort_flag = 0;
     s.bad_block = 0;
   }
   __syncthreads();
-  // Check every page id this CTA will read, and the lengths, before anything starts
-  // (one warp per item, lanes over its tiles).
-  for (int idx = first + warp * stride; idx < p.num_items; idx += (kThreads / 32) * stride) {
-    const Item it = item_geom(p, idx);
-    if (it.bad) s.bad_block = 2;
-    if (!it.valid) continue;
-    const int32_t* table = p.block_table + (size_t)it.b * p.max_blocks;
-    for (int k = lane; k < it.ntiles; k += 32) {
-      const int32_t blk = table[it.kt_hi - k];
-      if (blk < 0 || (long long)blk >= p.num_blocks) s.bad_block = 1;
-    }
+  for (int kt = kt_lo + (int)threadIdx.x; kt <= kt_hi; kt += kThreads) {
+    const int32_t blk = table[kt];
+    if (blk < 0 || (long long)blk >= p.num_blocks) s.bad_block = 1;
   }
   __syncthreads();
   if (s.bad_block) {
-    if (threadIdx.x == 0) report(p.status, s.bad_block == 1 ? kErrBadBlock : kErrBadInput);
+    if (threadIdx.x == 0) report(p.status, kErrBadBlock);
     return;
   }
 
   if (threadIdx.x == 0) {
     mbar_init(&s.q_full, 1);
-    mbar_init(&s.q_empty, 1);
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&s.k_full[i], 1);
       mbar_init(&s.v_full[i], 1);
@@ -187,7 +162,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_q,
       mbar_init(&s.p_full[i], 128);
     }
     mbar_init(&s.o_full, 1);
-    mbar_init(&s.o_free, 256);
     mbar_init(&s.drain, 1);
     fence_barrier_init();
   }
@@ -209,50 +183,39 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_q,
       tma_prefetch_desc(&map_q);
       tma_prefetch_desc(&map_k);
       tma_prefetch_desc(&map_v);
-      int g = 0, j = 0, issued = 0;  // tiles and items issued so far
-      bool ok = true;
-      for (int idx = first; ok && idx < p.num_items; idx += stride) {
-        const Item it = item_geom(p, idx);
-        if (!it.valid) continue;
-        // Q of this item may overwrite the previous item's once its last QK^T is done
-        if (j > 0 && !mbar_wait(&s.q_empty, (j - 1) & 1, abort_flag, p.status)) { ok = false; break; }
-        mbar_arrive_expect_tx(&s.q_full, it.has_b ? 65536u : 32768u);
-        tma_load_3d(s.q[0][0], &map_q, &s.q_full, 0, it.h0, it.t_glob0);
-        tma_load_3d(s.q[0][1], &map_q, &s.q_full, 64, it.h0, it.t_glob0);
-        if (it.has_b) {
-          tma_load_3d(s.q[1][0], &map_q, &s.q_full, 0, it.h0 + 1, it.t_glob0);
-          tma_load_3d(s.q[1][1], &map_q, &s.q_full, 64, it.h0 + 1, it.t_glob0);
-        }
-        const int32_t* table = p.block_table + (size_t)it.b * p.max_blocks;
-        for (int i = 0; i < it.ntiles; ++i, ++g) {
-          const int st = g % kStages;
-          if (g >= kStages && !mbar_wait(&s.kv_empty[st], ((g / kStages) - 1) & 1, abort_flag, p.status)) {
-            ok = false;
-            break;
-          }
-          const int page = table[it.kt_hi - i] * p.Hkv + it.kvh;
-          mbar_arrive_expect_tx(&s.k_full[st], 32768u);
-          tma_load_3d(s.k[st][0], &map_k, &s.k_full[st], 0, 0, page);
-          tma_load_3d(s.k[st][1], &map_k, &s.k_full[st], 64, 0, page);
-          mbar_arrive_expect_tx(&s.v_full[st], 32768u);
-          tma_load_3d(s.v[st][0], &map_v, &s.v_full[st], 0, 0, page);
-          tma_load_3d(s.v[st][1], &map_v, &s.v_full[st], 64, 0, page);
-          issued = g + 1;
-        }
-        ++j;
+      mbar_arrive_expect_tx(&s.q_full, has_b ? 65536u : 32768u);
+      tma_load_3d(s.q[0][0], &map_q, &s.q_full, 0, h0, t_glob0);
+      tma_load_3d(s.q[0][1], &map_q, &s.q_full, 64, h0, t_glob0);
+      if (has_b) {
+        tma_load_3d(s.q[1][0], &map_q, &s.q_full, 0, h0 + 1, t_glob0);
+        tma_load_3d(s.q[1][1], &map_q, &s.q_full, 64, h0 + 1, t_glob0);
       }
-      if (!ok) {
-        report(p.status, kErrTimeout);
-        s.abort_flag = 1;
+      int issued = 0;
+      for (int i = 0; i < ntiles; ++i) {
+        const int st = i % kStages;
+        if (i >= kStages && !mbar_wait(&s.kv_empty[st], ((i / kStages) - 1) & 1, abort_flag, p.status)) {
+          report(p.status, kErrTimeout);
+          s.abort_flag = 1;
+          break;
+        }
+        const int page = table[kt_hi - i] * p.Hkv + kvh;
+        mbar_arrive_expect_tx(&s.k_full[st], 32768u);
+        tma_load_3d(s.k[st][0], &map_k, &s.k_full[st], 0, 0, page);
+        tma_load_3d(s.k[st][1], &map_k, &s.k_full[st], 64, 0, page);
+        mbar_arrive_expect_tx(&s.v_full[st], 32768u);
+        tma_load_3d(s.v[st][0], &map_v, &s.v_full[st], 0, 0, page);
+        tma_load_3d(s.v[st][1], &map_v, &s.v_full[st], 64, 0, page);
+        issued = i + 1;
+      }
+      if (*abort_flag) {
         // let the copies already in flight land before the CTA goes away
-        volatile int never = 0;
-        for (int t = max(0, issued - kStages); t < issued; ++t) {
-          const int st = t % kStages;
-          const uint32_t ph = (t / kStages) & 1;
+        for (int i = max(0, issued - kStages); i < issued; ++i) {
+          const int st = i % kStages;
+          const uint32_t ph = (i / kStages) & 1;
+          volatile int never = 0;
           mbar_wait(&s.k_full[st], ph, &never);
           mbar_wait(&s.v_full[st], ph, &never);
         }
-        if (j > 0) mbar_wait(&s.q_full, (j - 1) & 1, &never);
       }
     }
    } else if (warp >= 10) {
@@ -262,144 +225,121 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_q,
     // so every softmax thread can read its reversed diagonal run with aligned 16-byte
     // loads.  Both warps arrive on b_full[stage] for every tile (count 64).
     const int slot = warp - 10;
+    const bool mine = slot == 0 || has_b;
+    const float* brow = p.bias + (size_t)(h0 + slot) * p.R;
     const int R = p.R;
-    int g = 0;
-    bool ok = true;
-    for (int idx = first; ok && idx < p.num_items; idx += stride) {
-      const Item it = item_geom(p, idx);
-      if (!it.valid) continue;
-      const bool mine = slot == 0 || it.has_b;
-      const float* brow = p.bias + (size_t)(it.h0 + slot) * R;
-      for (int i = 0; i < it.ntiles; ++i, ++g) {
-        const int st = g % kStages;
-        int w = 1;
-        if (lane == 0 && g >= kStages)
-          w = mbar_wait(&s.kv_empty[st], ((g / kStages) - 1) & 1, abort_flag, p.status);
-        if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
-        const int delta = it.P0 - (it.kt_hi - i) * kTile;
-        if (mine && delta - 127 < R - 1) {
-          float* dst = &s.bias[st][slot][0][0];
+    for (int i = 0; i < ntiles; ++i) {
+      const int st = i % kStages;
+      int ok = 1;
+      if (lane == 0 && i >= kStages)
+        ok = mbar_wait(&s.kv_empty[st], ((i / kStages) - 1) & 1, abort_flag, p.status);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      const int delta = P0 - (kt_hi - i) * kTile;
+      if (mine && delta - 127 < R - 1) {
+        float* dst = &s.bias[st][slot][0][0];
 #pragma unroll 4
-          for (int e = lane; e < 4 * 256; e += 32) {
-            const int q = e >> 8, jj = e & 255;  // copy q, entry jj holds rev[jj + q]
-            const int jx = jj + q;
-            if (jx < 256) {
-              int d = delta + 127 - jx;
-              d = d < 0 ? 0 : (d > R - 1 ? R - 1 : d);
-              cp_async_4(dst + q * kBiasCopy + jj, brow + d);
-            }
+        for (int e = lane; e < 4 * 256; e += 32) {
+          const int q = e >> 8, jj = e & 255;  // copy q, entry jj holds rev[jj + q]
+          const int j = jj + q;
+          if (j < 256) {
+            int d = delta + 127 - j;
+            d = d < 0 ? 0 : (d > R - 1 ? R - 1 : d);
+            cp_async_4(dst + q * kBiasCopy + jj, brow + d);
           }
         }
-        cp_async_mbar_arrive(&s.b_full[st]);
       }
+      cp_async_mbar_arrive(&s.b_full[st]);
     }
     // let outstanding copies land before the CTA can exit
     asm volatile("cp.async.wait_all;" ::: "memory");
   } else if (warp == 9) {
     // ------------------------------------------------------------- MMA issuer ---
-    int g = 0, tA = 0, tB = 0, j = 0;  // K/V tiles, S/P phases per group, items
-    bool ok = true, issued_any = false;
-    for (int idx = first; ok && idx < p.num_items; idx += stride) {
-      const Item it = item_geom(p, idx);
-      if (!it.valid) continue;
-      const int nt = it.ntiles;
-      const bool hb = it.has_b;
-      ok = mbar_wait(&s.q_full, j & 1, abort_flag, p.status) &&
-           mbar_wait(&s.k_full[g % kStages], (g / kStages) & 1, abort_flag, p.status);
-      if (!ok) break;
+    bool ok = mbar_wait(&s.q_full, 0, abort_flag, p.status) && mbar_wait(&s.k_full[0], 0, abort_flag, p.status);
+    bool issued_any = false;
+    if (ok) {
       tc_fence_after();
       if (lane == 0) {
-        const int st0 = g % kStages;
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
-          umma_ss(tmem + 0, desc_kmajor(s.q[0], ks), desc_kmajor(s.k[st0], ks), kIdescQK, ks > 0);
+          umma_ss(tmem + 0, desc_kmajor(s.q[0], ks), desc_kmajor(s.k[0], ks), kIdescQK, ks > 0);
         umma_commit(&s.s_full[0]);
-        if (hb) {
+        if (has_b) {
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
-            umma_ss(tmem + 128, desc_kmajor(s.q[1], ks), desc_kmajor(s.k[st0], ks), kIdescQK,
+            umma_ss(tmem + 128, desc_kmajor(s.q[1], ks), desc_kmajor(s.k[0], ks), kIdescQK,
                     ks > 0);
           umma_commit(&s.s_full[1]);
         }
-        if (nt == 1) umma_commit(&s.q_empty);  // the item's last QK^T is issued
       }
       issued_any = true;
       __syncwarp();
-      // O may be overwritten once the previous item's epilogue has read it
-      if (j > 0 && !mbar_wait(&s.o_free, (j - 1) & 1, abort_flag, p.status)) { ok = false; break; }
-      for (int i = 0; i < nt; ++i) {
-        const int gi = g + i;
-        const int st = gi % kStages;
-        ok = mbar_wait(&s.p_full[0], (tA + i) & 1, abort_flag, p.status) &&
-             mbar_wait(&s.v_full[st], (gi / kStages) & 1, abort_flag, p.status);
-        if (!ok) break;
-        if (i == 0 && (it.kt_hi + 1) * kTile > it.L) {
-          // keys past the end of the sequence: their P is 0, but junk V could be NaN
-          const int r0 = it.L - it.kt_hi * kTile;
-          const int chunks = (kTile - r0) * 8;  // 16-byte chunks per d half
-          for (int c = lane; c < 2 * chunks; c += 32) {
-            const int half = c / chunks, cc = c % chunks;
-            *reinterpret_cast<uint4*>(s.v[st][half] + (size_t)(r0 + cc / 8) * 128 + (cc % 8) * 16) =
-                make_uint4(0, 0, 0, 0);
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
+    }
+    for (int i = 0; ok && i < ntiles; ++i) {
+      const int st = i % kStages;
+      const uint32_t ph = (i / kStages) & 1;
+      ok = mbar_wait(&s.p_full[0], i & 1, abort_flag, p.status) && mbar_wait(&s.v_full[st], ph, abort_flag, p.status);
+      if (!ok) break;
+      if (i == 0 && (kt_hi + 1) * kTile > L) {
+        // keys past the end of the sequence: their P is 0, but junk V could be NaN
+        const int r0 = L - kt_hi * kTile;
+        const int chunks = (kTile - r0) * 8;  // 16-byte chunks per d half
+        for (int c = lane; c < 2 * chunks; c += 32) {
+          const int half = c / chunks, cc = c % chunks;
+          *reinterpret_cast<uint4*>(s.v[st][half] + (size_t)(r0 + cc / 8) * 128 + (cc % 8) * 16) =
+              make_uint4(0, 0, 0, 0);
         }
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
+      tc_fence_after();
+      if (lane == 0) {
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+          umma_ts(tmem + 256, tmem + 0 + ks * 8, desc_v(s.v[st], ks), kIdescPV, (i > 0 || ks > 0));
+      }
+      __syncwarp();
+      const bool more = i + 1 < ntiles;
+      const int st1 = (i + 1) % kStages;
+      if (more) {
+        ok = mbar_wait(&s.k_full[st1], ((i + 1) / kStages) & 1, abort_flag, p.status);
+        if (!ok) break;
         tc_fence_after();
         if (lane == 0) {
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
-            umma_ts(tmem + 256, tmem + 0 + ks * 8, desc_v(s.v[st], ks), kIdescPV, (i > 0 || ks > 0));
-        }
-        __syncwarp();
-        const bool more = i + 1 < nt;
-        const int st1 = (gi + 1) % kStages;
-        if (more) {
-          ok = mbar_wait(&s.k_full[st1], ((gi + 1) / kStages) & 1, abort_flag, p.status);
-          if (!ok) break;
-          tc_fence_after();
-          if (lane == 0) {
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks)
-              umma_ss(tmem + 0, desc_kmajor(s.q[0], ks), desc_kmajor(s.k[st1], ks), kIdescQK, ks > 0);
-            umma_commit(&s.s_full[0]);
-          }
-          __syncwarp();
-        }
-        if (hb) {
-          ok = mbar_wait(&s.p_full[1], (tB + i) & 1, abort_flag, p.status);
-          if (!ok) break;
-          tc_fence_after();
-          if (lane == 0) {
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks)
-              umma_ts(tmem + 384, tmem + 128 + ks * 8, desc_v(s.v[st], ks), kIdescPV,
-                      (i > 0 || ks > 0));
-          }
-          __syncwarp();
-        }
-        if (lane == 0) {
-          umma_commit(&s.kv_empty[st]);
-          if (hb && more) {
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks)
-              umma_ss(tmem + 128, desc_kmajor(s.q[1], ks), desc_kmajor(s.k[st1], ks), kIdescQK,
-                      ks > 0);
-            umma_commit(&s.s_full[1]);
-          }
-          if (i + 2 == nt) umma_commit(&s.q_empty);  // the item's last QK^T is issued
+            umma_ss(tmem + 0, desc_kmajor(s.q[0], ks), desc_kmajor(s.k[st1], ks), kIdescQK, ks > 0);
+          umma_commit(&s.s_full[0]);
         }
         __syncwarp();
       }
-      if (!ok) break;
-      if (lane == 0) umma_commit(&s.o_full);
+      if (has_b) {
+        ok = mbar_wait(&s.p_full[1], i & 1, abort_flag, p.status);
+        if (!ok) break;
+        tc_fence_after();
+        if (lane == 0) {
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            umma_ts(tmem + 384, tmem + 128 + ks * 8, desc_v(s.v[st], ks), kIdescPV,
+                    (i > 0 || ks > 0));
+        }
+        __syncwarp();
+      }
+      if (lane == 0) umma_commit(&s.kv_empty[st]);
+      if (has_b && more) {
+        if (lane == 0) {
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            umma_ss(tmem + 128, desc_kmajor(s.q[1], ks), desc_kmajor(s.k[st1], ks), kIdescQK,
+                    ks > 0);
+          umma_commit(&s.s_full[1]);
+        }
+      }
       __syncwarp();
-      g += nt;
-      tA += nt;
-      if (hb) tB += nt;
-      ++j;
     }
-    if (!ok) {
+    if (ok) {
+      if (lane == 0) umma_commit(&s.o_full);
+    } else {
       report(p.status, kErrTimeout);
       s.abort_flag = 1;
       if (issued_any) {
@@ -420,171 +360,165 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_q,
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_base + grp * 128;
     const uint32_t tO = tmem + lane_base + 256 + grp * 128;
-    const int R = p.R, W = p.window;
-    const int sh = (127 - r) & 3;
-    const int base = (127 - r) - sh;
-    const float2 sc2 = make_float2(p.scale, p.scale);
-    const float2 lg2 = make_float2(kLog2e, kLog2e);
-    int g = 0, tX = 0, j = 0;  // K/V tiles, this group's S/P phases, items
-    bool ok = true;
-    for (int idx = first; ok && idx < p.num_items; idx += stride) {
-      const Item it = item_geom(p, idx);
-      if (!it.valid) continue;
-      const bool active = grp == 0 || it.has_b;
-      const int h = it.h0 + grp;
-      const int L = it.L, P0 = it.P0;
+    const int h = h0 + grp;
+    if (grp == 0 || has_b) {
+      const float* brow = p.bias + (size_t)h * p.R;
+      const float bconst = __ldg(brow + p.R - 1);
+      const int R = p.R, W = p.window;
+      const int sh = (127 - r) & 3;
+      const int base = (127 - r) - sh;
       float m = -INFINITY;  // running max of the logits, natural units
       float2 l2 = make_float2(0.f, 0.f);
-      if (active) {
-        const float bconst = __ldg(p.bias + (size_t)h * R + R - 1);
-        for (int i = 0; i < it.ntiles; ++i) {
-          const int gi = g + i;
-          const int k0 = (it.kt_hi - i) * kTile;
-          const int delta = P0 - k0;
-          const bool clamped = delta - 127 >= R - 1;  // every distance past the table end
-          const bool masked = (delta < 127) || (W > 0 && delta + 127 > W - 1) || (k0 + 127 >= L);
-          const float* bias_buf = &s.bias[gi % kStages][grp][0][0];
-          if (!clamped && !mbar_wait(&s.b_full[gi % kStages], (gi / kStages) & 1, abort_flag, p.status)) {
-            ok = false;
-            break;
-          }
-          if (!mbar_wait(&s.s_full[grp], (tX + i) & 1, abort_flag, p.status)) { ok = false; break; }
-          tc_fence_after();
-          uint32_t sr[128];  // the S row; later the packed P pairs
-          tmem_ld32(tS + 0, sr);
-          tmem_ld32(tS + 32, sr + 32);
-          tmem_ld32(tS + 64, sr + 64);
-          tmem_ld32(tS + 96, sr + 96);
-          tmem_wait_ld();
-          reg_fence<128>(sr);
-          float2 x[64];  // logits in natural units, pairs of columns
-          const float4* bp = reinterpret_cast<const float4*>(bias_buf + sh * kBiasCopy + base);
-          const float2 bc2 = make_float2(bconst, bconst);
-#pragma unroll
-          for (int k = 0; k < 64; ++k) {
-            const float2 sv = make_float2(__uint_as_float(sr[2 * k]), __uint_as_float(sr[2 * k + 1]));
-            if (clamped) {
-              x[k] = __ffma2_rn(sv, sc2, bc2);
-            } else {
-              const float4 bv = bp[k >> 1];
-              x[k] = __ffma2_rn(sv, sc2, (k & 1) ? make_float2(bv.z, bv.w) : make_float2(bv.x, bv.y));
-            }
-          }
-          if (masked) {
-            const int dr = delta + r;  // distance at column 0
-            const int kend = L - k0;   // columns >= kend are past the sequence
-#pragma unroll
-            for (int k = 0; k < 64; ++k) {
-              const int c = 2 * k;
-              const int d = dr - c;
-              const bool a0 = d >= 0 && (W == 0 || d <= W - 1) && c < kend;
-              const bool a1 = d - 1 >= 0 && (W == 0 || d - 1 <= W - 1) && c + 1 < kend;
-              x[k].x = a0 ? x[k].x : -INFINITY;
-              x[k].y = a1 ? x[k].y : -INFINITY;
-            }
-          }
-          float mx0 = fmax3(x[0].x, x[0].y, x[1].x), mx1 = fmax3(x[1].y, x[2].x, x[2].y);
-          float mx2 = fmax3(x[3].x, x[3].y, x[4].x), mx3 = fmax3(x[4].y, x[5].x, x[5].y);
-#pragma unroll
-          for (int k = 6; k < 62; k += 4) {
-            mx0 = fmax3(mx0, x[k].x, x[k].y);
-            mx1 = fmax3(mx1, x[k + 1].x, x[k + 1].y);
-            mx2 = fmax3(mx2, x[k + 2].x, x[k + 2].y);
-            mx3 = fmax3(mx3, x[k + 3].x, x[k + 3].y);
-          }
-          mx0 = fmax3(mx0, x[62].x, x[62].y);
-          mx1 = fmax3(mx1, x[63].x, x[63].y);
-          const float m_new = fmax3(m, fmaxf(mx0, mx1), fmaxf(mx2, mx3));
-          const bool need = m_new > m + kRescaleThreshold || (m == -INFINITY && m_new > -INFINITY);
-          const float alpha = need ? ex2((m - m_new) * kLog2e) : 1.f;
-          if (need) {
-            l2.x *= alpha;
-            l2.y *= alpha;
-            m = m_new;
-          }
-          const float nm = m == -INFINITY ? 0.f : -m * kLog2e;  // p = 2^(x log2 e - m log2 e)
-          const float2 nm2 = make_float2(nm, nm);
-          // P as bf16 pairs, reusing the S registers
-#pragma unroll
-          for (int k = 0; k < 64; ++k) {
-            const float2 d2 = __ffma2_rn(x[k], lg2, nm2);
-            const float2 e2 = make_float2(ex2(d2.x), ex2(d2.y));
-            l2 = __fadd2_rn(l2, e2);
-            sr[k] = pack_bf16(e2.x, e2.y);
-          }
-          // rescale O (warp-wide, only when some row's max grew past the threshold)
-          if (__any_sync(0xffffffffu, need) && i > 0) {
-            // PV(i-1) was issued before S(i), so it is complete here
-            uint32_t orr[32];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              tmem_ld32(tO + c * 32, orr);
-              tmem_wait_ld();
-              reg_fence<32>(orr);
-#pragma unroll
-              for (int q = 0; q < 32; ++q) orr[q] = __float_as_uint(__uint_as_float(orr[q]) * alpha);
-              tmem_st32(tO + c * 32, orr);
-            }
-          }
-          tmem_st32(tS + 0, sr);
-          tmem_st32(tS + 32, sr + 32);
-          tmem_wait_st();
-          tc_fence_before();
-          mbar_arrive(&s.p_full[grp]);
+      const float2 sc2 = make_float2(p.scale, p.scale);
+      const float2 lg2 = make_float2(kLog2e, kLog2e);
+      bool ok = true;
+      for (int i = 0; i < ntiles; ++i) {
+        const int k0 = (kt_hi - i) * kTile;
+        const int delta = P0 - k0;
+        const bool clamped = delta - 127 >= R - 1;  // every distance past the table end
+        const bool masked = (delta < 127) || (W > 0 && delta + 127 > W - 1) || (k0 + 127 >= L);
+        const float* bias_buf = &s.bias[i % kStages][grp][0][0];
+        if (!clamped && !mbar_wait(&s.b_full[i % kStages], (i / kStages) & 1, abort_flag, p.status)) {
+          ok = false;
+          break;
         }
-        if (!ok) break;
+        if (!mbar_wait(&s.s_full[grp], i & 1, abort_flag, p.status)) { ok = false; break; }
+        tc_fence_after();
+        // S row in two halves: the second half's TMEM load overlaps work on the first
+        uint32_t sr[128];
+        tmem_ld32(tS + 0, sr);
+        tmem_ld32(tS + 32, sr + 32);
+        tmem_wait_ld();
+        reg_fence<64>(sr);
+        tmem_ld32(tS + 64, sr + 64);
+        tmem_ld32(tS + 96, sr + 96);
+        float2 x[64];  // logit * log2 e, pairs of columns
+        const float4* bp = reinterpret_cast<const float4*>(bias_buf + sh * kBiasCopy + base);
+        const float2 bc2 = make_float2(bconst, bconst);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          const float2 sv = make_float2(__uint_as_float(sr[2 * k]), __uint_as_float(sr[2 * k + 1]));
+          if (clamped) {
+            x[k] = __ffma2_rn(sv, sc2, bc2);
+          } else {
+            const float4 bv = bp[k >> 1];
+            x[k] = __ffma2_rn(sv, sc2, (k & 1) ? make_float2(bv.z, bv.w) : make_float2(bv.x, bv.y));
+          }
+        }
+        tmem_wait_ld();
+        reg_fence<64>(sr + 64);
+#pragma unroll
+        for (int k = 32; k < 64; ++k) {
+          const float2 sv = make_float2(__uint_as_float(sr[2 * k]), __uint_as_float(sr[2 * k + 1]));
+          if (clamped) {
+            x[k] = __ffma2_rn(sv, sc2, bc2);
+          } else {
+            const float4 bv = bp[k >> 1];
+            x[k] = __ffma2_rn(sv, sc2, (k & 1) ? make_float2(bv.z, bv.w) : make_float2(bv.x, bv.y));
+          }
+        }
+        if (masked) {
+          const int dr = delta + r;  // distance at column 0
+          const int kend = L - k0;   // columns >= kend are past the sequence
+#pragma unroll
+          for (int k = 0; k < 64; ++k) {
+            const int c = 2 * k;
+            const int d = dr - c;
+            const bool a0 = d >= 0 && (W == 0 || d <= W - 1) && c < kend;
+            const bool a1 = d - 1 >= 0 && (W == 0 || d - 1 <= W - 1) && c + 1 < kend;
+            x[k].x = a0 ? x[k].x : -INFINITY;
+            x[k].y = a1 ? x[k].y : -INFINITY;
+          }
+        }
+        float mx0 = fmax3(x[0].x, x[0].y, x[1].x), mx1 = fmax3(x[1].y, x[2].x, x[2].y);
+        float mx2 = fmax3(x[3].x, x[3].y, x[4].x), mx3 = fmax3(x[4].y, x[5].x, x[5].y);
+#pragma unroll
+        for (int k = 6; k < 62; k += 4) {
+          mx0 = fmax3(mx0, x[k].x, x[k].y);
+          mx1 = fmax3(mx1, x[k + 1].x, x[k + 1].y);
+          mx2 = fmax3(mx2, x[k + 2].x, x[k + 2].y);
+          mx3 = fmax3(mx3, x[k + 3].x, x[k + 3].y);
+        }
+        mx0 = fmax3(mx0, x[62].x, x[62].y);
+        mx1 = fmax3(mx1, x[63].x, x[63].y);
+        const float m_new = fmax3(m, fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+        const bool need = m_new > m + kRescaleThreshold || (m == -INFINITY && m_new > -INFINITY);
+        const float alpha = need ? ex2((m - m_new) * kLog2e) : 1.f;
+        if (need) {
+          l2.x *= alpha;
+          l2.y *= alpha;
+          m = m_new;
+        }
+        const float nm = m == -INFINITY ? 0.f : -m * kLog2e;  // p = 2^(x log2 e - m log2 e)
+        const float2 nm2 = make_float2(nm, nm);
+        // P as bf16 pairs, reusing the S registers
+#pragma unroll
+        for (int k = 0; k < 64; ++k) {
+          const float2 d2 = __ffma2_rn(x[k], lg2, nm2);
+          const float2 e2 = make_float2(ex2(d2.x), ex2(d2.y));
+          l2 = __fadd2_rn(l2, e2);
+          sr[k] = pack_bf16(e2.x, e2.y);
+        }
+        // rescale O (warp-wide, only when some row's max grew past the threshold)
+        if (__any_sync(0xffffffffu, need) && i > 0) {
+          // PV(i-1) was issued before S(i), so it is complete here
+          uint32_t orr[32];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            tmem_ld32(tO + c * 32, orr);
+            tmem_wait_ld();
+            reg_fence<32>(orr);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) orr[j] = __float_as_uint(__uint_as_float(orr[j]) * alpha);
+            tmem_st32(tO + c * 32, orr);
+          }
+        }
+        tmem_st32(tS + 0, sr);
+        tmem_st32(tS + 32, sr + 32);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&s.p_full[grp]);
       }
-      // epilogue: O of this item is final once o_full completes
-      if (!mbar_wait(&s.o_full, j & 1, abort_flag, p.status)) { ok = false; break; }
-      if (!active) {
-        mbar_arrive(&s.o_free);
+      const float l = l2.x + l2.y;
+      if (ok) ok = mbar_wait(&s.o_full, 0, abort_flag, p.status);
+      if (!ok) {
+        report(p.status, kErrTimeout);
+        s.abort_flag = 1;
       } else {
         tc_fence_after();
-        const float l = l2.x + l2.y;
         const float inv_l = 1.f / l;
-        const int t = it.t_glob0 + r;
-        const bool store = r < it.rows;
-        const size_t obase = ((size_t)t * p.Hq + h) * 128;
+        const int t = t_glob0 + r;
+        const bool store = r < rows;
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t orr[64];
-          tmem_ld32(tO + half * 64, orr);
-          tmem_ld32(tO + half * 64 + 32, orr + 32);
+        for (int c = 0; c < 4; ++c) {
+          uint32_t orr[32];
+          tmem_ld32(tO + c * 32, orr);
           tmem_wait_ld();
-          reg_fence<64>(orr);
-          if (half == 1) {
-            tc_fence_before();
-            mbar_arrive(&s.o_free);  // the next item's first PV may overwrite O now
-          }
-          if (!store) continue;
-          if (p.out_dtype == 0) {
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + obase + half * 64);
+          reg_fence<32>(orr);
+          if (store) {
+            const size_t obase = ((size_t)t * p.Hq + h) * 128 + c * 32;
+            if (p.out_dtype == 0) {
+              uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + obase);
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              uint4 w;
-              w.x = pack_bf16(__uint_as_float(orr[8 * q + 0]) * inv_l, __uint_as_float(orr[8 * q + 1]) * inv_l);
-              w.y = pack_bf16(__uint_as_float(orr[8 * q + 2]) * inv_l, __uint_as_float(orr[8 * q + 3]) * inv_l);
-              w.z = pack_bf16(__uint_as_float(orr[8 * q + 4]) * inv_l, __uint_as_float(orr[8 * q + 5]) * inv_l);
-              w.w = pack_bf16(__uint_as_float(orr[8 * q + 6]) * inv_l, __uint_as_float(orr[8 * q + 7]) * inv_l);
-              dst[q] = w;
+              for (int j = 0; j < 4; ++j) {
+                uint4 w;
+                w.x = pack_bf16(__uint_as_float(orr[8 * j + 0]) * inv_l, __uint_as_float(orr[8 * j + 1]) * inv_l);
+                w.y = pack_bf16(__uint_as_float(orr[8 * j + 2]) * inv_l, __uint_as_float(orr[8 * j + 3]) * inv_l);
+                w.z = pack_bf16(__uint_as_float(orr[8 * j + 4]) * inv_l, __uint_as_float(orr[8 * j + 5]) * inv_l);
+                w.w = pack_bf16(__uint_as_float(orr[8 * j + 6]) * inv_l, __uint_as_float(orr[8 * j + 7]) * inv_l);
+                dst[j] = w;
+              }
+            } else {
+              float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + obase);
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                dst[j] = make_float4(__uint_as_float(orr[4 * j + 0]) * inv_l, __uint_as_float(orr[4 * j + 1]) * inv_l,
+                                     __uint_as_float(orr[4 * j + 2]) * inv_l, __uint_as_float(orr[4 * j + 3]) * inv_l);
             }
-          } else {
-            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + obase + half * 64);
-#pragma unroll
-            for (int q = 0; q < 16; ++q)
-              dst[q] = make_float4(__uint_as_float(orr[4 * q + 0]) * inv_l, __uint_as_float(orr[4 * q + 1]) * inv_l,
-                                   __uint_as_float(orr[4 * q + 2]) * inv_l, __uint_as_float(orr[4 * q + 3]) * inv_l);
           }
         }
         if (store && p.lse != nullptr) p.lse[(size_t)t * p.Hq + h] = m + __log2f(l) * kLn2;
       }
-      g += it.ntiles;
-      if (active) tX += it.ntiles;
-      ++j;
-    }
-    if (!ok) {
-      report(p.status, kErrTimeout);
-      s.abort_flag = 1;
     }
   }
 
@@ -623,16 +557,9 @@ cudaError_t launch_prefill(const AttnArgs& a, const AttnMaps& maps, cudaStream_t
   p.max_q_len = a.max_q_len;
   p.num_blocks = a.num_blocks;
   p.scale = a.scale;
-  const long long items = (long long)p.q_tiles * p.B * p.head_pairs;
-  if (items == 0) return cudaSuccess;
-  if (items > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  p.num_items = (int)items;
-  // persistent: one CTA per SM (shared memory and TMEM admit no second one)
-  int dev = 0, sms = 0;
-  cudaError_t e0 = cudaGetDevice(&dev);
-  if (e0 == cudaSuccess) e0 = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (e0 != cudaSuccess) return e0;
-  const long long grid = items < sms ? items : sms;
+  const long long grid = (long long)p.q_tiles * p.B * p.head_pairs;
+  if (grid == 0) return cudaSuccess;
+  if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   const size_t smem = sizeof(Smem) + 1024;
   cudaError_t e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
