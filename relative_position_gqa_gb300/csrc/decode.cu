@@ -32,7 +32,9 @@ namespace decode {
 constexpr int kStages = 3;
 constexpr int kThreads = 192;
 constexpr int kMaxG = 16;
-constexpr int kBiasStride = 144;  // floats per staged head (>= 127 + 9)
+// floats per staged head (>= 127 + 9); 164 = 4 (mod 32), so the G heads x 4 tokens of a
+// warp (lane = t*G + g) hit distinct banks when they read column c
+constexpr int kBiasStride = 164;
 constexpr uint32_t kIdescQK = idesc_bf16(128, 128, false, false);
 constexpr uint32_t kIdescPV = idesc_bf16(128, 128, false, true);
 constexpr float kLog2e = 1.4426950408889634f;

@@ -24,9 +24,9 @@
 //
 // The relative bias ("sheared" along the tile diagonals): within a 128x128 tile the
 // distance is delta + r - c with delta = p0 - k0, so row r needs a contiguous run of the
-// table, reversed.  The stager warp puts the 255 values a tile needs in shared memory in
-// four copies shifted by one float each, so that every softmax thread reads its run with
-// aligned 16-byte loads.  Tiles whose smallest distance is already past R-1 use the single
+// table, reversed.  The stager warp puts the 255 values a tile needs in shared memory once,
+// in reversed order, so that at each column the 32 lanes of a warp read 32 consecutive
+// words (conflict-free 4-byte loads).  Tiles whose smallest distance is already past R-1 use the single
 // clamped value instead (no copies, no loads).  Logits are kept in natural units
 // (x = scale * q.k + b) and log2 e is folded into the exponent's FMA.  Key tiles are
 // visited from the diagonal backwards; only tiles that overlap the causal diagonal, the
@@ -56,7 +56,6 @@ constexpr int kSoftmaxRegs = 216;
 constexpr int kOtherRegs = 64;
 static_assert(2 * 128 * kSoftmaxRegs + 128 * kOtherRegs <= kThreads * kLaunchRegs,
               "register split exceeds the launch allocation");
-constexpr int kBiasCopy = 264;  // floats per shifted copy; 264/4 = 66 = 2 (mod 8) spreads banks
 constexpr uint32_t kIdescQK = idesc_bf16(128, 128, false, false);
 constexpr uint32_t kIdescPV = idesc_bf16(128, 128, false, true);
 constexpr float kLog2e = 1.4426950408889634f;
@@ -67,7 +66,7 @@ struct __align__(1024) Smem {
   uint8_t q[2][2][16384];        // [head slot][d half][128 rows x 128 B], swizzled
   uint8_t k[kStages][2][16384];  // [stage][d half][128 keys x 128 B]
   uint8_t v[kStages][2][16384];
-  float bias[kStages][2][4][kBiasCopy];  // [stage][head slot][shift][index], raw values
+  float bias[kStages][2][256];  // [stage][head slot][j]: rev[j] = b[h][clamp(delta + 127 - j)]
   uint64_t q_full;
   uint64_t k_full[kStages], v_full[kStages], kv_empty[kStages];
   uint64_t s_full[2], p_full[2], o_full, drain, b_full[kStages];
@@ -220,10 +219,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_q,
     }
    } else if (warp >= 10) {
     // ---------------------------------------------------------- bias stagers ---
-    // warp 10 stages head A's slices, warp 11 head B's, with 4-byte cp.async copies:
-    // copy_q[j - q] = rev[j] = b[h][clamp(delta + 127 - j, 0, R-1)], j < 256, q < 4,
-    // so every softmax thread can read its reversed diagonal run with aligned 16-byte
-    // loads.  Both warps arrive on b_full[stage] for every tile (count 64).
+    // warp 10 stages head A's slice, warp 11 head B's, with 4-byte cp.async copies:
+    // rev[j] = b[h][clamp(delta + 127 - j, 0, R-1)], j < 256, so softmax thread r reads its
+    // run rev[127 - r + c], c = 0..127, and a warp's 32 lanes read 32 consecutive words
+    // (no bank conflicts).  Both warps arrive on b_full[stage] for every tile (count 64).
     const int slot = warp - 10;
     const bool mine = slot == 0 || has_b;
     const float* brow = p.bias + (size_t)(h0 + slot) * p.R;
@@ -237,16 +236,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_q,
       if (!ok) break;
       const int delta = P0 - (kt_hi - i) * kTile;
       if (mine && delta - 127 < R - 1) {
-        float* dst = &s.bias[st][slot][0][0];
-#pragma unroll 4
-        for (int e = lane; e < 4 * 256; e += 32) {
-          const int q = e >> 8, jj = e & 255;  // copy q, entry jj holds rev[jj + q]
-          const int j = jj + q;
-          if (j < 256) {
-            int d = delta + 127 - j;
-            d = d < 0 ? 0 : (d > R - 1 ? R - 1 : d);
-            cp_async_4(dst + q * kBiasCopy + jj, brow + d);
-          }
+        float* dst = &s.bias[st][slot][0];
+#pragma unroll
+        for (int j = lane; j < 256; j += 32) {
+          int d = delta + 127 - j;
+          d = d < 0 ? 0 : (d > R - 1 ? R - 1 : d);
+          cp_async_4(dst + j, brow + d);
         }
       }
       cp_async_mbar_arrive(&s.b_full[st]);
@@ -365,8 +360,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_q,
       const float* brow = p.bias + (size_t)h * p.R;
       const float bconst = __ldg(brow + p.R - 1);
       const int R = p.R, W = p.window;
-      const int sh = (127 - r) & 3;
-      const int base = (127 - r) - sh;
       float m = -INFINITY;  // running max of the logits, natural units
       float2 l2 = make_float2(0.f, 0.f);
       const float2 sc2 = make_float2(p.scale, p.scale);
@@ -377,7 +370,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_q,
         const int delta = P0 - k0;
         const bool clamped = delta - 127 >= R - 1;  // every distance past the table end
         const bool masked = (delta < 127) || (W > 0 && delta + 127 > W - 1) || (k0 + 127 >= L);
-        const float* bias_buf = &s.bias[i % kStages][grp][0][0];
+        const float* bias_buf = &s.bias[i % kStages][grp][0];
         if (!clamped && !mbar_wait(&s.b_full[i % kStages], (i / kStages) & 1, abort_flag, p.status)) {
           ok = false;
           break;
@@ -393,7 +386,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_q,
         tmem_ld32(tS + 64, sr + 64);
         tmem_ld32(tS + 96, sr + 96);
         float2 x[64];  // logit * log2 e, pairs of columns
-        const float4* bp = reinterpret_cast<const float4*>(bias_buf + sh * kBiasCopy + base);
+        const float* rb = bias_buf + (127 - r);  // rb[c] = bias at distance delta + r - c
         const float2 bc2 = make_float2(bconst, bconst);
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
@@ -401,8 +394,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_q,
           if (clamped) {
             x[k] = __ffma2_rn(sv, sc2, bc2);
           } else {
-            const float4 bv = bp[k >> 1];
-            x[k] = __ffma2_rn(sv, sc2, (k & 1) ? make_float2(bv.z, bv.w) : make_float2(bv.x, bv.y));
+            x[k] = __ffma2_rn(sv, sc2, make_float2(rb[2 * k], rb[2 * k + 1]));
           }
         }
         tmem_wait_ld();
@@ -413,8 +405,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_q,
           if (clamped) {
             x[k] = __ffma2_rn(sv, sc2, bc2);
           } else {
-            const float4 bv = bp[k >> 1];
-            x[k] = __ffma2_rn(sv, sc2, (k & 1) ? make_float2(bv.z, bv.w) : make_float2(bv.x, bv.y));
+            x[k] = __ffma2_rn(sv, sc2, make_float2(rb[2 * k], rb[2 * k + 1]));
           }
         }
         if (masked) {
