@@ -68,7 +68,9 @@ struct __align__(1024) Smem {
   uint8_t v[kStages][2][16384];
   float bias[kStages][2][256];  // [stage][head slot][j]: rev[j] = b[h][clamp(delta + 127 - j)]
   uint64_t q_full;
-  uint64_t k_full[kStages], v_full[kStages], kv_empty[kStages];
+  // a K stage is free once the tile's last QK^T is done, a V stage once its last PV is
+  // done: K for the next tile is fetched while the current tile's softmax and PV run
+  uint64_t k_full[kStages], v_full[kStages], k_empty[kStages], v_empty[kStages];
   uint64_t s_full[2], p_full[2], o_full, drain, b_full[kStages];
   uint32_t tmem_base;
   int abort_flag;
@@ -153,7 +155,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_q,
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&s.k_full[i], 1);
       mbar_init(&s.v_full[i], 1);
-      mbar_init(&s.kv_empty[i], 1);
+      mbar_init(&s.k_empty[i], 1);
+      mbar_init(&s.v_empty[i], 1);
       mbar_init(&s.b_full[i], 64);
     }
     for (int i = 0; i < 2; ++i) {
@@ -192,7 +195,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_q,
       int issued = 0;
       for (int i = 0; i < ntiles; ++i) {
         const int st = i % kStages;
-        if (i >= kStages && !mbar_wait(&s.kv_empty[st], ((i / kStages) - 1) & 1, abort_flag, p.status)) {
+        const uint32_t eph = ((i / kStages) - 1) & 1;
+        if (i >= kStages && !mbar_wait(&s.k_empty[st], eph, abort_flag, p.status)) {
           report(p.status, kErrTimeout);
           s.abort_flag = 1;
           break;
@@ -201,6 +205,14 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_q,
         mbar_arrive_expect_tx(&s.k_full[st], 32768u);
         tma_load_3d(s.k[st][0], &map_k, &s.k_full[st], 0, 0, page);
         tma_load_3d(s.k[st][1], &map_k, &s.k_full[st], 64, 0, page);
+        if (i >= kStages && !mbar_wait(&s.v_empty[st], eph, abort_flag, p.status)) {
+          report(p.status, kErrTimeout);
+          s.abort_flag = 1;
+          issued = i;  // this tile's K is in flight too: let it land
+          volatile int never = 0;
+          mbar_wait(&s.k_full[st], (i / kStages) & 1, &never);
+          break;
+        }
         mbar_arrive_expect_tx(&s.v_full[st], 32768u);
         tma_load_3d(s.v[st][0], &map_v, &s.v_full[st], 0, 0, page);
         tma_load_3d(s.v[st][1], &map_v, &s.v_full[st], 64, 0, page);
@@ -231,7 +243,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_q,
       const int st = i % kStages;
       int ok = 1;
       if (lane == 0 && i >= kStages)
-        ok = mbar_wait(&s.kv_empty[st], ((i / kStages) - 1) & 1, abort_flag, p.status);
+        ok = mbar_wait(&s.v_empty[st], ((i / kStages) - 1) & 1, abort_flag, p.status);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       const int delta = P0 - (kt_hi - i) * kTile;
@@ -266,6 +278,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_q,
                     ks > 0);
           umma_commit(&s.s_full[1]);
         }
+        umma_commit(&s.k_empty[0]);  // tile 0's K has been read by both QK^T
       }
       issued_any = true;
       __syncwarp();
@@ -320,15 +333,16 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_q,
         }
         __syncwarp();
       }
-      if (lane == 0) umma_commit(&s.kv_empty[st]);
-      if (has_b && more) {
-        if (lane == 0) {
+      if (lane == 0) {
+        umma_commit(&s.v_empty[st]);  // both PV of tile i are issued
+        if (has_b && more) {
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
             umma_ss(tmem + 128, desc_kmajor(s.q[1], ks), desc_kmajor(s.k[st1], ks), kIdescQK,
                     ks > 0);
           umma_commit(&s.s_full[1]);
         }
+        if (more) umma_commit(&s.k_empty[st1]);  // both QK^T of tile i+1 are issued
       }
       __syncwarp();
     }
