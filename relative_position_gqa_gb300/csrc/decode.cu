@@ -196,12 +196,14 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
       const int dmax = (L - 1) - k0;                 // largest distance in the page
       if ((L - n) - k0 - 127 < R - 1) {              // not every distance clamped
         // head g: slot j holds b[kvh*G + g][clamp(dmax - j, 0, R-1)], j < 127 + n
-        float* dst = s.bias[st];
-        for (int e = lane; e < p.G * span; e += 32) {
-          const int gg = e / span, j = e % span;
-          int d = dmax - j;
-          d = d < 0 ? 0 : (d > R - 1 ? R - 1 : d);
-          cp_async_4(dst + gg * kBiasStride + j, p.bias + (size_t)(kvh * p.G + gg) * R + d);
+        for (int gg = 0; gg < p.G; ++gg) {
+          float* dst = s.bias[st] + gg * kBiasStride;
+          const float* src = p.bias + (size_t)(kvh * p.G + gg) * R;
+          for (int j = lane; j < span; j += 32) {
+            int d = dmax - j;
+            d = d < 0 ? 0 : (d > R - 1 ? R - 1 : d);
+            cp_async_4(dst + j, src + d);
+          }
         }
       }
       cp_async_mbar_arrive(&s.b_full[st]);
@@ -351,9 +353,14 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
           sr[c] = __float_as_uint(fmaf(__uint_as_float(sr[c]), p.scale, bconst));
       } else {
         const float* bp = bias_buf + g * kBiasStride + (n - 1 - t);
+        // 32 columns at a time: keeps the compiler from hoisting all 128 bias loads
 #pragma unroll
-        for (int c = 0; c < 128; ++c)
-          sr[c] = __float_as_uint(fmaf(__uint_as_float(sr[c]), p.scale, bp[c]));
+        for (int cb = 0; cb < 128; cb += 32) {
+#pragma unroll
+          for (int c = cb; c < cb + 32; ++c)
+            sr[c] = __float_as_uint(fmaf(__uint_as_float(sr[c]), p.scale, bp[c]));
+          asm volatile("" ::: "memory");
+        }
       }
       if (masked) {
         const int d0 = pq - k0;

@@ -212,6 +212,43 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
       INK_W8(0), INK_W8(8)
       : "memory");
 }
+// 16 lanes x 256 bits, 16 repetitions (128 columns): thread t gets, for chunk j = 0..15,
+// r[4j..4j+3] = (lane t/4, col 8j + 2(t%4)), (lane t/4, col 8j + 2(t%4) + 1),
+//               (lane t/4 + 8, col 8j + 2(t%4)), (lane t/4 + 8, col 8j + 2(t%4) + 1).
+__device__ __forceinline__ void tmem_ld_16x256b_x16(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, "
+      "%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, "
+      "%48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%64];"
+      : INK_R8(0), INK_R8(8), INK_R8(16), INK_R8(24), INK_R8(32), INK_R8(40), INK_R8(48),
+        INK_R8(56)
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st_16x256b_x16(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.16x256b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, "
+      "%33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, "
+      "%49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63, %64};" ::"r"(
+          taddr),
+      INK_W8(0), INK_W8(8), INK_W8(16), INK_W8(24), INK_W8(32), INK_W8(40), INK_W8(48),
+      INK_W8(56)
+      : "memory");
+}
+// 16 lanes x 128 bits, 16 repetitions (64 columns): thread t writes, for chunk j,
+// r[2j] -> (lane t/4, col 4j + t%4), r[2j+1] -> (lane t/4 + 8, col 4j + t%4).
+__device__ __forceinline__ void tmem_st_16x128b_x16(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.16x128b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(
+          taddr),
+      INK_W8(0), INK_W8(8), INK_W8(16), INK_W8(24)
+      : "memory");
+}
 #undef INK_R8
 #undef INK_W8
 
