@@ -52,6 +52,11 @@ def lib():
         L.oracle_sconv_kv.restype = ctypes.c_int
         L.oracle_sconv_kv.argtypes = [P, P, P, P, P, P, P, P, P, ctypes.c_int, ctypes.c_int,
                                       ctypes.c_int, ctypes.c_int64]
+        L.oracle_sconv_dense.restype = ctypes.c_int
+        L.oracle_sconv_dense.argtypes = [P, P, P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int]
+        L.oracle_sconv_rollback.restype = ctypes.c_int
+        L.oracle_sconv_rollback.argtypes = [P, P, P, P, P, P, ctypes.c_int, ctypes.c_int,
+                                            ctypes.c_int]
         L.oracle_rel_attn.restype = ctypes.c_int
         L.oracle_rel_attn.argtypes = [P, P, P, P, ctypes.c_int, P, P, P, ctypes.c_int,
                                       ctypes.c_double, ctypes.c_int, ctypes.c_int, ctypes.c_int,
@@ -144,3 +149,40 @@ def rel_attn(q, k_cache, v_cache, block_table, cu_q_lens, seq_lens, bias, *, sca
     if rc != 0:
         raise RuntimeError(f"oracle_rel_attn: {STATUS.get(rc, rc)}")
     return out, lse
+
+
+def sconv_dense(x, w, state, cu_q_lens):
+    """Sconv on one dense stream: returns y [T, C] bf16; `state` [B, 3, C] updated in place."""
+    assert state.is_contiguous() and state.dtype == torch.bfloat16 and state.device.type == "cpu"
+    xa = _u16(x)
+    wa = _arr(w, np.float32)
+    st = state.view(torch.int16).numpy().view(np.uint16)
+    cu = _arr(cu_q_lens, np.int32)
+    T, C = xa.shape
+    y = torch.empty((T, C), dtype=torch.bfloat16)
+    ya = y.view(torch.int16).numpy().view(np.uint16)
+    rc = lib().oracle_sconv_dense(_ptr(xa), _ptr(wa), _ptr(st), _ptr(cu), _ptr(ya),
+                                  cu.shape[0] - 1, T, C)
+    if rc != 0:
+        raise RuntimeError(f"oracle_sconv_dense: {STATUS.get(rc, rc)}")
+    return y
+
+
+def sconv_rollback(state_before, x0, x1, cu_q_lens, accepted):
+    """Sconv state after keeping only the first accepted[b] new tokens of a step.
+
+    streams = 2 when x1 is given (K/V pair state [B, 2, 3, C]), else 1 ([B, 3, C])."""
+    sb = _u16(state_before)
+    a0 = _u16(x0)
+    a1 = _u16(x1) if x1 is not None else a0
+    cu = _arr(cu_q_lens, np.int32)
+    acc = _arr(accepted, np.int32)
+    streams = 2 if x1 is not None else 1
+    C = a0.shape[1]
+    out = torch.empty(tuple(state_before.shape), dtype=torch.bfloat16)
+    oa = out.view(torch.int16).numpy().view(np.uint16)
+    rc = lib().oracle_sconv_rollback(_ptr(sb), _ptr(a0), _ptr(a1), _ptr(cu), _ptr(acc),
+                                     _ptr(oa), cu.shape[0] - 1, C, streams)
+    if rc != 0:
+        raise RuntimeError(f"oracle_sconv_rollback: {STATUS.get(rc, rc)}")
+    return out

@@ -261,3 +261,76 @@ int oracle_rel_attn(const uint16_t *q, const uint16_t *k_cache, const uint16_t *
     for (int i = 0; i < started; ++i) pthread_join(th[i], NULL);
     return jb.status;
 }
+
+/* ------------------------------------------------- sconv on a dense stream ---- */
+
+/*
+ * The same window-4 causal conv on one dense stream (the blog's "Model Architecture /
+ * Sconv" also applies sconv to the attention output and the MoE output), with its own
+ * 3-row cache and a dense output:
+ *   x~ = [state[b] rows 0..2 ; new rows of b],  y[t] = bf16(sum_j w[c][j] x~[t + j])
+ *   state[b] <- last 3 rows of x~
+ * x, y [T][C] bf16; w [C][4]; state [B][3][C] bf16 (in/out).
+ */
+int oracle_sconv_dense(const uint16_t *x, const float *w, uint16_t *state,
+                       const int32_t *cu_q_lens, uint16_t *y, int B, int T, int C)
+{
+    if (B < 0 || T < 0 || C <= 0) return OR_ERR_ARG;
+    if (cu_q_lens[0] != 0 || cu_q_lens[B] != T) return OR_ERR_ARG;
+    for (int b = 0; b < B; ++b) {
+        const int t0 = cu_q_lens[b];
+        const int n = cu_q_lens[b + 1] - t0;
+        if (n < 0) return OR_ERR_ARG;
+        uint16_t *st = state + (size_t)b * 3 * C;
+        uint16_t *ext = malloc(sizeof(uint16_t) * (size_t)(n + 3) * C);
+        if (!ext) return OR_ERR_NOMEM;
+        memcpy(ext, st, sizeof(uint16_t) * 3 * (size_t)C);
+        memcpy(ext + 3 * (size_t)C, x + (size_t)t0 * C, sizeof(uint16_t) * (size_t)n * C);
+        for (int t = 0; t < n; ++t)
+            for (int c = 0; c < C; ++c) {
+                double acc = 0.0;
+                for (int j = 0; j < OR_TAPS; ++j)
+                    acc += (double)w[(size_t)c * OR_TAPS + j] *
+                           oracle_bf16_to_double(ext[(size_t)(t + j) * C + c]);
+                y[(size_t)(t0 + t) * C + c] = oracle_bf16_round(acc);
+            }
+        memcpy(st, ext + (size_t)n * C, sizeof(uint16_t) * 3 * (size_t)C);
+        free(ext);
+    }
+    return OR_OK;
+}
+
+/*
+ * Sconv-cache rollback after a speculative (MTP) verify step (blog, "Model Architecture /
+ * MTP" and "Re-computing MTP KV cache": drafts can be rejected): only the first
+ * accepted[b] of the step's n_b new tokens are kept, so the cache must hold the last 3 raw
+ * rows of [state before the step ; the first accepted[b] new rows].  streams = 2 for the
+ * K/V pair layout of oracle_sconv_kv ([B][2][3][C] state, k and v rows), 1 for a dense
+ * stream ([B][3][C], rows in x0).  The conv outputs of the kept tokens need no change:
+ * the conv is causal.
+ */
+int oracle_sconv_rollback(const uint16_t *state_before, const uint16_t *x0,
+                          const uint16_t *x1, const int32_t *cu_q_lens,
+                          const int32_t *accepted, uint16_t *state_after, int B, int C,
+                          int streams)
+{
+    if (B < 0 || C <= 0 || (streams != 1 && streams != 2)) return OR_ERR_ARG;
+    for (int b = 0; b < B; ++b) {
+        const int t0 = cu_q_lens[b];
+        const int n = cu_q_lens[b + 1] - t0;
+        const int a = accepted[b];
+        if (n < 0 || a < 0 || a > n) return OR_ERR_ARG;
+        for (int s = 0; s < streams; ++s) {
+            const uint16_t *x = s == 0 ? x0 : x1;
+            const uint16_t *sb = state_before + ((size_t)b * streams + s) * 3 * C;
+            uint16_t *sa = state_after + ((size_t)b * streams + s) * 3 * C;
+            for (int r = 0; r < 3; ++r) {
+                /* row r of the new state is row (a + r) of [state_before ; kept rows] */
+                const int e = a + r;
+                const uint16_t *src = e < 3 ? sb + (size_t)e * C : x + (size_t)(t0 + e - 3) * C;
+                memcpy(sa + (size_t)r * C, src, sizeof(uint16_t) * (size_t)C);
+            }
+        }
+    }
+    return OR_OK;
+}

@@ -174,3 +174,80 @@ def test_linearity_in_taps():
         kc, _, _ = _run(case)
         outs.append(_gather_new(kc, case).double())
     assert torch.equal(outs[0] + outs[1], outs[2])
+
+
+# ------------------------------------------------ dense stream and MTP rollback ----
+
+def _dense_case(q_lens=(7, 2, 40), C=64, seed=18, state_random=True):
+    g = torch.Generator().manual_seed(seed)
+    T = sum(q_lens)
+    x = torch.randn(T, C, generator=g).to(torch.bfloat16)
+    w = (torch.randn(C, 4, generator=g) * 0.5).float()
+    st = (torch.randn(len(q_lens), 3, C, generator=g) if state_random
+          else torch.zeros(len(q_lens), 3, C)).to(torch.bfloat16)
+    cu = torch.tensor([0] + list(np.cumsum(q_lens)), dtype=torch.int32)
+    return x, w, st, cu
+
+
+def test_dense_sconv_equals_the_k_stream_of_sconv_kv():
+    """The dense-stream conv and the paged K/V conv are the same definition."""
+    case = W.make_case(_spec(q_lens=(7, 2, 19)), seed=19)
+    kc, _, st = _run(case)
+    st_d = case.state[:, 0].clone().contiguous()
+    y = oracle.sconv_dense(case.k_raw, case.w_k, st_d, case.cu_q_lens)
+    assert torch.equal(_gather_new(kc, case).view(torch.int16), y.view(torch.int16))
+    assert torch.equal(st[:, 0].contiguous().view(torch.int16), st_d.view(torch.int16))
+
+
+@pytest.mark.parametrize("taps,shift", [([0, 0, 0, 1], 0), ([1, 0, 0, 0], 3), ([0, 0, 1, 0], 1)])
+def test_dense_sconv_one_hot_taps(taps, shift):
+    x, _, st, cu = _dense_case()
+    w = torch.tensor(taps, dtype=torch.float32).repeat(x.shape[1], 1)
+    y = oracle.sconv_dense(x, w, st.clone(), cu)
+    c = cu.tolist()
+    for b in range(len(c) - 1):
+        ext = torch.cat([st[b], x[c[b]:c[b + 1]]])
+        n = c[b + 1] - c[b]
+        assert torch.equal(y[c[b]:c[b + 1]].view(torch.int16), ext[3 - shift:3 - shift + n].view(torch.int16))
+
+
+def test_dense_sconv_within_half_ulp_of_brute_force():
+    x, w, st, cu = _dense_case(q_lens=(11, 5), C=32)
+    y = oracle.sconv_dense(x, w, st.clone(), cu).double()
+    c = cu.tolist()
+    for b in range(len(c) - 1):
+        ref = torch.tensor(brute.sconv_rows(st[b].double().tolist(), x[c[b]:c[b + 1]].double().tolist(),
+                                            w.double().tolist()), dtype=torch.float64)
+        half_ulp = torch.exp2(torch.floor(torch.log2(ref.abs().clamp_min(2.0 ** -126))) - 8)
+        assert (y[c[b]:c[b + 1]] - ref).abs().le(half_ulp).all()
+
+
+@pytest.mark.parametrize("accepted", [[7, 2, 40], [0, 0, 0], [3, 1, 17], [1, 2, 2]])
+def test_rollback_equals_running_only_the_kept_tokens(accepted):
+    """After a step of n_b tokens of which only the first a_b are kept, the cache must be
+    what a step of just those a_b tokens would have left (rows of the conv are causal)."""
+    x, w, st0, cu = _dense_case(q_lens=(7, 2, 40))
+    st_full = st0.clone()
+    oracle.sconv_dense(x, w, st_full, cu)
+    rolled = oracle.sconv_rollback(st0, x, None, cu, torch.tensor(accepted, dtype=torch.int32))
+    c = cu.tolist()
+    keep = torch.cat([torch.arange(c[b], c[b] + a) for b, a in enumerate(accepted)])
+    cu_keep = torch.tensor([0] + list(np.cumsum(accepted)), dtype=torch.int32)
+    st_keep = st0.clone()
+    oracle.sconv_dense(x[keep], w, st_keep, cu_keep)
+    assert torch.equal(rolled.view(torch.int16), st_keep.view(torch.int16))
+    if accepted == [7, 2, 40]:
+        assert torch.equal(rolled.view(torch.int16), st_full.view(torch.int16))
+    if accepted == [0, 0, 0]:
+        assert torch.equal(rolled.view(torch.int16), st0.view(torch.int16))
+
+
+def test_rollback_kv_pair_layout():
+    case = W.make_case(_spec(q_lens=(9, 9, 4)), seed=20)
+    acc = torch.tensor([4, 9, 0], dtype=torch.int32)
+    rolled = oracle.sconv_rollback(case.state, case.k_raw, case.v_raw, case.cu_q_lens, acc)
+    c = case.cu_q_lens.tolist()
+    for b in range(3):
+        for which, raw in ((0, case.k_raw), (1, case.v_raw)):
+            ext = torch.cat([case.state[b, which], raw[c[b]:c[b] + int(acc[b])]])
+            assert torch.equal(rolled[b, which].view(torch.int16), ext[-3:].view(torch.int16))
