@@ -114,6 +114,47 @@ INKLING_API int inkling_sconv_kv(const void *k_raw, const void *v_raw, const flo
                      inkling_stream_t stream);
 
 /*
+ * inkling_sconv — the same window-4 causal short convolution on one dense stream with
+ * its own 3-row cache (blog, "Model Architecture / Sconv": the conv also follows the
+ * attention output projection, "all-reduce (after o_proj) -> sconv -> residual").
+ *
+ *   x[T][C] bf16 raw rows, w[C][4] fp32 taps, sconv_state[B][3][C] bf16 (in/out, raw rows,
+ *   oldest first), y[T][C] bf16 out.
+ *   x~ = [sconv_state[b] ; new rows of b];  y[t][c] = bf16_rne(sum_j w[c][j] * x~[t + j][c]);
+ *   sconv_state[b] = the last 3 rows of x~.
+ *
+ * C % 8 == 0; y must not be x.  T = cu_q_lens[B]; max_q_len >= every n_b.  Device
+ * errors: n_b > max_q_len, or cu_q_lens not monotone or past T -> INKLING_ERR_BAD_INPUT.
+ */
+INKLING_API int inkling_sconv(const void *x, const float *w, void *sconv_state, const int32_t *cu_q_lens,
+                  void *y, int32_t B, int32_t T, int32_t C, int32_t max_q_len,
+                  int32_t *dev_status, inkling_stream_t stream);
+
+/*
+ * inkling_sconv_state_rollback — the sconv cache after a speculative (MTP verify) step
+ * of which only the first accepted[b] of its n_b new tokens are kept (blog, "Model
+ * Architecture / MTP" and "Re-computing MTP KV cache": drafts past the first rejection
+ * are dropped).  The conv is causal, so the cache rows written for the kept tokens are
+ * already right; only the 3-row state must be recomputed:
+ *
+ *   state_after[b][s] = the last 3 rows of [state_before[b][s] ; raw rows
+ *                       cu_q_lens[b] .. cu_q_lens[b] + accepted[b] - 1 of stream s]
+ *
+ * streams = 2: the K/V pair, x0 = k_raw, x1 = v_raw, state [B][2][3][C] (the layout of
+ * inkling_sconv_kv); streams = 1: one dense stream, x1 unused, state [B][3][C].
+ * state_before is the state as it was before the step's conv call (the caller keeps that
+ * copy: 3*C*streams*2 bytes per sequence); state_after may be the same buffer.  accepted
+ * is a device array [B] (0 <= accepted[b] <= n_b, else INKLING_ERR_BAD_INPUT and the
+ * sequence's state is left unwritten); accepted[b] = n_b reproduces the conv call's own
+ * state update.  T = cu_q_lens[B].  The pages state the requirement, not an API: the
+ * entry point itself is this library's.
+ */
+INKLING_API int inkling_sconv_state_rollback(const void *state_before, const void *x0, const void *x1,
+                                 const int32_t *cu_q_lens, const int32_t *accepted,
+                                 void *state_after, int32_t B, int32_t T, int32_t C,
+                                 int32_t streams, int32_t *dev_status, inkling_stream_t stream);
+
+/*
  * inkling_rel_attn_prefill — relative-bias GQA attention (blog, "Model Architecture /
  * Attention") for every new token of every sequence, reading keys and values from the
  * paged cache (so a cached prefix is attended to as well: chunked prefill).

@@ -63,6 +63,42 @@ def sconv_kv(k_raw: torch.Tensor, v_raw: torch.Tensor, w_k: torch.Tensor, w_v: t
                   dev_status, _stream(stream))
 
 
+def sconv(x: torch.Tensor, w: torch.Tensor, sconv_state: torch.Tensor, cu_q_lens: torch.Tensor,
+          *, max_q_len: int, y: Optional[torch.Tensor] = None, dev_status=None,
+          stream=None) -> torch.Tensor:
+    """inkling_sconv: the conv on one dense stream x [T, C] with its own state [B, 3, C]
+    (updated in place); returns y [T, C] bf16 (allocated when not given)."""
+    if y is None:
+        y = torch.empty_like(x)
+    dev = _check_cuda(x, w, sconv_state, cu_q_lens, y, dev_status)
+    assert x.dtype == sconv_state.dtype == y.dtype == torch.bfloat16 and w.dtype == torch.float32
+    assert cu_q_lens.dtype == torch.int32
+    with torch.cuda.device(dev):
+        _lib.call("inkling_sconv", x, w, sconv_state, cu_q_lens, y, cu_q_lens.shape[0] - 1,
+                  x.shape[0], x.shape[1], int(max_q_len), dev_status, _stream(stream))
+    return y
+
+
+def sconv_state_rollback(state_before: torch.Tensor, x0: torch.Tensor,
+                         x1: Optional[torch.Tensor], cu_q_lens: torch.Tensor,
+                         accepted: torch.Tensor, state_after: Optional[torch.Tensor] = None, *,
+                         dev_status=None, stream=None) -> torch.Tensor:
+    """inkling_sconv_state_rollback: the sconv state after keeping only the first
+    accepted[b] new tokens of a step.  With x1 (v_raw) the state is the K/V pair layout
+    [B, 2, 3, C]; without it, one stream [B, 3, C].  state_after may be state_before."""
+    if state_after is None:
+        state_after = torch.empty_like(state_before)
+    dev = _check_cuda(state_before, x0, x1, cu_q_lens, accepted, state_after, dev_status)
+    assert state_before.dtype == state_after.dtype == x0.dtype == torch.bfloat16
+    assert cu_q_lens.dtype == accepted.dtype == torch.int32
+    streams = 2 if x1 is not None else 1
+    with torch.cuda.device(dev):
+        _lib.call("inkling_sconv_state_rollback", state_before, x0, x1, cu_q_lens, accepted,
+                  state_after, cu_q_lens.shape[0] - 1, x0.shape[0], x0.shape[1], streams,
+                  dev_status, _stream(stream))
+    return state_after
+
+
 def _attn_common(q, k_cache, v_cache, block_table, cu_q_lens, seq_lens, bias, out, lse,
                  dev_status):
     dev = _check_cuda(q, k_cache, v_cache, block_table, cu_q_lens, seq_lens, bias, out, lse,

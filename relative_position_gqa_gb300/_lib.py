@@ -18,6 +18,8 @@ SZ = ctypes.c_size_t
 # name -> argument types, in the order of include/inkling.h
 SIGNATURES = {
     "inkling_sconv_kv": [P, P, P, P, P, P, P, P, P, I32, I32, I32, I64, I32, P, P],
+    "inkling_sconv": [P, P, P, P, P, I32, I32, I32, I32, P, P],
+    "inkling_sconv_state_rollback": [P, P, P, P, P, P, I32, I32, I32, I32, P, P],
     "inkling_rel_attn_prefill": [P, P, P, P, I32, P, P, P, I32, F32, I32, P, I32, P, I32, I32,
                                  I32, I32, I64, I32, P, P],
     "inkling_rel_attn_decode_workspace_size": [I32, I32, I32, I32, I32, I32, I32],

@@ -128,6 +128,43 @@ int inkling_sconv_kv(const void* k_raw, const void* v_raw, const float* w_k, con
              : INKLING_ERR_CUDA;
 }
 
+int inkling_sconv(const void* x, const float* w, void* sconv_state, const int32_t* cu_q_lens,
+                  void* y, int32_t B, int32_t T, int32_t C, int32_t max_q_len,
+                  int32_t* dev_status, inkling_stream_t stream) {
+  if (B < 0 || T < 0 || C <= 0 || C % 8 != 0 || max_q_len < 0) return INKLING_ERR_INVALID_ARG;
+  if (B == 0 || T == 0 || max_q_len == 0) return INKLING_OK;
+  if (!x || !w || !sconv_state || !cu_q_lens || !y) return INKLING_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w) || !aligned16(sconv_state) || !aligned16(y))
+    return INKLING_ERR_INVALID_ARG;
+  if (x == y) return INKLING_ERR_INVALID_ARG;
+  if (B > 65535 || (max_q_len + 31) / 32 > 65535) return INKLING_ERR_UNSUPPORTED;
+  ink::SconvDenseArgs a{x, w, sconv_state, cu_q_lens, y, B, T, C, max_q_len, dev_status};
+  return ink::launch_sconv_dense(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? INKLING_OK
+             : INKLING_ERR_CUDA;
+}
+
+int inkling_sconv_state_rollback(const void* state_before, const void* x0, const void* x1,
+                                 const int32_t* cu_q_lens, const int32_t* accepted,
+                                 void* state_after, int32_t B, int32_t T, int32_t C,
+                                 int32_t streams, int32_t* dev_status,
+                                 inkling_stream_t stream) {
+  if (B < 0 || T < 0 || C <= 0 || C % 8 != 0 || (streams != 1 && streams != 2))
+    return INKLING_ERR_INVALID_ARG;
+  if (B == 0) return INKLING_OK;
+  if (!state_before || !x0 || !cu_q_lens || !accepted || !state_after) return INKLING_ERR_INVALID_ARG;
+  if (streams == 2 && !x1) return INKLING_ERR_INVALID_ARG;
+  if (!aligned16(state_before) || !aligned16(x0) || (streams == 2 && !aligned16(x1)) ||
+      !aligned16(state_after))
+    return INKLING_ERR_INVALID_ARG;
+  if (B > 65535) return INKLING_ERR_UNSUPPORTED;
+  ink::SconvRollbackArgs a{state_before, x0, streams == 2 ? x1 : nullptr, cu_q_lens, accepted,
+                           state_after, B, T, C, streams, dev_status};
+  return ink::launch_sconv_rollback(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? INKLING_OK
+             : INKLING_ERR_CUDA;
+}
+
 int inkling_rel_attn_prefill(const void* q, const void* k_cache, const void* v_cache,
                              const int32_t* block_table, int32_t max_blocks,
                              const int32_t* cu_q_lens, const int32_t* seq_lens,

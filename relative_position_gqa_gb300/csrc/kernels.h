@@ -25,6 +25,27 @@ struct SconvArgs {
   int* dev_status;
 };
 
+struct SconvDenseArgs {
+  const void* x;
+  const float* w;
+  void* state;
+  const int32_t* cu_q_lens;
+  void* y;
+  int B, T, C, max_q_len;
+  int* dev_status;
+};
+
+struct SconvRollbackArgs {
+  const void* state_before;
+  const void* x0;
+  const void* x1;  // nullptr when streams == 1
+  const int32_t* cu_q_lens;
+  const int32_t* accepted;
+  void* state_after;
+  int B, T, C, streams;
+  int* dev_status;
+};
+
 struct AttnArgs {
   const void* q;
   const void* k_cache;
@@ -60,6 +81,8 @@ struct AttnMaps {
 };
 
 cudaError_t launch_sconv_kv(const SconvArgs& a, cudaStream_t stream);
+cudaError_t launch_sconv_dense(const SconvDenseArgs& a, cudaStream_t stream);
+cudaError_t launch_sconv_rollback(const SconvRollbackArgs& a, cudaStream_t stream);
 cudaError_t launch_prefill(const AttnArgs& a, const AttnMaps& maps, cudaStream_t stream);
 cudaError_t launch_decode(const AttnArgs& a, const AttnMaps& maps, cudaStream_t stream);
 

@@ -3,6 +3,12 @@
 // "Model Architecture / Sconv" and "vLLM Integration & Optimization / Managing the
 // sconv cache").
 //
+// The same kernel serves the dense form of the op (one stream, output [T, C] instead of
+// cache pages), used for the conv on the attention output ("Model Architecture / Sconv":
+// the conv also sits after o_proj), and a rollback kernel recomputes the state when a
+// speculative step keeps only a prefix of its tokens ("Model Architecture / MTP",
+// "Re-computing MTP KV cache").
+//
 // One thread owns 8 consecutive channels of K or of V for a run of kChunk consecutive new
 // tokens of one sequence: it keeps the three previous raw rows in registers, so each raw
 // row is read once (plus a 3-row halo per run) and each conv output is written once,
@@ -36,34 +42,46 @@ __device__ __forceinline__ F8 unpack8(uint4 u) {
   return f;
 }
 
-__global__ void __launch_bounds__(kSconvThreads)
-sconv_kv_kernel(const uint16_t* __restrict__ k_raw, const uint16_t* __restrict__ v_raw,
-                const float* __restrict__ w_k, const float* __restrict__ w_v,
-                uint16_t* __restrict__ state, const int32_t* __restrict__ cu_q_lens,
-                const int64_t* __restrict__ slot_mapping, uint16_t* __restrict__ k_cache,
-                uint16_t* __restrict__ v_cache, int Hkv, long long num_slots, int max_q_len,
-                int* __restrict__ status) {
-  const int C = Hkv * 128;
-  const int vecs_per_kind = C / kVec;
+// Raw rows come from one or two streams (K and V); the conv output either lands in the
+// paged cache at slot_mapping[t] (head-major pages of 128 slots x 128 channels) or in a
+// dense [T, C] tensor.  The state is [B][streams][3][C], oldest row first.
+struct SconvDev {
+  const uint16_t* x[2];
+  const float* w[2];
+  uint16_t* out[2];  // paged caches, or the dense output (streams == 1)
+  uint16_t* state;
+  const int32_t* cu_q_lens;
+  const int64_t* slot_mapping;
+  int T, C, streams, Hkv, max_q_len;
+  long long num_slots;
+  int* status;
+};
+
+template <bool kPaged>
+__global__ void __launch_bounds__(kSconvThreads) sconv_kernel(const SconvDev p) {
+  const int C = p.C;
+  const int vecs_per_stream = C / kVec;
   const int vec = blockIdx.x * kSconvThreads + threadIdx.x;
-  if (vec >= 2 * vecs_per_kind) return;
-  const int which = vec / vecs_per_kind;  // 0 = K, 1 = V
-  const int c0 = (vec % vecs_per_kind) * kVec;
+  if (vec >= p.streams * vecs_per_stream) return;
+  const int which = vec / vecs_per_stream;
+  const int c0 = (vec % vecs_per_stream) * kVec;
   const int b = blockIdx.z;
-  const int t_begin = cu_q_lens[b];
-  const int n = cu_q_lens[b + 1] - t_begin;
-  if (n < 0 || n > max_q_len) {
-    if (blockIdx.y == 0 && threadIdx.x == 0) report(status, kErrBadInput);
+  const int t_begin = p.cu_q_lens[b];
+  const int n = p.cu_q_lens[b + 1] - t_begin;
+  if (t_begin < 0 || n < 0 || n > p.max_q_len || t_begin + n > p.T) {
+    if (blockIdx.y == 0 && threadIdx.x == 0) report(p.status, kErrBadInput);
     return;
   }
   const int ts = blockIdx.y * kChunk;
   if (ts >= n) return;
   const int te = min(ts + kChunk, n);
 
-  const uint16_t* x = which == 0 ? k_raw : v_raw;
-  const float* w = which == 0 ? w_k : w_v;
-  uint16_t* cache = which == 0 ? k_cache : v_cache;
-  uint16_t* st = state + ((size_t)b * 2 + which) * 3 * C + c0;
+  // selects, not a dynamic index into the parameter arrays (which would copy them to
+  // local memory)
+  const uint16_t* x = which == 0 ? p.x[0] : p.x[1];
+  const float* w = which == 0 ? p.w[0] : p.w[1];
+  uint16_t* out = which == 0 ? p.out[0] : p.out[1];
+  uint16_t* st = p.state + ((size_t)b * p.streams + which) * 3 * C + c0;
 
   float tap[kVec][4];
 #pragma unroll
@@ -99,17 +117,21 @@ sconv_kv_kernel(const uint16_t* __restrict__ k_raw, const uint16_t* __restrict__
       a = fmaf(tap[i][3], cur.v[i], a);
       y[i] = a;
     }
-    const long long slot = slot_mapping[tg];
-    if (slot >= num_slots) {
-      report(status, kErrBadBlock);
-    } else if (slot >= 0) {
-      const long long blk = slot >> 7, off = slot & 127;
-      uint4 o;
-      o.x = pack_bf16(y[0], y[1]);
-      o.y = pack_bf16(y[2], y[3]);
-      o.z = pack_bf16(y[4], y[5]);
-      o.w = pack_bf16(y[6], y[7]);
-      *reinterpret_cast<uint4*>(cache + (((size_t)blk * Hkv + head) * 128 + off) * 128 + d0) = o;
+    uint4 o;
+    o.x = pack_bf16(y[0], y[1]);
+    o.y = pack_bf16(y[2], y[3]);
+    o.z = pack_bf16(y[4], y[5]);
+    o.w = pack_bf16(y[6], y[7]);
+    if (kPaged) {
+      const long long slot = p.slot_mapping[tg];
+      if (slot >= p.num_slots) {
+        report(p.status, kErrBadBlock);
+      } else if (slot >= 0) {
+        const long long blk = slot >> 7, off = slot & 127;
+        *reinterpret_cast<uint4*>(out + (((size_t)blk * p.Hkv + head) * 128 + off) * 128 + d0) = o;
+      }
+    } else {
+      *reinterpret_cast<uint4*>(out + (size_t)tg * C + c0) = o;
     }
     h0 = h1; h1 = h2; h2 = cur;
   }
@@ -123,24 +145,103 @@ sconv_kv_kernel(const uint16_t* __restrict__ k_raw, const uint16_t* __restrict__
       if (idx >= 0) {
         v = __ldg(reinterpret_cast<const uint4*>(x + (size_t)(t_begin + idx) * C + c0));
       } else {
-        v = old_state[3 + idx];
+        v = idx == -1 ? old_state[2] : (idx == -2 ? old_state[1] : old_state[0]);
       }
       *reinterpret_cast<uint4*>(st + (size_t)r * C) = v;
     }
   }
 }
 
+// State after a speculative step of which only the first accepted[b] new tokens stay:
+// the last three rows of [state_before ; first accepted[b] raw rows].  One thread per
+// (sequence, stream, 8 channels); it reads all three of its rows before writing any, so
+// state_after may be state_before itself.
+__global__ void __launch_bounds__(kSconvThreads)
+sconv_rollback_kernel(const uint16_t* state_before, const uint16_t* __restrict__ x0,
+                      const uint16_t* __restrict__ x1, const int32_t* __restrict__ cu_q_lens,
+                      const int32_t* __restrict__ accepted, uint16_t* state_after, int T,
+                      int C, int streams, int* __restrict__ status) {
+  const int vecs_per_stream = C / kVec;
+  const int vec = blockIdx.x * kSconvThreads + threadIdx.x;
+  if (vec >= streams * vecs_per_stream) return;
+  const int which = vec / vecs_per_stream;
+  const int c0 = (vec % vecs_per_stream) * kVec;
+  const int b = blockIdx.y;
+  const int t_begin = cu_q_lens[b];
+  const int n = cu_q_lens[b + 1] - t_begin;
+  const int a = accepted[b];
+  if (t_begin < 0 || n < 0 || t_begin + n > T || a < 0 || a > n) {
+    if (vec == 0) report(status, kErrBadInput);
+    return;
+  }
+  const uint16_t* x = which == 0 ? x0 : x1;
+  const size_t so = ((size_t)b * streams + which) * 3 * C + c0;
+  uint4 rows[3];
+#pragma unroll
+  for (int r = 0; r < 3; ++r) {
+    const int idx = a - 3 + r;  // index among the new rows
+    rows[r] = idx >= 0 ? __ldg(reinterpret_cast<const uint4*>(x + (size_t)(t_begin + idx) * C + c0))
+                       : *reinterpret_cast<const uint4*>(state_before + so + (size_t)(3 + idx) * C);
+  }
+#pragma unroll
+  for (int r = 0; r < 3; ++r) *reinterpret_cast<uint4*>(state_after + so + (size_t)r * C) = rows[r];
+}
+
+static dim3 sconv_grid(int streams, int C, int max_q_len, int B) {
+  const int total_vecs = streams * C / kVec;
+  return dim3((total_vecs + kSconvThreads - 1) / kSconvThreads, (max_q_len + kChunk - 1) / kChunk, B);
+}
+
 cudaError_t launch_sconv_kv(const SconvArgs& a, cudaStream_t stream) {
-  const int C = a.Hkv * 128;
-  const int total_vecs = 2 * C / kVec;
-  dim3 grid((total_vecs + kSconvThreads - 1) / kSconvThreads,
-            (a.max_q_len + kChunk - 1) / kChunk, a.B);
+  SconvDev p{};
+  p.x[0] = static_cast<const uint16_t*>(a.k_raw);
+  p.x[1] = static_cast<const uint16_t*>(a.v_raw);
+  p.w[0] = a.w_k;
+  p.w[1] = a.w_v;
+  p.out[0] = static_cast<uint16_t*>(a.k_cache);
+  p.out[1] = static_cast<uint16_t*>(a.v_cache);
+  p.state = static_cast<uint16_t*>(a.state);
+  p.cu_q_lens = a.cu_q_lens;
+  p.slot_mapping = a.slot_mapping;
+  p.T = a.T;
+  p.C = a.Hkv * 128;
+  p.streams = 2;
+  p.Hkv = a.Hkv;
+  p.max_q_len = a.max_q_len;
+  p.num_slots = (long long)a.num_blocks * 128;
+  p.status = a.dev_status;
+  const dim3 grid = sconv_grid(2, p.C, a.max_q_len, a.B);
   if (grid.y == 0 || grid.z == 0) return cudaSuccess;
-  sconv_kv_kernel<<<grid, kSconvThreads, 0, stream>>>(
-      static_cast<const uint16_t*>(a.k_raw), static_cast<const uint16_t*>(a.v_raw), a.w_k, a.w_v,
-      static_cast<uint16_t*>(a.state), a.cu_q_lens, a.slot_mapping,
-      static_cast<uint16_t*>(a.k_cache), static_cast<uint16_t*>(a.v_cache), a.Hkv,
-      (long long)a.num_blocks * 128, a.max_q_len, a.dev_status);
+  sconv_kernel<true><<<grid, kSconvThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_sconv_dense(const SconvDenseArgs& a, cudaStream_t stream) {
+  SconvDev p{};
+  p.x[0] = p.x[1] = static_cast<const uint16_t*>(a.x);
+  p.w[0] = p.w[1] = a.w;
+  p.out[0] = p.out[1] = static_cast<uint16_t*>(a.y);
+  p.state = static_cast<uint16_t*>(a.state);
+  p.cu_q_lens = a.cu_q_lens;
+  p.T = a.T;
+  p.C = a.C;
+  p.streams = 1;
+  p.max_q_len = a.max_q_len;
+  p.status = a.dev_status;
+  const dim3 grid = sconv_grid(1, a.C, a.max_q_len, a.B);
+  if (grid.y == 0 || grid.z == 0) return cudaSuccess;
+  sconv_kernel<false><<<grid, kSconvThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_sconv_rollback(const SconvRollbackArgs& a, cudaStream_t stream) {
+  const int total_vecs = a.streams * a.C / kVec;
+  const dim3 grid((total_vecs + kSconvThreads - 1) / kSconvThreads, a.B);
+  if (grid.y == 0) return cudaSuccess;
+  sconv_rollback_kernel<<<grid, kSconvThreads, 0, stream>>>(
+      static_cast<const uint16_t*>(a.state_before), static_cast<const uint16_t*>(a.x0),
+      static_cast<const uint16_t*>(a.x1 ? a.x1 : a.x0), a.cu_q_lens, a.accepted,
+      static_cast<uint16_t*>(a.state_after), a.T, a.C, a.streams, a.dev_status);
   return cudaGetLastError();
 }
 

@@ -91,3 +91,36 @@ def test_workspace_size_rule(lib):
     two = ws(1, 8, 1, 9, 100000, 0, 2)
     assert two >= 2 * 72 * 130 * 4
     assert ws(1, 8, 1, 9, 100000, 0, 8) > two
+
+
+def test_dense_sconv_host_checks(lib):
+    f = lib.inkling_sconv
+    ok = dict(x=FAKE, w=FAKE, st=FAKE, cu=FAKE, y=FAKE + 4096, B=1, T=4, C=64, mq=4, ds=None, s=None)
+
+    def call(**over):
+        a = dict(ok)
+        a.update(over)
+        return f(*a.values())
+    assert call(C=12) == 1            # not a multiple of 8 channels
+    assert call(C=0) == 1
+    assert call(y=FAKE) == 1          # output aliases the input
+    assert call(x=FAKE + 8) == 1      # misaligned
+    assert call(w=None) == 1
+    assert call(B=0, T=0, x=None, w=None, st=None, cu=None, y=None) == 0
+
+
+def test_rollback_host_checks(lib):
+    f = lib.inkling_sconv_state_rollback
+    ok = dict(sb=FAKE, x0=FAKE, x1=FAKE, cu=FAKE, acc=FAKE, sa=FAKE, B=2, T=18, C=256, streams=2,
+              ds=None, s=None)
+
+    def call(**over):
+        a = dict(ok)
+        a.update(over)
+        return f(*a.values())
+    assert call(streams=3) == 1
+    assert call(streams=2, x1=None) == 1  # the K/V pair needs both raw streams
+    assert call(acc=None) == 1
+    assert call(sa=FAKE + 2) == 1
+    assert call(C=4) == 1
+    assert call(B=0) == 0

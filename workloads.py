@@ -221,3 +221,32 @@ def small(name="small", *, B=2, q_lens=(150, 37), seq_lens=None, hq=4, hkv=2, r=
                 history_random=has_prefix if history_random is None else history_random,
                 state_random=has_prefix if state_random is None else state_random,
                 spare_blocks=spare_blocks)
+
+
+@dataclasses.dataclass
+class DenseCase:
+    """One dense stream for the conv on a [T, C] activation (e.g. the attention output)."""
+    x: torch.Tensor            # [T, C] bf16 raw rows
+    w: torch.Tensor            # [C, 4] fp32 taps
+    state: torch.Tensor        # [B, 3, C] bf16, oldest row first
+    cu_q_lens: torch.Tensor    # [B+1] int32
+
+    @property
+    def max_q_len(self) -> int:
+        cu = self.cu_q_lens.tolist()
+        return max([b - a for a, b in zip(cu[:-1], cu[1:])] + [0])
+
+
+def make_dense(q_lens, C: int, seed: int, device="cpu", w_std: float = 0.5,
+               state_random: bool = True) -> DenseCase:
+    """Seeded dense-stream inputs: x ~ N(0,1) bf16, taps ~ N(0, w_std) fp32, state ~ N(0,1)
+    bf16 (zeros when state_random is False)."""
+    g = torch.Generator().manual_seed(seed)
+    T = int(sum(q_lens))
+    x = torch.randn(T, C, generator=g).to(torch.bfloat16)
+    w = torch.randn(C, 4, generator=g) * w_std
+    st = torch.randn(len(q_lens), 3, C, generator=g) if state_random else torch.zeros(len(q_lens), 3, C)
+    cu = torch.zeros(len(q_lens) + 1, dtype=torch.int32)
+    cu[1:] = torch.cumsum(torch.tensor(list(q_lens), dtype=torch.int64), 0).to(torch.int32)
+    return DenseCase(x.to(device), w.float().contiguous().to(device),
+                     st.to(torch.bfloat16).contiguous().to(device), cu.to(device))
