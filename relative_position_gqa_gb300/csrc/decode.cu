@@ -557,11 +557,33 @@ DecodeSplit decode_split(int B, int Hkv, int max_q_len, int max_seq_len, int win
   if (num_splits_req > 0) {
     ns = num_splits_req;
   } else {
-    // enough CTAs to balance ragged lengths over the SMs, but >= 16 pages per split
-    const long long pairs = (long long)B * Hkv;
-    ns = (8LL * num_sms + pairs - 1) / (pairs > 0 ? pairs : 1);
-    const long long cap = (range_pages + 15) / 16;
-    if (ns > cap) ns = cap;
+    // One CTA holds an SM (its K/V stages fill shared memory), so the grid runs in waves
+    // of num_sms CTAs.
+    const long long pairs = (B > 0 && Hkv > 0) ? (long long)B * Hkv : 1;
+    if (pairs >= num_sms) {
+      // Many sequences: about 8 CTAs per SM balance their ragged lengths, but a split
+      // shorter than 32 pages costs more in pipeline fill and partial traffic than the
+      // balance gains (a 4096-token window is not split at all).
+      ns = (8LL * num_sms + pairs - 1) / pairs;
+      long long cap = range_pages / 32;
+      if (cap < 1) cap = 1;
+      if (ns > cap) ns = cap;
+    } else {
+      // Few sequences (long context): equal splits that fill whole waves, the fewest
+      // waves whose last one is at least 85% full; splits of at least 16 pages.
+      long long cap = range_pages / 16;
+      if (cap < 1) cap = 1;
+      ns = 1;
+      for (long long w = 1; w <= 8; ++w) {
+        long long n_w = w * num_sms / pairs;
+        if (n_w > cap) n_w = cap;
+        if (n_w < 1) continue;
+        ns = n_w;
+        const long long ctas = n_w * pairs;
+        const long long waves = (ctas + num_sms - 1) / num_sms;
+        if (n_w == cap || ctas * 100 >= 85LL * waves * num_sms) break;
+      }
+    }
   }
   if (ns < 1) ns = 1;
   if (ns > range_pages) ns = range_pages;
