@@ -8,6 +8,10 @@ Default workload (one step = the whole hot path over one batch):
 Metric: attention TFLOP/s counting only allowed (query, key) pairs, 4*D flops per pair
 per head (QK^T and PV).  Other workloads (--workload 1..5) print the same line shape;
 the decode ones report KV-read GB/s (algorithmic K/V bytes inside the causal/window range).
+--workload 4 also times the sconv-state rollback after the verify step on its own
+(config.rollback_us, not part of the step).  --workload 6 is the conv on a dense stream
+(inkling_sconv on the sliding-window prefill's attention output, 32768 tokens x 4096
+channels), reported in GB/s of algorithmic bytes (raw rows read + outputs written).
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload 2]
 Under torchrun (N > 1) every rank runs an independent replica (the path has no exchange
@@ -75,6 +79,16 @@ def is_decode(n: int) -> bool:
     return n in (4, 5)
 
 
+DENSE_Q_LENS = (8192,) * 4   # the sliding-window prefill's sequences
+DENSE_C = 32 * 128           # its attention output width (Hq x head dim)
+
+
+def dense_bytes(q_lens, C: int) -> float:
+    """Raw rows read once + conv outputs written once + state rows read and written."""
+    T = sum(q_lens)
+    return float(2 * T * C * 2 + 2 * len(q_lens) * 3 * C * 2)
+
+
 def workload_spec(n: int, variant=None) -> W.Spec:
     return W.config(n, variant=variant)
 
@@ -99,6 +113,7 @@ class ClockSampler:
             pass
         self.proc = None
         self.lines = []
+        self.skip = 0
 
     def __enter__(self):
         try:
@@ -108,6 +123,11 @@ class ClockSampler:
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
+            # nvidia-smi takes a moment to start: begin timing once it is sampling
+            t_end = time.time() + 3.0
+            while not self.lines and time.time() < t_end and self.proc.poll() is None:
+                time.sleep(0.01)
+            self.skip = len(self.lines)
         except (FileNotFoundError, OSError):
             self.proc = None
         return self
@@ -127,7 +147,8 @@ class ClockSampler:
     def summary(self):
         sm, smax, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.lines:
+        # the samples taken while the timed region ran (the last one before it included)
+        for line in self.lines[max(0, self.skip - 1):]:
             parts = [x.strip() for x in line.split(",")]
             if len(parts) < 9:
                 continue
@@ -141,6 +162,31 @@ class ClockSampler:
                     reasons.add(nm)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
                 "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# DRAM bytes (read + write) per launch of the dominant kernel, from one ncu capture of
+# `python bench.py --steps 2 --warmup 3 --no-cpu-baseline` (see profiles/), keyed by the
+# workload and by the SHA-256 of the kernel source it was taken on: when that source has
+# changed since, the figure no longer applies and the line reports null.
+TRAFFIC = {
+    2: ("prefill.cu", "e86268fba922aa6bed3c7649ad11a0296a14ab9b0d1388c8f01604c495a0478a", 616.9e6),
+}
+
+
+def kernel_traffic(workload: int):
+    entry = TRAFFIC.get(workload)
+    if entry is None:
+        return None
+    import hashlib
+    src, sha, nbytes = entry
+    path = os.path.join(ROOT, "relative_position_gqa_gb300", "csrc", src)
+    try:
+        with open(path, "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest() != sha:
+                return None
+    except OSError:
+        return None
+    return nbytes
 
 
 def measured_peaks():
@@ -221,6 +267,26 @@ def run_ours(args, ws, rank, local):
     attn_ms = sum(b.elapsed_time(c) for _, b, c in ev) / args.steps
     sconv_ms = sum(a.elapsed_time(b) for a, b, _ in ev) / args.steps
 
+    rollback_us = None
+    if args.workload == 4:
+        # after a verify step, keep a seeded random prefix of each sequence's 9 tokens
+        gen = torch.Generator().manual_seed(4)
+        accepted = torch.randint(0, 10, (spec.batch,), generator=gen, dtype=torch.int32).to(dev)
+        rb = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+        for i in range(args.warmup + args.steps):
+            reset()
+            if i >= args.warmup:
+                rb[i - args.warmup][0].record(stream)
+            ink.sconv_state_rollback(state0, g.k_raw, g.v_raw, g.cu_q_lens, accepted, g.state,
+                                     dev_status=status)
+            if i >= args.warmup:
+                rb[i - args.warmup][1].record(stream)
+        torch.cuda.synchronize()
+        if int(status.item()) != 0:
+            raise RuntimeError(f"device status {ink.status_string(int(status.item()))}")
+        rollback_us = round(1e3 * sum(a.elapsed_time(b) for a, b in rb) / args.steps, 2)
+
     # ---- end to end through the public API with host buffers
     host_in = [t.cpu().pin_memory() for t in (g.q, g.k_raw, g.v_raw)]
     dev_in = [torch.empty_like(t, device=dev) for t in host_in]
@@ -271,7 +337,7 @@ def run_ours(args, ws, rank, local):
                 "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
                 "peak_source": f"{peak_src} bf16_tflops (burst; kernel timed per launch)",
                 "kernel": "prefill_kernel"}
-    roof["traffic"] = args.traffic
+    roof["traffic"] = args.traffic if args.traffic is not None else kernel_traffic(args.workload)
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": unit, "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 4),
@@ -287,7 +353,102 @@ def run_ours(args, ws, rank, local):
         "roofline": roof,
         "clocks": clocks.summary(),
     }
+    if rollback_us is not None:
+        line["config"]["rollback_us"] = rollback_us
     return line
+
+
+def run_dense(args, ws, rank, local):
+    """--workload 6: inkling_sconv on a dense [T, C] stream with its own state."""
+    import relative_position_gqa_gb300 as ink
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    ink._lib.load()
+    c = W.make_dense(DENSE_Q_LENS, DENSE_C, seed=6 + 1000 * rank, device=dev)
+    T = sum(DENSE_Q_LENS)
+    y = torch.empty_like(c.x)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    state0 = c.state.clone()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(x):
+        ink.sconv(x, c.w, c.state, c.cu_q_lens, max_q_len=max(DENSE_Q_LENS), y=y,
+                  dev_status=status)
+
+    def reset():
+        c.state.copy_(state0)
+        flush.fill_(1.0)
+
+    for _ in range(args.warmup):
+        reset()
+        step(c.x)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        for i in range(args.steps):
+            reset()
+            ev[i][0].record(stream)
+            step(c.x)
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {ink.status_string(int(status.item()))}")
+    step_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+    host_in = c.x.cpu().pin_memory()
+    dev_in = torch.empty_like(host_in, device=dev)
+    host_out = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+    e2e_ev = []
+    for i in range(args.warmup + args.steps):
+        reset()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        dev_in.copy_(host_in, non_blocking=True)
+        step(dev_in)
+        host_out.copy_(y, non_blocking=True)
+        b.record(stream)
+        if i >= args.warmup:
+            e2e_ev.append((a, b))
+    torch.cuda.synchronize()
+    e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_ev) / len(e2e_ev)
+    t = torch.tensor([step_ms, e2e_ms], dtype=torch.float64, device=dev)
+    if ws > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    step_ms, e2e_ms = t.tolist()
+    peaks, peak_src = measured_peaks()
+    work = dense_bytes(DENSE_Q_LENS, DENSE_C)
+    achieved = work / (step_ms * 1e-3) / 1e9
+    peak = float(peaks["hbm_gbs"])
+    return {
+        "metric": METRIC, "value": round(ws * achieved, 1), "unit": "GB/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) rows and state, N(0,0.5) taps)",
+        "config": {"workload": f"attn_out_sconv: B=4 x 8192 tokens, C={DENSE_C}, window 4",
+                   "global_batch": 4 * ws, "seq_len": 8192, "parallelism": f"replicas x{ws}",
+                   "l2": "flushed (512 MB write) between timed steps"},
+        "e2e": {"value": round(ws * work / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                "h2d_bytes_per_step": host_in.numel() * 2, "d2h_bytes_per_step": host_out.numel() * 2},
+        "gpu_launches": args.steps,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": args.traffic,
+                     "peak_source": f"{peak_src} hbm_gbs", "kernel": "sconv_kernel<false>"},
+        "clocks": clocks.summary(),
+    }
+
+
+def dense_oracle_sample(seed: int):
+    """The oracle's dense conv on one 8192-token sequence of the same width."""
+    import oracle
+    c = W.make_dense(DENSE_Q_LENS[:1], DENSE_C, seed=seed)
+    t0 = time.perf_counter()
+    oracle.sconv_dense(c.x, c.w, c.state.clone(), c.cu_q_lens)
+    secs = time.perf_counter() - t0
+    return dense_bytes(DENSE_Q_LENS[:1], DENSE_C), secs
 
 
 # ------------------------------------------------------------- oracle (CPU) arm -----
@@ -335,7 +496,27 @@ def oracle_sample(spec: W.Spec, case, budget_s: float, seed: int):
     return (done_pairs, t_attn, t_sconv, len(rows), cores, spec)
 
 
+def run_reference_dense(args, ws):
+    per = [dense_oracle_sample(seed=6 + i) for i in range(args.warmup + args.steps)][args.warmup:]
+    work = sum(b for b, _ in per)
+    secs = sum(t for _, t in per)
+    value = work / secs / 1e9
+    cores = 1  # the dense conv oracle is single-threaded
+    desc = f"fp64 C oracle, one thread: one 8192-token sequence x {DENSE_C} channels per step"
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(secs / len(per) * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": f"attn_out_sconv: B=4 x 8192 tokens, C={DENSE_C}"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
 def run_reference(args, ws, rank):
+    if args.workload == 6:
+        return run_reference_dense(args, ws)
     spec = workload_spec(args.workload, args.variant)
     decode = is_decode(args.workload)
     per_step = []
@@ -375,10 +556,10 @@ def run_reference(args, ws, rank):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5, 6])
     ap.add_argument("--variant", default=None, help="mtp_decode: swa|full; decode_1m: n1|n9")
     ap.add_argument("--ref-seconds", type=float, default=6.0,
                     help="oracle seconds per reference step / for the cpu_baseline sample")
@@ -398,6 +579,20 @@ def main():
     if args.impl == "reference":
         if rank == 0:
             print(json.dumps(run_reference(args, ws, rank)), flush=True)
+        if ws > 1:
+            torch.distributed.destroy_process_group()
+        return
+
+    if args.workload == 6:
+        line = run_dense(args, ws, rank, local)
+        if rank == 0 and not args.no_cpu_baseline:
+            b, t = dense_oracle_sample(seed=99)
+            line["cpu_baseline"] = {"value": b / t / 1e9, "unit": "GB/s", "cores": 1,
+                                    "kind": "oracle",
+                                    "sample": f"one 8192-token sequence x {DENSE_C} channels, "
+                                              f"fp64 C oracle, one thread, {t:.2f} s"}
+        if rank == 0:
+            print(json.dumps(line), flush=True)
         if ws > 1:
             torch.distributed.destroy_process_group()
         return

@@ -24,9 +24,11 @@
 //
 // The relative bias ("sheared" along the tile diagonals): within a 128x128 tile the
 // distance is delta + r - c with delta = p0 - k0, so row r needs a contiguous run of the
-// table, reversed.  The stager warp puts the 255 values a tile needs in shared memory once,
-// in reversed order, so that at each column the 32 lanes of a warp read 32 consecutive
-// words (conflict-free 4-byte loads).  Tiles whose smallest distance is already past R-1 use the single
+// table, reversed.  The stager warp puts the 255 values a tile needs in shared memory in
+// reversed order, four times: copy j shifted by j words, the copies 264 words apart.  Row
+// r then reads its run as 16-byte loads from copy (127 - r) mod 4, and the eight loads of
+// each quarter-warp land in distinct banks (a quarter of the load instructions of 4-byte
+// reads, with no bank conflicts).  Tiles whose smallest distance is already past R-1 use the single
 // clamped value instead (no copies, no loads).  Logits are kept in natural units
 // (x = scale * q.k + b) and log2 e is folded into the exponent's FMA.  Key tiles are
 // visited from the diagonal backwards; only tiles that overlap the causal diagonal, the
@@ -61,12 +63,18 @@ constexpr uint32_t kIdescPV = idesc_bf16(128, 128, false, true);
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 5.545177444479562f;  // 8 ln 2: rescale O past 256x growth
+// Bias slice layout: copy j (j = 0..3) holds rev[i + j] at word j * kBiasCopyStride + i.
+// 264 = 256 + 8 words puts the copies' 16-byte chunks in different bank groups for the
+// eight consecutive rows of a quarter-warp, whatever the row offset.
+constexpr int kBiasCopyStride = 264;
+constexpr int kBiasWords = 3 * kBiasCopyStride + 256;
 
 struct __align__(1024) Smem {
   uint8_t q[2][2][16384];        // [head slot][d half][128 rows x 128 B], swizzled
   uint8_t k[kStages][2][16384];  // [stage][d half][128 keys x 128 B]
   uint8_t v[kStages][2][16384];
-  float bias[kStages][2][256];  // [stage][head slot][j]: rev[j] = b[h][clamp(delta + 127 - j)]
+  // [stage][head slot][copy layout]: rev[j] = b[h][clamp(delta + 127 - j)], four shifted copies
+  float bias[kStages][2][kBiasWords];
   uint64_t q_full;
   // a K stage is free once the tile's last QK^T is done, a V stage once its last PV is
   // done: K for the next tile is fetched while the current tile's softmax and PV run
@@ -232,9 +240,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_q,
    } else if (warp >= 10) {
     // ---------------------------------------------------------- bias stagers ---
     // warp 10 stages head A's slice, warp 11 head B's, with 4-byte cp.async copies:
-    // rev[j] = b[h][clamp(delta + 127 - j, 0, R-1)], j < 256, so softmax thread r reads its
-    // run rev[127 - r + c], c = 0..127, and a warp's 32 lanes read 32 consecutive words
-    // (no bank conflicts).  Both warps arrive on b_full[stage] for every tile (count 64).
+    // rev[j] = b[h][clamp(delta + 127 - j, 0, R-1)], j < 256, written to the four shifted
+    // copies, so softmax thread r reads its run rev[127 - r + c], c = 0..127, four values
+    // at a time.  Both warps arrive on b_full[stage] for every tile (count 64).
     const int slot = warp - 10;
     const bool mine = slot == 0 || has_b;
     const float* brow = p.bias + (size_t)(h0 + slot) * p.R;
@@ -253,7 +261,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_q,
         for (int j = lane; j < 256; j += 32) {
           int d = delta + 127 - j;
           d = d < 0 ? 0 : (d > R - 1 ? R - 1 : d);
-          cp_async_4(dst + j, brow + d);
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            if (j >= c) cp_async_4(dst + c * kBiasCopyStride + j - c, brow + d);
         }
       }
       cp_async_mbar_arrive(&s.b_full[st]);
@@ -400,26 +410,37 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_q,
         tmem_ld32(tS + 64, sr + 64);
         tmem_ld32(tS + 96, sr + 96);
         float2 x[64];  // logit * log2 e, pairs of columns
-        const float* rb = bias_buf + (127 - r);  // rb[c] = bias at distance delta + r - c
+        // rb4[k] = bias at distance delta + r - c for columns c = 4k .. 4k+3 (16-byte aligned)
+        const int bsh = (127 - r) & 3;
+        const float4* rb4 =
+            reinterpret_cast<const float4*>(bias_buf + bsh * kBiasCopyStride + (127 - r - bsh));
         const float2 bc2 = make_float2(bconst, bconst);
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          const float2 sv = make_float2(__uint_as_float(sr[2 * k]), __uint_as_float(sr[2 * k + 1]));
+        for (int k = 0; k < 32; k += 2) {
+          const float2 sv0 = make_float2(__uint_as_float(sr[2 * k]), __uint_as_float(sr[2 * k + 1]));
+          const float2 sv1 = make_float2(__uint_as_float(sr[2 * k + 2]), __uint_as_float(sr[2 * k + 3]));
           if (clamped) {
-            x[k] = __ffma2_rn(sv, sc2, bc2);
+            x[k] = __ffma2_rn(sv0, sc2, bc2);
+            x[k + 1] = __ffma2_rn(sv1, sc2, bc2);
           } else {
-            x[k] = __ffma2_rn(sv, sc2, make_float2(rb[2 * k], rb[2 * k + 1]));
+            const float4 b4 = rb4[k >> 1];
+            x[k] = __ffma2_rn(sv0, sc2, make_float2(b4.x, b4.y));
+            x[k + 1] = __ffma2_rn(sv1, sc2, make_float2(b4.z, b4.w));
           }
         }
         tmem_wait_ld();
         reg_fence<64>(sr + 64);
 #pragma unroll
-        for (int k = 32; k < 64; ++k) {
-          const float2 sv = make_float2(__uint_as_float(sr[2 * k]), __uint_as_float(sr[2 * k + 1]));
+        for (int k = 32; k < 64; k += 2) {
+          const float2 sv0 = make_float2(__uint_as_float(sr[2 * k]), __uint_as_float(sr[2 * k + 1]));
+          const float2 sv1 = make_float2(__uint_as_float(sr[2 * k + 2]), __uint_as_float(sr[2 * k + 3]));
           if (clamped) {
-            x[k] = __ffma2_rn(sv, sc2, bc2);
+            x[k] = __ffma2_rn(sv0, sc2, bc2);
+            x[k + 1] = __ffma2_rn(sv1, sc2, bc2);
           } else {
-            x[k] = __ffma2_rn(sv, sc2, make_float2(rb[2 * k], rb[2 * k + 1]));
+            const float4 b4 = rb4[k >> 1];
+            x[k] = __ffma2_rn(sv0, sc2, make_float2(b4.x, b4.y));
+            x[k + 1] = __ffma2_rn(sv1, sc2, make_float2(b4.z, b4.w));
           }
         }
         if (masked) {
