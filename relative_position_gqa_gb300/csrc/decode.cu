@@ -7,8 +7,10 @@
 // and G = 8), so each K/V page is read from HBM once per KV head.  The packed Q lives in
 // tensor memory (64 columns of bf16 pairs) and both contractions run on the tensor core:
 // S = Q K^T with Q from TMEM (TS form), O += P V with P from TMEM.
-//   warp 4      TMA producer: K/V pages of the split (three-stage ring of 64 KB); its
-//               lanes also cp.async each page's bias slices (G heads) into the ring.
+//   warp 4      TMA producer: K/V pages of the split (three-stage ring of 64 KB).
+//   warp 6      bias stager: cp.async each page's bias slices (G heads) into a ring of
+//               its own, whose slots the softmax frees as soon as it has added the bias,
+//               so the slices of later pages load while the current one is processed.
 //   warp 5      MMA issuer; S is double-buffered so S(i+1) overlaps softmax(i).  Page i's
 //               "P ready" barrier is p_full[i & 1]: S(i+1) is issued before P(i) is
 //               consumed, so a fast warp may finish page i+1 while a slow one is still on
@@ -30,7 +32,7 @@ namespace ink {
 namespace decode {
 
 constexpr int kStages = 3;
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;
 constexpr int kMaxG = 16;
 // floats per staged head (>= 127 + 9); 164 = 4 (mod 32), so the G heads x 4 tokens of a
 // warp (lane = t*G + g) hit distinct banks when they read column c
@@ -46,7 +48,7 @@ struct __align__(1024) Smem {
   uint8_t k[kStages][2][16384];
   uint8_t v[kStages][2][16384];
   float bias[kStages][kMaxG * kBiasStride];  // raw table values, staged per page by the TMA warp
-  uint64_t k_full[kStages], v_full[kStages], kv_empty[kStages], b_full[kStages];
+  uint64_t k_full[kStages], v_full[kStages], kv_empty[kStages], b_full[kStages], b_empty[kStages];
   uint64_t q_ready, s_full[2], p_full[2], pv_done, o_full, drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -137,6 +139,7 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
       mbar_init(&s.v_full[i], 1);
       mbar_init(&s.kv_empty[i], 1);
       mbar_init(&s.b_full[i], 32);
+      mbar_init(&s.b_empty[i], nact);
     }
     mbar_init(&s.q_ready, nact);
     mbar_init(&s.s_full[0], 1);
@@ -160,30 +163,20 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
 
   if (warp == 4) {
     // ------------------------------------------------------------ TMA producer ---
-    // Lane 0 issues the K/V page loads; all 32 lanes stage the page's bias slice with
-    // 4-byte cp.async copies (no register round trip) and arrive on b_full[stage] when
-    // their copies land.  The warp runs up to kStages pages ahead of the softmax.
+    // Lane 0 issues the K/V page loads, up to kStages pages ahead of the softmax.
     const uint64_t pol = l2_policy_evict_first();
     if (lane == 0) {
       tma_prefetch_desc(&map_k);
       tma_prefetch_desc(&map_v);
-    }
-    const int R = p.R, span = 127 + n;
-    int issued = 0;
-    for (int i = 0; i < np; ++i) {
-      const int st = i % kStages;
-      int ok = 1;
-      if (lane == 0 && i >= kStages)
-        ok = mbar_wait(&s.kv_empty[st], ((i / kStages) - 1) & 1, abort_flag, p.status);
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) {
-        if (lane == 0) {
+      int issued = 0;
+      for (int i = 0; i < np; ++i) {
+        const int st = i % kStages;
+        if (i >= kStages &&
+            !mbar_wait(&s.kv_empty[st], ((i / kStages) - 1) & 1, abort_flag, p.status)) {
           report(p.status, kErrTimeout);
           s.abort_flag = 1;
+          break;
         }
-        break;
-      }
-      if (lane == 0) {
         const int page = table[pg0 + i] * p.Hkv + kvh;
         mbar_arrive_expect_tx(&s.k_full[st], 32768u);
         tma_load_3d_hint(s.k[st][0], &map_k, &s.k_full[st], 0, 0, page, pol);
@@ -191,6 +184,37 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
         mbar_arrive_expect_tx(&s.v_full[st], 32768u);
         tma_load_3d_hint(s.v[st][0], &map_v, &s.v_full[st], 0, 0, page, pol);
         tma_load_3d_hint(s.v[st][1], &map_v, &s.v_full[st], 64, 0, page, pol);
+        issued = i + 1;
+      }
+      if (*abort_flag) {
+        // let the copies already in flight land before the CTA goes away
+        for (int i = max(0, issued - kStages); i < issued; ++i) {
+          const int st = i % kStages;
+          const uint32_t ph = (i / kStages) & 1;
+          volatile int never = 0;
+          mbar_wait(&s.k_full[st], ph, &never);
+          mbar_wait(&s.v_full[st], ph, &never);
+        }
+      }
+    }
+  } else if (warp == 6) {
+    // ------------------------------------------------------------ bias stager ---
+    // All 32 lanes stage the page's bias slices with 4-byte cp.async copies (no register
+    // round trip) and arrive on b_full[slot] when their copies land.  A slot is reused
+    // once every softmax thread has added the slice it held (b_empty).
+    const int R = p.R, span = 127 + n;
+    for (int i = 0; i < np; ++i) {
+      const int st = i % kStages;
+      int ok = 1;
+      if (lane == 0 && i >= kStages)
+        ok = mbar_wait(&s.b_empty[st], ((i / kStages) - 1) & 1, abort_flag, p.status);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) {
+        if (lane == 0) {
+          report(p.status, kErrTimeout);
+          s.abort_flag = 1;
+        }
+        break;
       }
       const int k0 = (pg0 + i) * 128;
       const int dmax = (L - 1) - k0;                 // largest distance in the page
@@ -207,18 +231,9 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
         }
       }
       cp_async_mbar_arrive(&s.b_full[st]);
-      issued = i + 1;
     }
-    if (lane == 0 && *abort_flag) {
-      for (int i = max(0, issued - kStages); i < issued; ++i) {
-        const int st = i % kStages;
-        const uint32_t ph = (i / kStages) & 1;
-        volatile int never = 0;
-        mbar_wait(&s.k_full[st], ph, &never);
-        mbar_wait(&s.v_full[st], ph, &never);
-        mbar_wait(&s.b_full[st], ph, &never);
-      }
-    }
+    // let outstanding copies land before the CTA can exit
+    asm volatile("cp.async.wait_all;" ::: "memory");
   } else if (warp == 5) {
     // ------------------------------------------------------------- MMA issuer ---
     bool ok = mbar_wait(&s.q_ready, 0, abort_flag, p.status) && mbar_wait(&s.k_full[0], 0, abort_flag, p.status);
@@ -324,7 +339,11 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
     const int R = p.R, W = p.window;
     const float bconst = __ldg(brow + R - 1);
     const int pq = L - n + t;  // position of this row's token
-    float m = -INFINITY, l = 0.f;
+    float m = -INFINITY;
+    float2 l2 = make_float2(0.f, 0.f);
+    const float2 sc2 = make_float2(p.scale, p.scale);
+    const float2 bc2 = make_float2(bconst, bconst);
+    const float2 lg2 = make_float2(kLog2e, kLog2e);
     bool ok = true;
     for (int i = 0; i < np; ++i) {
       const int k0 = (pg0 + i) * 128;
@@ -340,65 +359,72 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
       if (!mbar_wait(&s.s_full[i & 1], (i >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
       tc_fence_after();
       const uint32_t tS = tmem + lane_base + kColS0 + (i & 1) * 128;
-      uint32_t sr[128];  // S row, then x = logit * log2 e, then packed bf16 P pairs
+      uint32_t sr[128];  // S row, then packed bf16 P pairs
       tmem_ld32(tS + 0, sr);
       tmem_ld32(tS + 32, sr + 32);
       tmem_ld32(tS + 64, sr + 64);
       tmem_ld32(tS + 96, sr + 96);
       tmem_wait_ld();
       reg_fence<128>(sr);
+      float2 x[64];  // logits in natural units, pairs of columns
       if (clamped) {
 #pragma unroll
-        for (int c = 0; c < 128; ++c)
-          sr[c] = __float_as_uint(fmaf(__uint_as_float(sr[c]), p.scale, bconst));
+        for (int k = 0; k < 64; ++k)
+          x[k] = __ffma2_rn(make_float2(__uint_as_float(sr[2 * k]), __uint_as_float(sr[2 * k + 1])),
+                            sc2, bc2);
       } else {
         const float* bp = bias_buf + g * kBiasStride + (n - 1 - t);
         // 32 columns at a time: keeps the compiler from hoisting all 128 bias loads
 #pragma unroll
-        for (int cb = 0; cb < 128; cb += 32) {
+        for (int kb = 0; kb < 64; kb += 16) {
 #pragma unroll
-          for (int c = cb; c < cb + 32; ++c)
-            sr[c] = __float_as_uint(fmaf(__uint_as_float(sr[c]), p.scale, bp[c]));
+          for (int k = kb; k < kb + 16; ++k)
+            x[k] = __ffma2_rn(make_float2(__uint_as_float(sr[2 * k]), __uint_as_float(sr[2 * k + 1])),
+                              sc2, make_float2(bp[2 * k], bp[2 * k + 1]));
           asm volatile("" ::: "memory");
         }
       }
+      // this page's bias slot may be refilled (the loads above are ordered before it)
+      mbar_arrive(&s.b_empty[i % kStages]);
       if (masked) {
         const int d0 = pq - k0;
 #pragma unroll
-        for (int c = 0; c < 128; ++c) {
-          const int d = d0 - c;
-          const bool allowed = d >= 0 && (W == 0 || d <= W - 1);
-          sr[c] = allowed ? sr[c] : __float_as_uint(-INFINITY);
+        for (int k = 0; k < 64; ++k) {
+          const int d = d0 - 2 * k;
+          const bool a0 = d >= 0 && (W == 0 || d <= W - 1);
+          const bool a1 = d - 1 >= 0 && (W == 0 || d - 1 <= W - 1);
+          x[k].x = a0 ? x[k].x : -INFINITY;
+          x[k].y = a1 ? x[k].y : -INFINITY;
         }
       }
-      float mx0 = __uint_as_float(sr[0]), mx1 = __uint_as_float(sr[1]);
-      float mx2 = __uint_as_float(sr[2]), mx3 = __uint_as_float(sr[3]);
+      float mx0 = fmax3(x[0].x, x[0].y, x[1].x), mx1 = fmax3(x[1].y, x[2].x, x[2].y);
+      float mx2 = fmax3(x[3].x, x[3].y, x[4].x), mx3 = fmax3(x[4].y, x[5].x, x[5].y);
 #pragma unroll
-      for (int c = 4; c < 128; c += 4) {
-        mx0 = fmaxf(mx0, __uint_as_float(sr[c]));
-        mx1 = fmaxf(mx1, __uint_as_float(sr[c + 1]));
-        mx2 = fmaxf(mx2, __uint_as_float(sr[c + 2]));
-        mx3 = fmaxf(mx3, __uint_as_float(sr[c + 3]));
+      for (int k = 6; k < 62; k += 4) {
+        mx0 = fmax3(mx0, x[k].x, x[k].y);
+        mx1 = fmax3(mx1, x[k + 1].x, x[k + 1].y);
+        mx2 = fmax3(mx2, x[k + 2].x, x[k + 2].y);
+        mx3 = fmax3(mx3, x[k + 3].x, x[k + 3].y);
       }
-      const float m_new = fmaxf(m, fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)));
+      mx0 = fmax3(mx0, x[62].x, x[62].y);
+      mx1 = fmax3(mx1, x[63].x, x[63].y);
+      const float m_new = fmax3(m, fmaxf(mx0, mx1), fmaxf(mx2, mx3));
       const bool need = m_new > m + kRescaleThreshold || (m == -INFINITY && m_new > -INFINITY);
       const float alpha = need ? ex2((m - m_new) * kLog2e) : 1.f;
       if (need) {
-        l *= alpha;
+        l2.x *= alpha;
+        l2.y *= alpha;
         m = m_new;
       }
       const float nm = m == -INFINITY ? 0.f : -m * kLog2e;  // p = 2^(x log2 e - m log2 e)
-      float l0 = 0.f, l1 = 0.f;
-      // P pairs overwrite the registers they came from (index c/2 <= c)
+      const float2 nm2 = make_float2(nm, nm);
 #pragma unroll
-      for (int c = 0; c < 128; c += 2) {
-        const float e0 = ex2(fmaf(__uint_as_float(sr[c]), kLog2e, nm));
-        const float e1 = ex2(fmaf(__uint_as_float(sr[c + 1]), kLog2e, nm));
-        l0 += e0;
-        l1 += e1;
-        sr[c / 2] = pack_bf16(e0, e1);
+      for (int k = 0; k < 64; ++k) {
+        const float2 d2 = __ffma2_rn(x[k], lg2, nm2);
+        const float2 e2 = make_float2(ex2(d2.x), ex2(d2.y));
+        l2 = __fadd2_rn(l2, e2);
+        sr[k] = pack_bf16(e2.x, e2.y);
       }
-      l += l0 + l1;
       // rescale O (warp-wide, only when some row's max grew past the threshold)
       if (__any_sync(0xffffffffu, need) && i > 0) {
         // O must hold PV(i-1) before it is scaled
@@ -423,6 +449,7 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
       mbar_arrive(&s.p_full[i & 1]);
       if (!ok) break;
     }
+    const float l = l2.x + l2.y;
     if (ok) ok = mbar_wait(&s.o_full, 0, abort_flag, p.status);
     if (!ok) {
       report(p.status, kErrTimeout);

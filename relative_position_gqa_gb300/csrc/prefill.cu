@@ -13,8 +13,8 @@
 //   warps 10-11 bias stagers (one per head): cp.async the tile's slice of the bias table
 //               into shared memory, one stage ahead.
 //   warps 0-3   softmax for head A, warps 4-7 softmax for head B: thread r owns query row
-//               r (= TMEM lane r).  It loads its S row, adds the relative bias, masks,
-//               keeps a running max / sum (rescaling O in TMEM only when the max grew by
+//               r (= TMEM lane r).  It loads its S row, adds the relative bias (which
+//               carries the mask), keeps a running max / sum (rescaling O in TMEM only when the max grew by
 //               more than 2^8), writes P as bf16 over the S columns, and finally
 //               normalises O and stores it.
 // Tensor memory (512 columns): S_A [0,128) S_B [128,256) O_A [256,384) O_B [384,512);
@@ -28,12 +28,15 @@
 // reversed order, four times: copy j shifted by j words, the copies 264 words apart.  Row
 // r then reads its run as 16-byte loads from copy (127 - r) mod 4, and the eight loads of
 // each quarter-warp land in distinct banks (a quarter of the load instructions of 4-byte
-// reads, with no bank conflicts).  Tiles whose smallest distance is already past R-1 use the single
-// clamped value instead (no copies, no loads).  Logits are kept in natural units
-// (x = scale * q.k + b) and log2 e is folded into the exponent's FMA.  Key tiles are
-// visited from the diagonal backwards; only tiles that overlap the causal diagonal, the
-// window edge or the end of the sequence pay for masking; tiles outside the window are
-// never visited.
+// reads, with no bank conflicts).  The mask rides on the slice: a distance that is not
+// attended (negative, or past the window) is staged as -inf, so tiles on the causal
+// diagonal or the window edge run the same code as the others, and the rows of K and V
+// past the end of the sequence are zeroed in shared memory so that stale slots cannot
+// put a NaN into the logits.  Tiles whose smallest distance is already past R-1, and
+// that need no mask, use the single clamped value instead (no copies, no loads).
+// Logits are kept in natural units (x = scale * q.k + b) and log2 e is folded into the
+// exponent's FMA.  Key tiles are visited from the diagonal backwards; tiles outside the
+// window are never visited.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -44,6 +47,9 @@
 
 namespace ink {
 namespace prefill {
+
+// Source of the masked bias slots: the stagers copy it like any other table entry.
+__device__ const float kMaskedBias = -INFINITY;
 
 constexpr int kTile = 128;
 constexpr int kStages = 2;
@@ -82,7 +88,6 @@ struct __align__(1024) Smem {
   uint64_t s_full[2], p_full[2], o_full, drain, b_full[kStages];
   uint32_t tmem_base;
   int abort_flag;
-  int bad_block;
 };
 
 struct Params {
@@ -143,22 +148,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_q,
   const int t_glob0 = t_seq0 + qt * kTile;
   const int32_t* table = p.block_table + (size_t)b * p.max_blocks;
 
+  // Page ids are checked by the producer as it reaches them (a TMA load with an id
+  // outside the cache would only read the fill value, but the call must report it).
   if (threadIdx.x == 0) {
     s.abort_flag = 0;
-    s.bad_block = 0;
-  }
-  __syncthreads();
-  for (int kt = kt_lo + (int)threadIdx.x; kt <= kt_hi; kt += kThreads) {
-    const int32_t blk = table[kt];
-    if (blk < 0 || (long long)blk >= p.num_blocks) s.bad_block = 1;
-  }
-  __syncthreads();
-  if (s.bad_block) {
-    if (threadIdx.x == 0) report(p.status, kErrBadBlock);
-    return;
-  }
-
-  if (threadIdx.x == 0) {
     mbar_init(&s.q_full, 1);
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&s.k_full[i], 1);
@@ -201,15 +194,28 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_q,
         tma_load_3d(s.q[1][1], &map_q, &s.q_full, 64, h0 + 1, t_glob0);
       }
       int issued = 0;
+      // page ids read three tiles ahead, so no TMA issue waits on a block-table load
+      auto page_id = [&](int j) -> int32_t { return j < ntiles ? table[kt_hi - j] : 0; };
+      int32_t id1 = page_id(0), id2 = page_id(1), id3 = page_id(2);
       for (int i = 0; i < ntiles; ++i) {
         const int st = i % kStages;
         const uint32_t eph = ((i / kStages) - 1) & 1;
+        const int32_t blk = id1;
+        id1 = id2;
+        id2 = id3;
+        id3 = page_id(i + 3);
         if (i >= kStages && !mbar_wait(&s.k_empty[st], eph, abort_flag, p.status)) {
           report(p.status, kErrTimeout);
           s.abort_flag = 1;
           break;
         }
-        const int page = table[kt_hi - i] * p.Hkv + kvh;
+        if (blk < 0 || (long long)blk >= p.num_blocks) {
+          report(p.status, kErrBadBlock);  // first error wins: reported before the abort
+          s.abort_flag = 1;
+          issued = i;
+          break;
+        }
+        const int page = blk * p.Hkv + kvh;
         mbar_arrive_expect_tx(&s.k_full[st], 32768u);
         tma_load_3d(s.k[st][0], &map_k, &s.k_full[st], 0, 0, page);
         tma_load_3d(s.k[st][1], &map_k, &s.k_full[st], 64, 0, page);
@@ -228,6 +234,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_q,
       }
       if (*abort_flag) {
         // let the copies already in flight land before the CTA goes away
+        volatile int never_q = 0;
+        mbar_wait(&s.q_full, 0, &never_q);
         for (int i = max(0, issued - kStages); i < issued; ++i) {
           const int st = i % kStages;
           const uint32_t ph = (i / kStages) & 1;
@@ -246,7 +254,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_q,
     const int slot = warp - 10;
     const bool mine = slot == 0 || has_b;
     const float* brow = p.bias + (size_t)(h0 + slot) * p.R;
-    const int R = p.R;
+    const int R = p.R, W = p.window;
     for (int i = 0; i < ntiles; ++i) {
       const int st = i % kStages;
       int ok = 1;
@@ -255,15 +263,19 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_q,
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       const int delta = P0 - (kt_hi - i) * kTile;
-      if (mine && delta - 127 < R - 1) {
+      const bool masked = delta < 127 || (W > 0 && delta + 127 > W - 1);
+      if (mine && (delta - 127 < R - 1 || masked)) {
+        // rev[j] at distance d = delta + 127 - j: b[h][min(d, R-1)], or -inf where d is
+        // not attended (d < 0, or past the window), so the mask rides on the bias
         float* dst = &s.bias[st][slot][0];
 #pragma unroll
         for (int j = lane; j < 256; j += 32) {
-          int d = delta + 127 - j;
-          d = d < 0 ? 0 : (d > R - 1 ? R - 1 : d);
+          const int d = delta + 127 - j;
+          const bool off = d < 0 || (W > 0 && d > W - 1);
+          const float* src = off ? &kMaskedBias : brow + (d > R - 1 ? R - 1 : d);
 #pragma unroll
           for (int c = 0; c < 4; ++c)
-            if (j >= c) cp_async_4(dst + c * kBiasCopyStride + j - c, brow + d);
+            if (j >= c) cp_async_4(dst + c * kBiasCopyStride + j - c, src);
         }
       }
       cp_async_mbar_arrive(&s.b_full[st]);
@@ -275,6 +287,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_q,
     bool ok = mbar_wait(&s.q_full, 0, abort_flag, p.status) && mbar_wait(&s.k_full[0], 0, abort_flag, p.status);
     bool issued_any = false;
     if (ok) {
+      // tile 0 holds the diagonal: keys past the end of the sequence are stale slots
+      if ((kt_hi + 1) * kTile > L) zero_tail_rows(s.k[0], L - kt_hi * kTile, lane);
       tc_fence_after();
       if (lane == 0) {
 #pragma unroll
@@ -298,18 +312,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_q,
       const uint32_t ph = (i / kStages) & 1;
       ok = mbar_wait(&s.p_full[0], i & 1, abort_flag, p.status) && mbar_wait(&s.v_full[st], ph, abort_flag, p.status);
       if (!ok) break;
-      if (i == 0 && (kt_hi + 1) * kTile > L) {
-        // keys past the end of the sequence: their P is 0, but junk V could be NaN
-        const int r0 = L - kt_hi * kTile;
-        const int chunks = (kTile - r0) * 8;  // 16-byte chunks per d half
-        for (int c = lane; c < 2 * chunks; c += 32) {
-          const int half = c / chunks, cc = c % chunks;
-          *reinterpret_cast<uint4*>(s.v[st][half] + (size_t)(r0 + cc / 8) * 128 + (cc % 8) * 16) =
-              make_uint4(0, 0, 0, 0);
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-      }
+      // keys past the end of the sequence: their P is 0, but junk V could be NaN
+      if (i == 0 && (kt_hi + 1) * kTile > L) zero_tail_rows(s.v[st], L - kt_hi * kTile, lane);
       tc_fence_after();
       if (lane == 0) {
 #pragma unroll
@@ -392,8 +396,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_q,
       for (int i = 0; i < ntiles; ++i) {
         const int k0 = (kt_hi - i) * kTile;
         const int delta = P0 - k0;
-        const bool clamped = delta - 127 >= R - 1;  // every distance past the table end
-        const bool masked = (delta < 127) || (W > 0 && delta + 127 > W - 1) || (k0 + 127 >= L);
+        // the single clamped value serves only tiles with every distance past the table end
+        // and attended; the others read the staged slice, which carries the mask as -inf
+        const bool clamped = delta - 127 >= R - 1 && !(delta < 127 || (W > 0 && delta + 127 > W - 1));
         const float* bias_buf = &s.bias[i % kStages][grp][0];
         if (!clamped && !mbar_wait(&s.b_full[i % kStages], (i / kStages) & 1, abort_flag, p.status)) {
           ok = false;
@@ -441,19 +446,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_q,
             const float4 b4 = rb4[k >> 1];
             x[k] = __ffma2_rn(sv0, sc2, make_float2(b4.x, b4.y));
             x[k + 1] = __ffma2_rn(sv1, sc2, make_float2(b4.z, b4.w));
-          }
-        }
-        if (masked) {
-          const int dr = delta + r;  // distance at column 0
-          const int kend = L - k0;   // columns >= kend are past the sequence
-#pragma unroll
-          for (int k = 0; k < 64; ++k) {
-            const int c = 2 * k;
-            const int d = dr - c;
-            const bool a0 = d >= 0 && (W == 0 || d <= W - 1) && c < kend;
-            const bool a1 = d - 1 >= 0 && (W == 0 || d - 1 <= W - 1) && c + 1 < kend;
-            x[k].x = a0 ? x[k].x : -INFINITY;
-            x[k].y = a1 ? x[k].y : -INFINITY;
           }
         }
         float mx0 = fmax3(x[0].x, x[0].y, x[1].x), mx1 = fmax3(x[1].y, x[2].x, x[2].y);

@@ -317,4 +317,19 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// Keys at or past the end of a sequence live in cache slots nobody wrote: zero rows
+// r0..127 of a staged 128-row K or V page (two 64-wide d halves of 128-byte rows, 16 KB
+// apart) so that no stale NaN reaches an MMA.  One warp; the generic-proxy stores are
+// fenced for the tensor core's async-proxy reads.
+__device__ __forceinline__ void zero_tail_rows(uint8_t (*page)[16384], int r0, int lane) {
+  const int chunks = (128 - r0) * 8;  // 16-byte chunks per d half
+  for (int c = lane; c < 2 * chunks; c += 32) {
+    const int half = c / chunks, cc = c % chunks;
+    *reinterpret_cast<uint4*>(page[half] + (size_t)(r0 + cc / 8) * 128 + (cc % 8) * 16) =
+        make_uint4(0, 0, 0, 0);
+  }
+  fence_proxy_async_smem();
+  __syncwarp();
+}
+
 }  // namespace ink
