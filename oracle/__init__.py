@@ -57,6 +57,20 @@ def lib():
         L.oracle_sconv_rollback.restype = ctypes.c_int
         L.oracle_sconv_rollback.argtypes = [P, P, P, P, P, P, ctypes.c_int, ctypes.c_int,
                                             ctypes.c_int]
+        L.oracle_e4m3_round.restype = ctypes.c_uint8
+        L.oracle_e4m3_round.argtypes = [ctypes.c_double]
+        L.oracle_e4m3_to_double.restype = ctypes.c_double
+        L.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
+        L.oracle_sconv_kv_fp8.restype = ctypes.c_int
+        L.oracle_sconv_kv_fp8.argtypes = [P, P, P, P, P, P, P, P, P, ctypes.c_double,
+                                          ctypes.c_double, ctypes.c_int, ctypes.c_int,
+                                          ctypes.c_int, ctypes.c_int64]
+        L.oracle_rel_attn_fp8.restype = ctypes.c_int
+        L.oracle_rel_attn_fp8.argtypes = [P, P, P, ctypes.c_double, ctypes.c_double, P,
+                                          ctypes.c_int, P, P, P, ctypes.c_int, ctypes.c_double,
+                                          ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                          ctypes.c_int, ctypes.c_int64, P, ctypes.c_int, P, P,
+                                          ctypes.c_int]
         L.oracle_rel_attn.restype = ctypes.c_int
         L.oracle_rel_attn.argtypes = [P, P, P, P, ctypes.c_int, P, P, P, ctypes.c_int,
                                       ctypes.c_double, ctypes.c_int, ctypes.c_int, ctypes.c_int,
@@ -186,3 +200,67 @@ def sconv_rollback(state_before, x0, x1, cu_q_lens, accepted):
     if rc != 0:
         raise RuntimeError(f"oracle_sconv_rollback: {STATUS.get(rc, rc)}")
     return out
+
+
+# ----------------------------------------------------------------- FP8 KV cache ----
+
+def e4m3_round(y: float) -> int:
+    """Round a float64 to an OCP E4M3 code (nearest, ties to even, saturating at 448)."""
+    return int(lib().oracle_e4m3_round(float(y)))
+
+
+def e4m3_to_float(code: int) -> float:
+    return float(lib().oracle_e4m3_to_double(int(code) & 0xFF))
+
+
+def _u8(t) -> np.ndarray:
+    if isinstance(t, np.ndarray):
+        assert t.dtype == np.uint8
+        return np.ascontiguousarray(t)
+    assert t.dtype == torch.uint8 and t.device.type == "cpu"
+    return t.contiguous().numpy()
+
+
+def sconv_kv_fp8(k_raw, v_raw, w_k, w_v, state, cu_q_lens, slot_mapping, k_cache, v_cache,
+                 k_scale: float, v_scale: float):
+    """sconv_kv into FP8 caches (uint8 E4M3 codes, updated in place): code = e4m3(y / scale)."""
+    for t in (k_cache, v_cache):
+        assert t.is_contiguous() and t.dtype == torch.uint8 and t.device.type == "cpu"
+    assert state.is_contiguous() and state.dtype == torch.bfloat16
+    kr, vr = _u16(k_raw), _u16(v_raw)
+    wk, wv = _arr(w_k, np.float32), _arr(w_v, np.float32)
+    st = state.view(torch.int16).numpy().view(np.uint16)
+    kc, vc = k_cache.numpy(), v_cache.numpy()
+    cu = _arr(cu_q_lens, np.int32)
+    sm = _arr(slot_mapping, np.int64)
+    B = cu.shape[0] - 1
+    T = kr.shape[0] if kr.ndim == 2 else 0
+    rc = lib().oracle_sconv_kv_fp8(_ptr(kr), _ptr(vr), _ptr(wk), _ptr(wv), _ptr(st), _ptr(cu),
+                                   _ptr(sm), _ptr(kc), _ptr(vc), float(k_scale), float(v_scale),
+                                   B, T, kc.shape[1], kc.shape[0])
+    if rc != 0:
+        raise RuntimeError(f"oracle_sconv_kv_fp8: {STATUS.get(rc, rc)}")
+
+
+def rel_attn_fp8(q, k_cache, v_cache, k_scale: float, v_scale: float, block_table, cu_q_lens,
+                 seq_lens, bias, *, scale: float, window: int, rows=None, n_threads=None):
+    """rel_attn over FP8 caches: K = e4m3(code) * k_scale, V = e4m3(code) * v_scale."""
+    qa = _u16(q)
+    kc, vc = _u8(k_cache), _u8(v_cache)
+    bt = _arr(block_table, np.int32)
+    cu = _arr(cu_q_lens, np.int32)
+    sl = _arr(seq_lens, np.int32)
+    bi = _arr(bias, np.float32)
+    T, hq = qa.shape[0], qa.shape[1]
+    rows = np.arange(T, dtype=np.int32) if rows is None else _arr(rows, np.int32)
+    out = np.zeros((rows.shape[0], hq, 128), dtype=np.float64)
+    lse = np.zeros((rows.shape[0], hq), dtype=np.float64)
+    rc = lib().oracle_rel_attn_fp8(_ptr(qa), _ptr(kc), _ptr(vc), float(k_scale), float(v_scale),
+                                   _ptr(bt), bt.shape[1], _ptr(cu), _ptr(sl), _ptr(bi),
+                                   bi.shape[1], float(scale), int(window), cu.shape[0] - 1, T,
+                                   hq, kc.shape[1], kc.shape[0], _ptr(rows), rows.shape[0],
+                                   _ptr(out), _ptr(lse),
+                                   host_cores() if n_threads is None else int(n_threads))
+    if rc != 0:
+        raise RuntimeError(f"oracle_rel_attn_fp8: {STATUS.get(rc, rc)}")
+    return out, lse

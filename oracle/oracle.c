@@ -31,6 +31,12 @@
  * Storage: the KV cache is paged, [num_blocks][Hkv][128 slots][128 dims] bf16; logical
  * key j of sequence b lives in page block_table[b][j / 128], slot j % 128.  bf16 values
  * are passed as their 16-bit patterns.
+ *
+ * FP8 KV cache (the blog's "Roadmap": FP8 attention and KV cache for the full-attention
+ * layers, not specified further): the same pages hold one byte per element in the OCP
+ * E4M3 format, code = e4m3(y / scale) rounded to nearest even and saturated at +-448,
+ * with one fp32 scale for K and one for V; attention reads K = e4m3(code) * k_scale and
+ * V = e4m3(code) * v_scale.
  */
 #include <math.h>
 #include <pthread.h>
@@ -139,7 +145,8 @@ int oracle_sconv_kv(const uint16_t *k_raw, const uint16_t *v_raw, const float *w
 /* ---------------------------------------------------------------- attention ---- */
 
 typedef struct {
-    const uint16_t *q, *k_cache, *v_cache;
+    const uint16_t *q;
+    const void *k_cache, *v_cache;  /* bf16 patterns, or e4m3 codes when kv_fp8 */
     const int32_t *block_table, *cu_q_lens, *seq_lens, *rows;
     const float *bias;
     int max_blocks, R, window, B, T, Hq, Hkv, n_rows;
@@ -148,7 +155,19 @@ typedef struct {
     double *out, *lse;
     long next;  /* shared work counter over (row, head) items */
     int status;
+    int kv_fp8;
+    double k_scale, v_scale;
 } attn_job;
+
+double oracle_e4m3_to_double(uint8_t c);
+
+/* Element d of cache row `row` (an element index) as a double: a bf16 pattern, or an
+ * e4m3 code times the cache's scale. */
+static double kv_elem(const attn_job *jb, const void *cache, size_t idx, double scale)
+{
+    if (jb->kv_fp8) return oracle_e4m3_to_double(((const uint8_t *)cache)[idx]) * scale;
+    return oracle_bf16_to_double(((const uint16_t *)cache)[idx]);
+}
 
 static int seq_of_token(const int32_t *cu, int B, int t)
 {
@@ -182,10 +201,9 @@ static int attend_one(attn_job *jb, int item, double *s)
     for (int j = j_lo; j <= j_hi; ++j) {
         const int32_t blk = jb->block_table[(size_t)b * jb->max_blocks + j / OR_PAGE];
         if (blk < 0 || blk >= jb->num_blocks) return OR_ERR_BLOCK;
-        const uint16_t *krow =
-            jb->k_cache + (((size_t)blk * jb->Hkv + kv) * OR_PAGE + j % OR_PAGE) * OR_D;
+        const size_t krow = (((size_t)blk * jb->Hkv + kv) * OR_PAGE + j % OR_PAGE) * OR_D;
         double dot = 0.0;
-        for (int d = 0; d < OR_D; ++d) dot += qd[d] * oracle_bf16_to_double(krow[d]);
+        for (int d = 0; d < OR_D; ++d) dot += qd[d] * kv_elem(jb, jb->k_cache, krow + d, jb->k_scale);
         const int dist = p - j;
         const int bi = dist < jb->R - 1 ? dist : jb->R - 1;
         s[j - j_lo] = jb->scale * dot + (double)jb->bias[(size_t)h * jb->R + bi];
@@ -197,9 +215,8 @@ static int attend_one(attn_job *jb, int item, double *s)
         const double e = exp(s[j - j_lo] - smax);
         denom += e;
         const int32_t blk = jb->block_table[(size_t)b * jb->max_blocks + j / OR_PAGE];
-        const uint16_t *vrow =
-            jb->v_cache + (((size_t)blk * jb->Hkv + kv) * OR_PAGE + j % OR_PAGE) * OR_D;
-        for (int d = 0; d < OR_D; ++d) acc[d] += e * oracle_bf16_to_double(vrow[d]);
+        const size_t vrow = (((size_t)blk * jb->Hkv + kv) * OR_PAGE + j % OR_PAGE) * OR_D;
+        for (int d = 0; d < OR_D; ++d) acc[d] += e * kv_elem(jb, jb->v_cache, vrow + d, jb->v_scale);
     }
     double *o = jb->out + ((size_t)ri * jb->Hq + h) * OR_D;
     for (int d = 0; d < OR_D; ++d) o[d] = acc[d] / denom;
@@ -231,11 +248,12 @@ static void *attn_worker(void *arg)
  * q [T][Hq][128]; block_table [B][max_blocks]; bias [Hq][R] fp32;
  * out [n_rows][Hq][128] fp64; lse [n_rows][Hq] fp64 (natural log; may be NULL).
  */
-int oracle_rel_attn(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
-                    const int32_t *block_table, int max_blocks, const int32_t *cu_q_lens,
-                    const int32_t *seq_lens, const float *bias, int R, double scale,
-                    int window, int B, int T, int Hq, int Hkv, int64_t num_blocks,
-                    const int32_t *rows, int n_rows, double *out, double *lse, int n_threads)
+static int run_attn(const uint16_t *q, const void *k_cache, const void *v_cache, int kv_fp8,
+                    double k_scale, double v_scale, const int32_t *block_table, int max_blocks,
+                    const int32_t *cu_q_lens, const int32_t *seq_lens, const float *bias,
+                    int R, double scale, int window, int B, int T, int Hq, int Hkv,
+                    int64_t num_blocks, const int32_t *rows, int n_rows, double *out,
+                    double *lse, int n_threads)
 {
     if (B <= 0 || T < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || R < 1 || window < 0 ||
         n_rows < 0 || max_blocks <= 0)
@@ -248,7 +266,7 @@ int oracle_rel_attn(const uint16_t *q, const uint16_t *k_cache, const uint16_t *
         if (rows[i] < 0 || rows[i] >= T) return OR_ERR_ARG;
     attn_job jb = {q, k_cache, v_cache, block_table, cu_q_lens, seq_lens, rows, bias,
                    max_blocks, R, window, B, T, Hq, Hkv, n_rows, num_blocks, scale,
-                   out, lse, 0, OR_OK};
+                   out, lse, 0, OR_OK, kv_fp8, k_scale, v_scale};
     if (n_threads < 1) n_threads = 1;
     if (n_threads > 512) n_threads = 512;
     pthread_t th[512];
@@ -260,6 +278,30 @@ int oracle_rel_attn(const uint16_t *q, const uint16_t *k_cache, const uint16_t *
     if (started == 0) attn_worker(&jb);
     for (int i = 0; i < started; ++i) pthread_join(th[i], NULL);
     return jb.status;
+}
+
+int oracle_rel_attn(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                    const int32_t *block_table, int max_blocks, const int32_t *cu_q_lens,
+                    const int32_t *seq_lens, const float *bias, int R, double scale,
+                    int window, int B, int T, int Hq, int Hkv, int64_t num_blocks,
+                    const int32_t *rows, int n_rows, double *out, double *lse, int n_threads)
+{
+    return run_attn(q, k_cache, v_cache, 0, 1.0, 1.0, block_table, max_blocks, cu_q_lens,
+                    seq_lens, bias, R, scale, window, B, T, Hq, Hkv, num_blocks, rows, n_rows,
+                    out, lse, n_threads);
+}
+
+/* The same attention over an FP8 cache: K = e4m3(code) * k_scale, V = e4m3(code) * v_scale. */
+int oracle_rel_attn_fp8(const uint16_t *q, const uint8_t *k_cache, const uint8_t *v_cache,
+                        double k_scale, double v_scale, const int32_t *block_table,
+                        int max_blocks, const int32_t *cu_q_lens, const int32_t *seq_lens,
+                        const float *bias, int R, double scale, int window, int B, int T,
+                        int Hq, int Hkv, int64_t num_blocks, const int32_t *rows, int n_rows,
+                        double *out, double *lse, int n_threads)
+{
+    return run_attn(q, k_cache, v_cache, 1, k_scale, v_scale, block_table, max_blocks,
+                    cu_q_lens, seq_lens, bias, R, scale, window, B, T, Hq, Hkv, num_blocks,
+                    rows, n_rows, out, lse, n_threads);
 }
 
 /* ------------------------------------------------- sconv on a dense stream ---- */
@@ -330,6 +372,90 @@ int oracle_sconv_rollback(const uint16_t *state_before, const uint16_t *x0,
                 const uint16_t *src = e < 3 ? sb + (size_t)e * C : x + (size_t)(t0 + e - 3) * C;
                 memcpy(sa + (size_t)r * C, src, sizeof(uint16_t) * (size_t)C);
             }
+        }
+    }
+    return OR_OK;
+}
+
+/* ------------------------------------------------------------ FP8 (E4M3) ---- */
+
+/* e4m3 code -> double, exact.  Bit 7 sign, bits 6..3 exponent (bias 7), bits 2..0
+ * mantissa; exponent 0 holds subnormals m * 2^-9; S.1111.111 is NaN (no infinities), so
+ * the largest finite value is 1.75 * 2^8 = 448. */
+double oracle_e4m3_to_double(uint8_t c)
+{
+    const int e = (c >> 3) & 15, m = c & 7;
+    if (e == 15 && m == 7) return NAN;
+    const double v = e == 0 ? ldexp((double)m, -9) : ldexp((double)(8 + m), e - 10);
+    return (c & 0x80) ? -v : v;
+}
+
+/* double -> e4m3 code, round to nearest with ties to even, saturating: |y| >= 448 gives
+ * +-448, NaN gives 0x7f.  The non-negative finite codes 0..126 increase with their value,
+ * so the two neighbours of |y| are found by walking the codes; on a tie the even code
+ * (mantissa LSB 0) wins. */
+uint8_t oracle_e4m3_round(double y)
+{
+    if (isnan(y)) return 0x7f;
+    const uint8_t sign = signbit(y) ? 0x80 : 0;
+    const double a = fabs(y);
+    if (a >= 448.0) return sign | 0x7e;
+    int lo = 0;
+    while (lo < 126 && oracle_e4m3_to_double((uint8_t)(lo + 1)) <= a) ++lo;
+    const double vlo = oracle_e4m3_to_double((uint8_t)lo);
+    if (vlo == a) return sign | (uint8_t)lo;
+    const double vhi = oracle_e4m3_to_double((uint8_t)(lo + 1));
+    const double dlo = a - vlo, dhi = vhi - a;
+    const int c = dlo < dhi ? lo : (dhi < dlo ? lo + 1 : ((lo & 1) ? lo + 1 : lo));
+    return sign | (uint8_t)c;
+}
+
+/*
+ * oracle_sconv_kv with an FP8 cache: the same conv sum y in fp64, stored as
+ * e4m3(y / k_scale) in the K cache and e4m3(y / v_scale) in the V cache; the state update
+ * is unchanged.  Caches [num_blocks][Hkv][128][128] bytes.
+ */
+int oracle_sconv_kv_fp8(const uint16_t *k_raw, const uint16_t *v_raw, const float *w_k,
+                        const float *w_v, uint16_t *state, const int32_t *cu_q_lens,
+                        const int64_t *slot_mapping, uint8_t *k_cache, uint8_t *v_cache,
+                        double k_scale, double v_scale, int B, int T, int Hkv,
+                        int64_t num_blocks)
+{
+    if (B < 0 || T < 0 || Hkv <= 0 || num_blocks < 0 || !(k_scale > 0) || !(v_scale > 0))
+        return OR_ERR_ARG;
+    if (cu_q_lens[0] != 0 || cu_q_lens[B] != T) return OR_ERR_ARG;
+    const int C = Hkv * OR_D;
+    for (int b = 0; b < B; ++b) {
+        const int t0 = cu_q_lens[b];
+        const int n = cu_q_lens[b + 1] - t0;
+        if (n < 0) return OR_ERR_ARG;
+        for (int which = 0; which < 2; ++which) {
+            const uint16_t *x = which == 0 ? k_raw : v_raw;
+            const float *w = which == 0 ? w_k : w_v;
+            uint8_t *cache = which == 0 ? k_cache : v_cache;
+            const double scale = which == 0 ? k_scale : v_scale;
+            uint16_t *st = state + ((size_t)b * 2 + which) * 3 * C;
+            uint16_t *ext = malloc(sizeof(uint16_t) * (size_t)(n + 3) * C);
+            if (!ext) return OR_ERR_NOMEM;
+            memcpy(ext, st, sizeof(uint16_t) * 3 * (size_t)C);
+            memcpy(ext + 3 * (size_t)C, x + (size_t)t0 * C, sizeof(uint16_t) * (size_t)n * C);
+            for (int t = 0; t < n; ++t) {
+                const int64_t slot = slot_mapping[t0 + t];
+                if (slot < 0) continue;
+                if (slot >= num_blocks * OR_PAGE) { free(ext); return OR_ERR_BLOCK; }
+                const int64_t blk = slot / OR_PAGE, off = slot % OR_PAGE;
+                for (int c = 0; c < C; ++c) {
+                    double y = 0.0;
+                    for (int j = 0; j < OR_TAPS; ++j)
+                        y += (double)w[(size_t)c * OR_TAPS + j] *
+                             oracle_bf16_to_double(ext[(size_t)(t + j) * C + c]);
+                    const int h = c / OR_D, d = c % OR_D;
+                    cache[(((size_t)blk * Hkv + h) * OR_PAGE + off) * OR_D + d] =
+                        oracle_e4m3_round(y / scale);
+                }
+            }
+            memcpy(st, ext + (size_t)n * C, sizeof(uint16_t) * 3 * (size_t)C);
+            free(ext);
         }
     }
     return OR_OK;
