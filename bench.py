@@ -8,6 +8,8 @@ Default workload (one step = the whole hot path over one batch):
 Metric: attention TFLOP/s counting only allowed (query, key) pairs, 4*D flops per pair
 per head (QK^T and PV).  Other workloads (--workload 1..5) print the same line shape;
 the decode ones report KV-read GB/s (algorithmic K/V bytes inside the causal/window range).
+--kv fp8 (decode workloads) runs the FP8 KV cache path (inkling_sconv_kv_fp8 +
+inkling_rel_attn_decode_fp8); its GB/s count the E4M3 bytes, half of the bf16 cache's.
 --workload 4 also times the sconv-state rollback after the verify step on its own
 (config.rollback_us, not part of the step).  --workload 6 is the conv on a dense stream
 (inkling_sconv on the sliding-window prefill's attention output, 32768 tokens x 4096
@@ -205,7 +207,14 @@ def run_ours(args, ws, rank, local):
     ink._lib.load()  # raises if the CUDA library is missing: no fallback
     spec = workload_spec(args.workload, args.variant)
     decode = is_decode(args.workload)
+    fp8 = args.kv == "fp8"
+    if fp8 and not decode:
+        raise SystemExit("--kv fp8 applies to the decode workloads (4, 5)")
     g = W.make_case(spec, seed=args.workload + 1000 * rank, device=dev)
+    K_SCALE, V_SCALE = 0.0625, 0.0625
+    if fp8:
+        g.k_cache = W.fp8_history(g.k_cache, K_SCALE)
+        g.v_cache = W.fp8_history(g.v_cache, V_SCALE)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     out = torch.empty(spec.total_q, spec.hq, 128, dtype=torch.bfloat16, device=dev)
     state0 = g.state.clone()
@@ -219,7 +228,13 @@ def run_ours(args, ws, rank, local):
     stream = torch.cuda.current_stream()
 
     def attn(q, o):
-        if decode:
+        if fp8:
+            ink.rel_attn_decode_fp8(q, g.k_cache, g.v_cache, g.block_table, g.cu_q_lens,
+                                    g.seq_lens, g.bias, k_scale=K_SCALE, v_scale=V_SCALE,
+                                    scale=spec.scale, window=spec.window,
+                                    max_q_len=spec.max_q_len, max_seq_len=spec.max_seq_len,
+                                    out=o, workspace=workspace, dev_status=status)
+        elif decode:
             ink.rel_attn_decode(q, g.k_cache, g.v_cache, g.block_table, g.cu_q_lens, g.seq_lens,
                                 g.bias, scale=spec.scale, window=spec.window,
                                 max_q_len=spec.max_q_len, max_seq_len=spec.max_seq_len, out=o,
@@ -230,8 +245,13 @@ def run_ours(args, ws, rank, local):
                                  max_q_len=spec.max_q_len, out=o, dev_status=status)
 
     def sconv(kr, vr):
-        ink.sconv_kv(kr, vr, g.w_k, g.w_v, g.state, g.cu_q_lens, g.slot_mapping, g.k_cache,
-                     g.v_cache, max_q_len=spec.max_q_len, dev_status=status)
+        if fp8:
+            ink.sconv_kv_fp8(kr, vr, g.w_k, g.w_v, g.state, g.cu_q_lens, g.slot_mapping,
+                             g.k_cache, g.v_cache, k_scale=K_SCALE, v_scale=V_SCALE,
+                             max_q_len=spec.max_q_len, dev_status=status)
+        else:
+            ink.sconv_kv(kr, vr, g.w_k, g.w_v, g.state, g.cu_q_lens, g.slot_mapping, g.k_cache,
+                         g.v_cache, max_q_len=spec.max_q_len, dev_status=status)
 
     def reset():
         g.state.copy_(state0)
@@ -317,7 +337,7 @@ def run_ours(args, ws, rank, local):
 
     peaks, peak_src = measured_peaks()
     if decode:
-        work = decode_kv_bytes(spec)
+        work = decode_kv_bytes(spec) / (2 if fp8 else 1)
         unit = "GB/s"
         value = ws * work / (step_ms * 1e-3) / 1e9
         e2e_value = ws * work / (e2e_ms * 1e-3) / 1e9
@@ -325,7 +345,8 @@ def run_ours(args, ws, rank, local):
         peak = float(peaks["hbm_gbs"])
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": None,
-                "peak_source": f"{peak_src} hbm_gbs", "kernel": "decode_kernel (+combine)"}
+                "peak_source": f"{peak_src} hbm_gbs",
+                "kernel": "decode_kernel<true> (FP8 cache)" if fp8 else "decode_kernel (+combine)"}
     else:
         work = attn_flops(spec)
         unit = "TFLOP/s"
@@ -341,9 +362,11 @@ def run_ours(args, ws, rank, local):
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": unit, "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16 (KV cache e4m3, f16 MMA)" if fp8 else "bf16",
         "data": "synthetic (seeded N(0,1) Q/K/V, N(0,0.5) sconv taps, N(0,sd) bias)",
-        "config": {"workload": workload_name(spec), "global_batch": spec.batch * ws,
+        "config": {"workload": workload_name(spec) + (" kv=e4m3" if fp8 else ""),
+                   "global_batch": spec.batch * ws,
                    "seq_len": spec.max_seq_len, "parallelism": f"replicas x{ws}",
                    "l2": "flushed (512 MB write) between timed steps",
                    "attn_ms": round(attn_ms, 4), "sconv_ms": round(sconv_ms, 4)},
@@ -561,6 +584,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5, 6])
     ap.add_argument("--variant", default=None, help="mtp_decode: swa|full; decode_1m: n1|n9")
+    ap.add_argument("--kv", choices=["bf16", "fp8"], default="bf16",
+                    help="KV cache type for the decode workloads")
     ap.add_argument("--ref-seconds", type=float, default=6.0,
                     help="oracle seconds per reference step / for the cpu_baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -114,6 +114,25 @@ INKLING_API int inkling_sconv_kv(const void *k_raw, const void *v_raw, const flo
                      inkling_stream_t stream);
 
 /*
+ * inkling_sconv_kv_fp8 — inkling_sconv_kv writing an FP8 KV cache (blog, "Roadmap": FP8
+ * for the global-attention layers).  The caches hold one OCP E4M3
+ * byte per element in the same page layout, [num_blocks][Hkv][128 slots][128 dims] uint8:
+ *
+ *   cache[slot_mapping[t]] = e4m3(y[t] / scale)   (round to nearest even, saturating at
+ *                                                  +-448; k_scale for K, v_scale for V)
+ *
+ * with y computed as in inkling_sconv_kv (fp32); the sconv state update is unchanged.
+ * k_scale, v_scale: finite and > 0 (else INKLING_ERR_INVALID_ARG).  Other arguments and
+ * errors as inkling_sconv_kv.
+ */
+INKLING_API int inkling_sconv_kv_fp8(const void *k_raw, const void *v_raw, const float *w_k,
+                         const float *w_v, void *sconv_state, const int32_t *cu_q_lens,
+                         const int64_t *slot_mapping, void *k_cache, void *v_cache,
+                         float k_scale, float v_scale, int32_t B, int32_t T, int32_t Hkv,
+                         int64_t num_blocks, int32_t max_q_len, int32_t *dev_status,
+                         inkling_stream_t stream);
+
+/*
  * inkling_sconv — the same window-4 causal short convolution on one dense stream with
  * its own 3-row cache (blog, "Model Architecture / Sconv": the conv also follows the
  * attention output projection, "all-reduce (after o_proj) -> sconv -> residual").
@@ -205,6 +224,24 @@ INKLING_API int inkling_rel_attn_decode(const void *q, const void *k_cache, cons
                             int32_t max_seq_len, int32_t num_splits, void *workspace,
                             size_t workspace_bytes, int32_t *dev_status,
                             inkling_stream_t stream);
+
+/*
+ * inkling_rel_attn_decode_fp8 — inkling_rel_attn_decode over an FP8 KV cache written by
+ * inkling_sconv_kv_fp8: K = e4m3(code) * k_scale, V = e4m3(code) * v_scale.  The pages
+ * are read as bytes (half the HBM traffic of the bf16 cache) and widened to f16 in shared
+ * memory, which is exact; Q, P and the products then run on the f16 tensor core with
+ * fp32 accumulation, so Q must lie in the f16 range (|q| < 65504).  Arguments, workspace
+ * and errors as inkling_rel_attn_decode (the workspace size query is the same call).
+ */
+INKLING_API int inkling_rel_attn_decode_fp8(const void *q, const void *k_cache, const void *v_cache,
+                                float k_scale, float v_scale, const int32_t *block_table,
+                                int32_t max_blocks, const int32_t *cu_q_lens,
+                                const int32_t *seq_lens, const float *bias, int32_t R,
+                                float scale, int32_t window, void *out, int32_t out_dtype,
+                                float *lse, int32_t B, int32_t T, int32_t Hq, int32_t Hkv,
+                                int64_t num_blocks, int32_t max_q_len, int32_t max_seq_len,
+                                int32_t num_splits, void *workspace, size_t workspace_bytes,
+                                int32_t *dev_status, inkling_stream_t stream);
 
 /*
  * inkling_rel_attn_decode_noalloc — inkling_rel_attn_decode for callers that cannot give

@@ -32,8 +32,8 @@
  * key j of sequence b lives in page block_table[b][j / 128], slot j % 128.  bf16 values
  * are passed as their 16-bit patterns.
  *
- * FP8 KV cache (the blog's "Roadmap": FP8 attention and KV cache for the full-attention
- * layers, not specified further): the same pages hold one byte per element in the OCP
+ * FP8 KV cache (the blog's "Roadmap" plans FP8 for the global-attention layers, whose
+ * BF16 compute and KV cache it names as a bottleneck; nothing more is specified): the same pages hold one byte per element in the OCP
  * E4M3 format, code = e4m3(y / scale) rounded to nearest even and saturated at +-448,
  * with one fp32 scale for K and one for V; attention reads K = e4m3(code) * k_scale and
  * V = e4m3(code) * v_scale.

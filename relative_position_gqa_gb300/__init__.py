@@ -63,6 +63,22 @@ def sconv_kv(k_raw: torch.Tensor, v_raw: torch.Tensor, w_k: torch.Tensor, w_v: t
                   dev_status, _stream(stream))
 
 
+def sconv_kv_fp8(k_raw, v_raw, w_k, w_v, sconv_state, cu_q_lens, slot_mapping, k_cache,
+                 v_cache, *, k_scale: float, v_scale: float, max_q_len: int,
+                 dev_status=None, stream=None) -> None:
+    """inkling_sconv_kv_fp8: the conv into FP8 (E4M3, uint8) paged caches,
+    code = e4m3(y / scale)."""
+    dev = _check_cuda(k_raw, v_raw, w_k, w_v, sconv_state, cu_q_lens, slot_mapping, k_cache,
+                      v_cache, dev_status)
+    assert k_raw.dtype == v_raw.dtype == sconv_state.dtype == torch.bfloat16
+    assert k_cache.dtype == v_cache.dtype == torch.uint8
+    with torch.cuda.device(dev):
+        _lib.call("inkling_sconv_kv_fp8", k_raw, v_raw, w_k, w_v, sconv_state, cu_q_lens,
+                  slot_mapping, k_cache, v_cache, float(k_scale), float(v_scale),
+                  cu_q_lens.shape[0] - 1, k_raw.shape[0], k_cache.shape[1], k_cache.shape[0],
+                  int(max_q_len), dev_status, _stream(stream))
+
+
 def sconv(x: torch.Tensor, w: torch.Tensor, sconv_state: torch.Tensor, cu_q_lens: torch.Tensor,
           *, max_q_len: int, y: Optional[torch.Tensor] = None, dev_status=None,
           stream=None) -> torch.Tensor:
@@ -161,6 +177,35 @@ def rel_attn_decode(q, k_cache, v_cache, block_table, cu_q_lens, seq_lens, bias,
                   int(window), out, out_dtype, lse, B, T, hq, hkv, k_cache.shape[0],
                   int(max_q_len), int(max_seq_len), int(num_splits), workspace, ws_bytes,
                   dev_status, _stream(stream))
+
+
+def rel_attn_decode_fp8(q, k_cache, v_cache, block_table, cu_q_lens, seq_lens, bias, *,
+                        k_scale: float, v_scale: float, scale: float, window: int,
+                        max_q_len: int, max_seq_len: int, out: torch.Tensor,
+                        lse: Optional[torch.Tensor] = None, num_splits: int = 0,
+                        workspace: Optional[torch.Tensor] = None, dev_status=None,
+                        stream=None) -> None:
+    """inkling_rel_attn_decode_fp8: decode over FP8 (E4M3, uint8) caches,
+    K = code * k_scale, V = code * v_scale."""
+    dev = _check_cuda(q, k_cache, v_cache, block_table, cu_q_lens, seq_lens, bias, out, lse,
+                      dev_status)
+    assert q.dtype == torch.bfloat16 and k_cache.dtype == v_cache.dtype == torch.uint8
+    assert block_table.dtype == cu_q_lens.dtype == seq_lens.dtype == torch.int32
+    out_dtype = OUT_BF16 if out.dtype == torch.bfloat16 else OUT_F32
+    T, hq = q.shape[0], q.shape[1]
+    B = cu_q_lens.shape[0] - 1
+    hkv = k_cache.shape[1]
+    with torch.cuda.device(dev):
+        need = _lib.workspace_size(B, hq, hkv, int(max_q_len), int(max_seq_len), int(window),
+                                   int(num_splits))
+        if workspace is None and need > 0:
+            workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+        ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+        _lib.call("inkling_rel_attn_decode_fp8", q, k_cache, v_cache, float(k_scale),
+                  float(v_scale), block_table, block_table.shape[1], cu_q_lens, seq_lens, bias,
+                  bias.shape[1], float(scale), int(window), out, out_dtype, lse, B, T, hq, hkv,
+                  k_cache.shape[0], int(max_q_len), int(max_seq_len), int(num_splits), workspace,
+                  ws_bytes, dev_status, _stream(stream))
 
 
 def decode_noalloc_capacity() -> int:

@@ -18,6 +18,7 @@ SZ = ctypes.c_size_t
 # name -> argument types, in the order of include/inkling.h
 SIGNATURES = {
     "inkling_sconv_kv": [P, P, P, P, P, P, P, P, P, I32, I32, I32, I64, I32, P, P],
+    "inkling_sconv_kv_fp8": [P, P, P, P, P, P, P, P, P, F32, F32, I32, I32, I32, I64, I32, P, P],
     "inkling_sconv": [P, P, P, P, P, I32, I32, I32, I32, P, P],
     "inkling_sconv_state_rollback": [P, P, P, P, P, P, I32, I32, I32, I32, P, P],
     "inkling_rel_attn_prefill": [P, P, P, P, I32, P, P, P, I32, F32, I32, P, I32, P, I32, I32,
@@ -25,6 +26,8 @@ SIGNATURES = {
     "inkling_rel_attn_decode_workspace_size": [I32, I32, I32, I32, I32, I32, I32],
     "inkling_rel_attn_decode": [P, P, P, P, I32, P, P, P, I32, F32, I32, P, I32, P, I32, I32,
                                 I32, I32, I64, I32, I32, I32, P, SZ, P, P],
+    "inkling_rel_attn_decode_fp8": [P, P, P, F32, F32, P, I32, P, P, P, I32, F32, I32, P, I32, P,
+                                    I32, I32, I32, I32, I64, I32, I32, I32, P, SZ, P, P],
     "inkling_rel_attn_decode_noalloc_capacity": [],
     "inkling_rel_attn_decode_noalloc": [P, P, P, P, I32, P, P, P, I32, F32, I32, P, I32, P, I32,
                                         I32, I32, I32, I64, I32, I32, I32, P, P],

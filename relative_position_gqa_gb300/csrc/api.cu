@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <cmath>
 #include <cstdint>
 #include <mutex>
 
@@ -34,12 +35,12 @@ bool get_encoder() {
 // 3-D bf16 tensor map, 128-byte swizzle, box inner extent 64 elements (128 bytes).
 bool make_map3(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
                uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t b0, uint32_t b1,
-               uint32_t b2) {
+               uint32_t b2, CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   cuuint64_t dims[3] = {d0, d1, d2};
   cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
   cuuint32_t box[3] = {b0, b1, b2};
   cuuint32_t es[3] = {1, 1, 1};
-  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+  return g_encode(m, dtype, 3, const_cast<void*>(base), dims, strides,
                   box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -80,6 +81,15 @@ int build_maps(const AttnArgs& a, AttnMaps* maps, bool need_q) {
                  128))
     return INKLING_ERR_INVALID_ARG;
   const uint64_t pages = (uint64_t)a.num_blocks * a.Hkv;
+  if (a.kv_fp8) {
+    // E4M3 pages: one 128-byte x 128-slot box per page-head
+    if (!make_map3(&maps->k, a.k_cache, 128, 128, pages, 128, 16384, 128, 128, 1,
+                   CU_TENSOR_MAP_DATA_TYPE_UINT8) ||
+        !make_map3(&maps->v, a.v_cache, 128, 128, pages, 128, 16384, 128, 128, 1,
+                   CU_TENSOR_MAP_DATA_TYPE_UINT8))
+      return INKLING_ERR_INVALID_ARG;
+    return INKLING_OK;
+  }
   if (!make_map3(&maps->k, a.k_cache, 128, 128, pages, 256, 32768, 64, 128, 1))
     return INKLING_ERR_INVALID_ARG;
   if (!make_map3(&maps->v, a.v_cache, 128, 128, pages, 256, 32768, 64, 128, 1))
@@ -123,6 +133,33 @@ int inkling_sconv_kv(const void* k_raw, const void* v_raw, const float* w_k, con
   if (B > 65535 || (max_q_len + 31) / 32 > 65535) return INKLING_ERR_UNSUPPORTED;
   ink::SconvArgs a{k_raw, v_raw, w_k, w_v, sconv_state, cu_q_lens, slot_mapping, k_cache,
                    v_cache, B, T, Hkv, (long long)num_blocks, max_q_len, dev_status};
+  return ink::launch_sconv_kv(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? INKLING_OK
+             : INKLING_ERR_CUDA;
+}
+
+int inkling_sconv_kv_fp8(const void* k_raw, const void* v_raw, const float* w_k,
+                         const float* w_v, void* sconv_state, const int32_t* cu_q_lens,
+                         const int64_t* slot_mapping, void* k_cache, void* v_cache,
+                         float k_scale, float v_scale, int32_t B, int32_t T, int32_t Hkv,
+                         int64_t num_blocks, int32_t max_q_len, int32_t* dev_status,
+                         inkling_stream_t stream) {
+  if (B < 0 || T < 0 || Hkv <= 0 || num_blocks <= 0 || max_q_len < 0) return INKLING_ERR_INVALID_ARG;
+  if (!(k_scale > 0.f) || !(v_scale > 0.f) || !std::isfinite(k_scale) || !std::isfinite(v_scale))
+    return INKLING_ERR_INVALID_ARG;
+  if (B == 0 || T == 0 || max_q_len == 0) return INKLING_OK;
+  if (!k_raw || !v_raw || !w_k || !w_v || !sconv_state || !cu_q_lens || !slot_mapping ||
+      !k_cache || !v_cache)
+    return INKLING_ERR_INVALID_ARG;
+  if (!aligned16(k_raw) || !aligned16(v_raw) || !aligned16(w_k) || !aligned16(w_v) ||
+      !aligned16(sconv_state) || !aligned16(k_cache) || !aligned16(v_cache))
+    return INKLING_ERR_INVALID_ARG;
+  if (B > 65535 || (max_q_len + 31) / 32 > 65535) return INKLING_ERR_UNSUPPORTED;
+  ink::SconvArgs a{k_raw, v_raw, w_k, w_v, sconv_state, cu_q_lens, slot_mapping, k_cache,
+                   v_cache, B, T, Hkv, (long long)num_blocks, max_q_len, dev_status};
+  a.fp8 = true;
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
   return ink::launch_sconv_kv(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
              ? INKLING_OK
              : INKLING_ERR_CUDA;
@@ -200,7 +237,8 @@ size_t inkling_rel_attn_decode_workspace_size(int32_t B, int32_t Hq, int32_t Hkv
   return ink::decode_workspace_bytes(B, Hq, Hkv, max_q_len, sp.num_splits);
 }
 
-int inkling_rel_attn_decode(const void* q, const void* k_cache, const void* v_cache,
+static int decode_entry(bool kv_fp8, float k_scale, float v_scale,
+                        const void* q, const void* k_cache, const void* v_cache,
                             const int32_t* block_table, int32_t max_blocks,
                             const int32_t* cu_q_lens, const int32_t* seq_lens,
                             const float* bias, int32_t R, float scale, int32_t window,
@@ -215,6 +253,10 @@ int inkling_rel_attn_decode(const void* q, const void* k_cache, const void* v_ca
   a.R = R; a.scale = scale; a.window = window; a.out = out; a.out_dtype = out_dtype; a.lse = lse;
   a.B = B; a.T = T; a.Hq = Hq; a.Hkv = Hkv; a.num_blocks = num_blocks; a.max_q_len = max_q_len;
   a.dev_status = dev_status; a.max_seq_len = max_seq_len;
+  a.kv_fp8 = kv_fp8; a.k_scale = k_scale; a.v_scale = v_scale;
+  if (kv_fp8 && (!(k_scale > 0.f) || !(v_scale > 0.f) || !std::isfinite(k_scale) ||
+                 !std::isfinite(v_scale)))
+    return INKLING_ERR_INVALID_ARG;
   const int rc = check_attn(a);
   if (rc != INKLING_OK) return rc;
   if (max_q_len > INKLING_MAX_DECODE_Q || max_seq_len < 0 || num_splits < 0)
@@ -239,6 +281,36 @@ int inkling_rel_attn_decode(const void* q, const void* k_cache, const void* v_ca
   return ink::launch_decode(a, maps, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
              ? INKLING_OK
              : INKLING_ERR_CUDA;
+}
+
+int inkling_rel_attn_decode(const void* q, const void* k_cache, const void* v_cache,
+                            const int32_t* block_table, int32_t max_blocks,
+                            const int32_t* cu_q_lens, const int32_t* seq_lens,
+                            const float* bias, int32_t R, float scale, int32_t window,
+                            void* out, int32_t out_dtype, float* lse, int32_t B, int32_t T,
+                            int32_t Hq, int32_t Hkv, int64_t num_blocks, int32_t max_q_len,
+                            int32_t max_seq_len, int32_t num_splits, void* workspace,
+                            size_t workspace_bytes, int32_t* dev_status,
+                            inkling_stream_t stream) {
+  return decode_entry(false, 1.f, 1.f, q, k_cache, v_cache, block_table, max_blocks, cu_q_lens,
+                      seq_lens, bias, R, scale, window, out, out_dtype, lse, B, T, Hq, Hkv,
+                      num_blocks, max_q_len, max_seq_len, num_splits, workspace,
+                      workspace_bytes, dev_status, stream);
+}
+
+int inkling_rel_attn_decode_fp8(const void* q, const void* k_cache, const void* v_cache,
+                                float k_scale, float v_scale, const int32_t* block_table,
+                                int32_t max_blocks, const int32_t* cu_q_lens,
+                                const int32_t* seq_lens, const float* bias, int32_t R,
+                                float scale, int32_t window, void* out, int32_t out_dtype,
+                                float* lse, int32_t B, int32_t T, int32_t Hq, int32_t Hkv,
+                                int64_t num_blocks, int32_t max_q_len, int32_t max_seq_len,
+                                int32_t num_splits, void* workspace, size_t workspace_bytes,
+                                int32_t* dev_status, inkling_stream_t stream) {
+  return decode_entry(true, k_scale, v_scale, q, k_cache, v_cache, block_table, max_blocks,
+                      cu_q_lens, seq_lens, bias, R, scale, window, out, out_dtype, lse, B, T,
+                      Hq, Hkv, num_blocks, max_q_len, max_seq_len, num_splits, workspace,
+                      workspace_bytes, dev_status, stream);
 }
 
 }  // extern "C"

@@ -33,12 +33,26 @@ namespace decode {
 
 constexpr int kStages = 3;
 constexpr int kThreads = 224;
+// FP8 cache: four warpgroups.  Warps 8-11 widen the E4M3 K pages and 12-15 the V pages
+// (32 rows each), warp 7 idles.  Widening a page with two warps took 0.8 us and, with one
+// f16 page per tensor, set the page period (a clock64 trace: widen V(j) -> PV(j) ->
+// widen V(j+1)); four halve it.  Register split (setmaxnreg) like the prefill: built for
+// 128 registers a thread at launch (65536 / 512), the softmax warpgroup grows to 256 and
+// the other three give back down to 80: 128*256 + 384*80 = 63488 <= 512*128.  The host
+// refuses the launch unless the built count is 128.
+constexpr int kThreadsF8 = 512;
+constexpr int kF8LaunchRegs = 128, kF8SoftmaxRegs = 256, kF8OtherRegs = 80;
+constexpr int kConvWarps = 4;  // per tensor
+static_assert(128 * kF8SoftmaxRegs + (kThreadsF8 - 128) * kF8OtherRegs <= kThreadsF8 * kF8LaunchRegs,
+              "register split exceeds the launch allocation");
 constexpr int kMaxG = 16;
 // floats per staged head (>= 127 + 9); 164 = 4 (mod 32), so the G heads x 4 tokens of a
 // warp (lane = t*G + g) hit distinct banks when they read column c
 constexpr int kBiasStride = 164;
 constexpr uint32_t kIdescQK = idesc_bf16(128, 128, false, false);
 constexpr uint32_t kIdescPV = idesc_bf16(128, 128, false, true);
+constexpr uint32_t kIdescQK16 = idesc_f16(128, 128, false, false);
+constexpr uint32_t kIdescPV16 = idesc_f16(128, 128, false, true);
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 5.545177444479562f;  // 8 ln 2: rescale O past 256x growth
@@ -48,8 +62,11 @@ struct __align__(1024) Smem {
   uint8_t k[kStages][2][16384];
   uint8_t v[kStages][2][16384];
   float bias[kStages][kMaxG * kBiasStride];  // raw table values, staged per page by the TMA warp
-  uint64_t k_full[kStages], v_full[kStages], kv_empty[kStages], b_full[kStages], b_empty[kStages];
+  // k_full / v_full: kStages bf16 stages or kStagesF8 (4) E4M3 stages
+  uint64_t k_full[4], v_full[4], kv_empty[kStages], b_full[kStages], b_empty[kStages];
   uint64_t q_ready, s_full[2], p_full[2], pv_done, o_full, drain;
+  // FP8 cache only: the converters' hand-offs (see convert_rows)
+  uint64_t k8_empty[4], v8_empty[4], kh_full[2], kh_empty[2], vh_full[2], vh_empty[2];
   uint32_t tmem_base;
   int abort_flag;
   int bad_block;
@@ -67,6 +84,7 @@ struct Params {
   float* part_ml;  // [B][Hkv][S][rmax][2]
   int* status;
   int max_blocks, R, window, out_dtype;
+  float v_scale;  // FP8 cache: V = code * v_scale, applied to O (1 for a bf16 cache)
   int B, T, Hq, Hkv, G, max_q_len, rmax, num_splits, pages_per_split;
   long long num_blocks;
   float scale;
@@ -86,7 +104,57 @@ __device__ __forceinline__ uint64_t desc_v(const uint8_t (*atoms)[16384], int ks
   return sdesc_sw128(smem_u32(atoms[0]) + ks * 2048, 16384, 1024);
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+// FP8 cache layout in shared memory, carved out of the bf16 K/V ring (192 KB = twelve
+// 16 KB slots): E4M3 pages as the TMA writes them (one 128-byte-swizzled box of 128 slots
+// x 128 bytes), three stages each for K (slots 0-2) and V (slots 3-5), and f16 pages for
+// K (s.v[0], s.v[1] when two) and V (s.v[2]) in the layout of the bf16 ring, which the
+// MMAs read.
+constexpr int kStagesF8 = 3;
+constexpr int kF16BufsK = 1, kF16BufsV = 1;
+static_assert(kStagesF8 <= 4 &&
+                  2 * kStagesF8 * 16384 + (kF16BufsK + kF16BufsV) * 32768 <= 2 * kStages * 32768,
+              "E4M3 stages and f16 pages must fit in the bf16 K/V ring");
+__device__ __forceinline__ uint8_t* f8_page(Smem& s, int which, int st) {
+  return &s.k[0][0][0] + (which * kStagesF8 + st) * 16384;
+}
+__device__ __forceinline__ uint8_t (*f16_page(Smem& s, int which, int buf))[16384] {
+  return which == 0 ? s.v[buf] : s.v[2];
+}
+
+// E4M3 page (16 KB, rows of 128 bytes, 16-byte chunk c of row r stored at chunk c ^ (r%8))
+// -> f16 page (two 64-wide d halves of 128-byte rows, same swizzle), exactly: every E4M3
+// value is an f16 value.  Rows r >= r0 (slots past the end of the sequence) become 0.
+// One warp converts 128 / kConvWarps rows from row_base: lane l takes rows row_base + l,
+// row_base + l + 32, ...
+__device__ __forceinline__ void convert_rows(const uint8_t* src, uint8_t (*dst)[16384], int r0,
+                                             int row_base, int lane) {
+#pragma unroll
+  for (int rr = 0; rr < 4 / kConvWarps; ++rr) {
+    const int r = row_base + lane + 32 * rr;
+    const int sw = r & 7;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      uint4 in = make_uint4(0, 0, 0, 0);
+      if (r < r0) in = *reinterpret_cast<const uint4*>(src + r * 128 + ((c ^ sw) << 4));
+      const uint32_t w[4] = {in.x, in.y, in.z, in.w};
+      uint32_t h[8];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        h[2 * j] = e4m3x2_to_f16x2((uint16_t)(w[j] & 0xffffu));
+        h[2 * j + 1] = e4m3x2_to_f16x2((uint16_t)(w[j] >> 16));
+      }
+      uint8_t* half = dst[c >> 2] + r * 128;
+      const int c0 = (c & 3) * 2;
+      *reinterpret_cast<uint4*>(half + ((c0 ^ sw) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
+      *reinterpret_cast<uint4*>(half + (((c0 + 1) ^ sw) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
+    }
+  }
+  fence_proxy_async_smem();
+  __syncwarp();
+}
+
+template <bool kFp8>
+__global__ void __launch_bounds__(kFp8 ? kThreadsF8 : kThreads, 1)
 decode_kernel(const __grid_constant__ CUtensorMap map_k,
               const __grid_constant__ CUtensorMap map_v, const Params p) {
   extern __shared__ uint8_t smem_raw[];
@@ -94,6 +162,8 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
                                      ~uintptr_t(1023));
   const int warp = warp_id(), lane = lane_id();
   const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  constexpr int NS = kFp8 ? kStagesF8 : kStages;  // K/V load stages
+  pdl_wait();
   const int t_seq0 = p.cu_q_lens[b];
   const int n = p.cu_q_lens[b + 1] - t_seq0;
   if (n == 0) return;
@@ -124,7 +194,7 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
     s.bad_block = 0;
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < np; i += kThreads) {
+  for (int i = threadIdx.x; i < np; i += (kFp8 ? kThreadsF8 : kThreads)) {
     const int32_t blk = table[pg0 + i];
     if (blk < 0 || (long long)blk >= p.num_blocks) s.bad_block = 1;
   }
@@ -149,6 +219,22 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
     mbar_init(&s.pv_done, 1);
     mbar_init(&s.o_full, 1);
     mbar_init(&s.drain, 1);
+    if (kFp8) {
+      for (int i = 0; i < kStagesF8; ++i) {
+        if (i >= kStages) {  // the stages past the bf16 ring's
+          mbar_init(&s.k_full[i], 1);
+          mbar_init(&s.v_full[i], 1);
+        }
+        mbar_init(&s.k8_empty[i], kConvWarps);
+        mbar_init(&s.v8_empty[i], kConvWarps);
+      }
+      for (int i = 0; i < 2; ++i) {
+        mbar_init(&s.kh_full[i], kConvWarps);
+        mbar_init(&s.kh_empty[i], 1);
+        mbar_init(&s.vh_full[i], kConvWarps);
+        mbar_init(&s.vh_empty[i], 1);
+      }
+    }
     fence_barrier_init();
   }
   if (warp == 5) {
@@ -161,7 +247,9 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
   const uint32_t tmem = s.tmem_base;
   volatile int* abort_flag = &s.abort_flag;
 
-  if (warp == 4) {
+  if (warp >= 4) {
+   if constexpr (kFp8) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kF8OtherRegs));
+   if (warp == 4) {
     // ------------------------------------------------------------ TMA producer ---
     // Lane 0 issues the K/V page loads, up to kStages pages ahead of the softmax.
     const uint64_t pol = l2_policy_evict_first();
@@ -170,14 +258,37 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
       tma_prefetch_desc(&map_v);
       int issued = 0;
       for (int i = 0; i < np; ++i) {
-        const int st = i % kStages;
+        const int st = i % NS;
+        const int page = table[pg0 + i] * p.Hkv + kvh;
+        if (kFp8) {
+          // one 16 KB E4M3 box per K and V page; a stage is free once converted
+          const uint32_t eph = ((i / NS) - 1) & 1;
+          if (i >= NS && !mbar_wait(&s.k8_empty[st], eph, abort_flag, p.status)) {
+            report(p.status, kErrTimeout);
+            s.abort_flag = 1;
+            break;
+          }
+          mbar_arrive_expect_tx(&s.k_full[st], 16384u);
+          tma_load_3d_hint(f8_page(s, 0, st), &map_k, &s.k_full[st], 0, 0, page, pol);
+          if (i >= NS && !mbar_wait(&s.v8_empty[st], eph, abort_flag, p.status)) {
+            report(p.status, kErrTimeout);
+            s.abort_flag = 1;
+            issued = i;  // this page's K is in flight too: let it land
+            volatile int never = 0;
+            mbar_wait(&s.k_full[st], (i / NS) & 1, &never);
+            break;
+          }
+          mbar_arrive_expect_tx(&s.v_full[st], 16384u);
+          tma_load_3d_hint(f8_page(s, 1, st), &map_v, &s.v_full[st], 0, 0, page, pol);
+          issued = i + 1;
+          continue;
+        }
         if (i >= kStages &&
             !mbar_wait(&s.kv_empty[st], ((i / kStages) - 1) & 1, abort_flag, p.status)) {
           report(p.status, kErrTimeout);
           s.abort_flag = 1;
           break;
         }
-        const int page = table[pg0 + i] * p.Hkv + kvh;
         mbar_arrive_expect_tx(&s.k_full[st], 32768u);
         tma_load_3d_hint(s.k[st][0], &map_k, &s.k_full[st], 0, 0, page, pol);
         tma_load_3d_hint(s.k[st][1], &map_k, &s.k_full[st], 64, 0, page, pol);
@@ -188,14 +299,42 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
       }
       if (*abort_flag) {
         // let the copies already in flight land before the CTA goes away
-        for (int i = max(0, issued - kStages); i < issued; ++i) {
-          const int st = i % kStages;
-          const uint32_t ph = (i / kStages) & 1;
+        for (int i = max(0, issued - NS); i < issued; ++i) {
+          const int st = i % NS;
+          const uint32_t ph = (i / NS) & 1;
           volatile int never = 0;
           mbar_wait(&s.k_full[st], ph, &never);
           mbar_wait(&s.v_full[st], ph, &never);
         }
       }
+    }
+  } else if (kFp8 && warp >= 8) {
+    // ------------------------------------------------------------ FP8 converters ---
+    // Warps 8-11 widen K pages, 12-15 V pages, 32 rows each: page j's K goes to its f16
+    // page once QK has read the page's previous occupant, its V once PV has.
+    const int which = (warp - 8) / kConvWarps, row_base = ((warp - 8) % kConvWarps) * (128 / kConvWarps);
+    const int r_end = L - pg0 * 128;  // rows of page j at or past r_end - 128 j are empty
+    uint64_t* full8 = which == 0 ? s.k_full : s.v_full;
+    uint64_t* empty8 = which == 0 ? s.k8_empty : s.v8_empty;
+    uint64_t* full_h = which == 0 ? s.kh_full : s.vh_full;
+    uint64_t* empty_h = which == 0 ? s.kh_empty : s.vh_empty;
+    bool ok = true;
+    for (int j = 0; ok && j < np; ++j) {
+      const int nb = which == 0 ? kF16BufsK : kF16BufsV;
+      const int st = j % NS, hb = j % nb;
+      ok = mbar_wait(&full8[st], (j / NS) & 1, abort_flag, p.status) &&
+           (j < nb || mbar_wait(&empty_h[hb], ((j / nb) - 1) & 1, abort_flag, p.status));
+      if (!ok) break;
+      convert_rows(f8_page(s, which, st), f16_page(s, which, hb), min(128, r_end - 128 * j),
+                   row_base, lane);
+      if (lane == 0) {
+        mbar_arrive(&full_h[hb]);
+        mbar_arrive(&empty8[st]);
+      }
+    }
+    if (!ok) {
+      report(p.status, kErrTimeout);
+      s.abort_flag = 1;
     }
   } else if (warp == 6) {
     // ------------------------------------------------------------ bias stager ---
@@ -236,15 +375,22 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
     asm volatile("cp.async.wait_all;" ::: "memory");
   } else if (warp == 5) {
     // ------------------------------------------------------------- MMA issuer ---
-    bool ok = mbar_wait(&s.q_ready, 0, abort_flag, p.status) && mbar_wait(&s.k_full[0], 0, abort_flag, p.status);
+    // FP8: K and V come from the converters' f16 pages (f16_page), f16 MMAs
+    constexpr uint32_t idQK = kFp8 ? kIdescQK16 : kIdescQK;
+    constexpr uint32_t idPV = kFp8 ? kIdescPV16 : kIdescPV;
+    bool ok = mbar_wait(&s.q_ready, 0, abort_flag, p.status) &&
+              (kFp8 ? mbar_wait(&s.kh_full[0], 0, abort_flag, p.status)
+                    : mbar_wait(&s.k_full[0], 0, abort_flag, p.status));
     bool issued_any = false;
     if (ok) {
       tc_fence_after();
       if (lane == 0) {
+        const uint8_t (*kp)[16384] = kFp8 ? f16_page(s, 0, 0) : s.k[0];
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
-          umma_ts(tmem + kColS0, tmem + kColQ + ks * 8, desc_k(s.k[0], ks), kIdescQK, ks > 0);
+          umma_ts(tmem + kColS0, tmem + kColQ + ks * 8, desc_k(kp, ks), idQK, ks > 0);
         umma_commit(&s.s_full[0]);
+        if (kFp8) umma_commit(&s.kh_empty[0]);
       }
       issued_any = true;
       __syncwarp();
@@ -253,23 +399,28 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
       const int st = i % kStages;
       if (i + 1 < np) {
         const int st1 = (i + 1) % kStages;
-        ok = mbar_wait(&s.k_full[st1], ((i + 1) / kStages) & 1, abort_flag, p.status);
+        ok = kFp8 ? mbar_wait(&s.kh_full[(i + 1) % kF16BufsK], ((i + 1) / kF16BufsK) & 1, abort_flag,
+                              p.status)
+                  : mbar_wait(&s.k_full[st1], ((i + 1) / kStages) & 1, abort_flag, p.status);
         if (!ok) break;
         tc_fence_after();
         if (lane == 0) {
           const uint32_t dS = tmem + kColS0 + ((i + 1) & 1) * 128;
+          const uint8_t (*kp)[16384] = kFp8 ? f16_page(s, 0, (i + 1) % kF16BufsK) : s.k[st1];
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
-            umma_ts(dS, tmem + kColQ + ks * 8, desc_k(s.k[st1], ks), kIdescQK, ks > 0);
+            umma_ts(dS, tmem + kColQ + ks * 8, desc_k(kp, ks), idQK, ks > 0);
           umma_commit(&s.s_full[(i + 1) & 1]);
+          if (kFp8) umma_commit(&s.kh_empty[(i + 1) % kF16BufsK]);
         }
         __syncwarp();
       }
       ok = mbar_wait(&s.p_full[i & 1], (i >> 1) & 1, abort_flag, p.status) &&
-           mbar_wait(&s.v_full[st], (i / kStages) & 1, abort_flag, p.status);
+           (kFp8 ? mbar_wait(&s.vh_full[0], i & 1, abort_flag, p.status)
+                 : mbar_wait(&s.v_full[st], (i / kStages) & 1, abort_flag, p.status));
       if (!ok) break;
       const int kt = pg0 + i;
-      if ((kt + 1) * 128 > L) {
+      if (!kFp8 && (kt + 1) * 128 > L) {  // (the converter zeroes the f16 page's tail)
         // slots past the end of the sequence: P is 0 there but the stale V could be NaN
         const int r0 = L - kt * 128;
         const int chunks = (128 - r0) * 8;
@@ -284,10 +435,11 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
       tc_fence_after();
       if (lane == 0) {
         const uint32_t aP = tmem + kColS0 + (i & 1) * 128;
+        const uint8_t (*vp)[16384] = kFp8 ? f16_page(s, 1, 0) : s.v[st];
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
-          umma_ts(tmem + kColO, aP + ks * 8, desc_v(s.v[st], ks), kIdescPV, (i > 0 || ks > 0));
-        umma_commit(&s.kv_empty[st]);
+          umma_ts(tmem + kColO, aP + ks * 8, desc_v(vp, ks), idPV, (i > 0 || ks > 0));
+        umma_commit(kFp8 ? &s.vh_empty[0] : &s.kv_empty[st]);
         umma_commit(&s.pv_done);
       }
       __syncwarp();
@@ -305,7 +457,10 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
       }
     }
     __syncwarp();
-  } else if (warp * 32 < rows) {
+   }
+  } else {
+   if constexpr (kFp8) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kF8SoftmaxRegs));
+   if (warp * 32 < rows) {
     // ------------------------------------------------------------ softmax group ---
     const int r = threadIdx.x;  // 0..nact-1
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
@@ -327,6 +482,11 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
       } else {
 #pragma unroll
         for (int j = 0; j < 64; ++j) qr[j] = 0u;
+      }
+      if (kFp8) {  // the f16 MMAs take Q as f16 (exact for |q| < 65504)
+#pragma unroll
+        for (int j = 0; j < 64; ++j)
+          qr[j] = pack_f16(__uint_as_float(qr[j] << 16), __uint_as_float(qr[j] & 0xffff0000u));
       }
       tmem_st32(tmem + lane_base + kColQ, qr);
       tmem_st32(tmem + lane_base + kColQ + 32, qr + 32);
@@ -423,7 +583,7 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
         const float2 d2 = __ffma2_rn(x[k], lg2, nm2);
         const float2 e2 = make_float2(ex2(d2.x), ex2(d2.y));
         l2 = __fadd2_rn(l2, e2);
-        sr[k] = pack_bf16(e2.x, e2.y);
+        sr[k] = kFp8 ? pack_f16(e2.x, e2.y) : pack_bf16(e2.x, e2.y);
       }
       // rescale O (warp-wide, only when some row's max grew past the threshold)
       if (__any_sync(0xffffffffu, need) && i > 0) {
@@ -458,7 +618,8 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
       tc_fence_after();
       const uint32_t tO = tmem + lane_base + kColO;
       const bool direct = nsplit_b == 1;
-      const float inv_l = direct ? 1.f / l : 1.f;
+      // V = code * v_scale for an FP8 cache: scaled here, partials included
+      const float inv_l = direct ? p.v_scale / l : p.v_scale;
       const size_t prow = (((size_t)b * p.Hkv + kvh) * p.num_splits + split) * p.rmax + r;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
@@ -471,8 +632,8 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
           float4* dst = reinterpret_cast<float4*>(p.part_o + prow * 128 + c * 32);
 #pragma unroll
           for (int j = 0; j < 8; ++j)
-            dst[j] = make_float4(__uint_as_float(orr[4 * j]), __uint_as_float(orr[4 * j + 1]),
-                                 __uint_as_float(orr[4 * j + 2]), __uint_as_float(orr[4 * j + 3]));
+            dst[j] = make_float4(__uint_as_float(orr[4 * j]) * inv_l, __uint_as_float(orr[4 * j + 1]) * inv_l,
+                                 __uint_as_float(orr[4 * j + 2]) * inv_l, __uint_as_float(orr[4 * j + 3]) * inv_l);
         } else {
           const size_t obase = ((size_t)(t_seq0 + t) * p.Hq + h) * 128 + c * 32;
           if (p.out_dtype == 0) {
@@ -504,6 +665,7 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
         }
       }
     }
+   }
   }
 
   tc_fence_before();
@@ -526,6 +688,7 @@ combine_kernel(const Params p) {
   const int kvh = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = blockIdx.x * kCombineWarps + warp;
+  pdl_wait();
   const int t_seq0 = p.cu_q_lens[b];
   const int n = p.cu_q_lens[b + 1] - t_seq0;
   if (n <= 0 || n > p.max_q_len || r >= n * p.G) return;
@@ -651,7 +814,8 @@ cudaError_t launch_decode(const AttnArgs& a, const AttnMaps& maps, cudaStream_t 
   p.num_splits = a.num_splits;
   p.pages_per_split = a.pages_per_split;
   p.num_blocks = a.num_blocks;
-  p.scale = a.scale;
+  p.scale = a.kv_fp8 ? a.scale * a.k_scale : a.scale;  // K = code * k_scale
+  p.v_scale = a.kv_fp8 ? a.v_scale : 1.f;
   p.part_o = nullptr;
   p.part_ml = nullptr;
   if (a.num_splits > 1) {
@@ -662,16 +826,23 @@ cudaError_t launch_decode(const AttnArgs& a, const AttnMaps& maps, cudaStream_t 
   }
   if (a.B == 0) return cudaSuccess;
   const size_t smem = sizeof(Smem) + 1024;
-  cudaError_t e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
+  cudaError_t e = cudaFuncSetAttribute(a.kv_fp8 ? decode_kernel<true> : decode_kernel<false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid(a.num_splits, a.Hkv, a.B);
-  decode_kernel<<<grid, kThreads, smem, stream>>>(maps.k, maps.v, p);
-  e = cudaGetLastError();
+  if (a.kv_fp8) {
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, decode_kernel<true>);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs != kF8LaunchRegs) return cudaErrorInvalidConfiguration;  // see kF8LaunchRegs
+  }
+  e = a.kv_fp8 ? launch_pdl(decode_kernel<true>, grid, dim3(kThreadsF8), smem, stream, maps.k,
+                            maps.v, p)
+               : launch_pdl(decode_kernel<false>, grid, dim3(kThreads), smem, stream, maps.k,
+                            maps.v, p);
   if (e != cudaSuccess || a.num_splits <= 1) return e;
-  combine_kernel<<<dim3((p.rmax + kCombineWarps - 1) / kCombineWarps, a.Hkv, a.B),
-                   kCombineWarps * 32, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel, dim3((p.rmax + kCombineWarps - 1) / kCombineWarps, a.Hkv, a.B),
+                    dim3(kCombineWarps * 32), 0, stream, p);
 }
 
 }  // namespace ink

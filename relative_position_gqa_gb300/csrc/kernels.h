@@ -6,8 +6,28 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <utility>
 
 namespace ink {
+
+// Launch with programmatic stream serialization allowed: the kernel may begin while the
+// previous kernel on the stream drains, and every kernel of the library starts with
+// pdl_wait() before it touches global inputs.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 struct SconvArgs {
   const void* k_raw;
@@ -23,6 +43,8 @@ struct SconvArgs {
   long long num_blocks;
   int max_q_len;
   int* dev_status;
+  bool fp8 = false;  // caches hold E4M3 bytes: code = e4m3(y / scale)
+  float k_scale = 1.f, v_scale = 1.f;
 };
 
 struct SconvDenseArgs {
@@ -71,6 +93,9 @@ struct AttnArgs {
   int pages_per_split;
   void* workspace;
   size_t workspace_bytes;
+  // FP8 (E4M3) cache: K = code * k_scale, V = code * v_scale (decode only)
+  bool kv_fp8 = false;
+  float k_scale = 1.f, v_scale = 1.f;
 };
 
 // Tensor maps built by the host for the attention kernels.

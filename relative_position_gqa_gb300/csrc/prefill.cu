@@ -121,6 +121,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_q,
   Smem& s = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                      ~uintptr_t(1023));
   const int warp = warp_id(), lane = lane_id();
+  pdl_wait();
 
   // ---- work item: heavy (late) query tiles first, head pairs fastest ----
   const int idx = blockIdx.x;
@@ -586,8 +587,8 @@ cudaError_t launch_prefill(const AttnArgs& a, const AttnMaps& maps, cudaStream_t
   e = cudaFuncGetAttributes(&fa, prefill_kernel);
   if (e != cudaSuccess) return e;
   if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;  // see kLaunchRegs
-  prefill_kernel<<<(unsigned)grid, kThreads, smem, stream>>>(maps.q, maps.k, maps.v, p);
-  return cudaGetLastError();
+  return launch_pdl(prefill_kernel, dim3((unsigned)grid), dim3(kThreads), smem, stream, maps.q,
+                    maps.k, maps.v, p);
 }
 
 }  // namespace ink

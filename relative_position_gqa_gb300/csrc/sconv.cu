@@ -59,11 +59,14 @@ struct SconvDev {
   const int64_t* slot_mapping;
   int T, C, streams, Hkv, max_q_len;
   long long num_slots;
+  float inv_scale[2];  // FP8 cache: code = e4m3(y * inv_scale), per stream
   int* status;
 };
 
-template <bool kPaged>
+template <bool kPaged, bool kFp8 = false>
 __global__ void __launch_bounds__(kSconvThreads) sconv_kernel(const SconvDev p) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int C = p.C;
   const int vecs_per_stream = C / kVec;
   const int vec = blockIdx.x * kSconvThreads + threadIdx.x;
@@ -87,6 +90,7 @@ __global__ void __launch_bounds__(kSconvThreads) sconv_kernel(const SconvDev p) 
   const uint16_t* x = which == 0 ? p.x[0] : p.x[1];
   const float* w = which == 0 ? p.w[0] : p.w[1];
   uint16_t* out = which == 0 ? p.out[0] : p.out[1];
+  const float inv_scale = which == 0 ? p.inv_scale[0] : p.inv_scale[1];
   uint16_t* st = p.state + ((size_t)b * p.streams + which) * 3 * C + c0;
 
   float tap[kVec][4];
@@ -121,6 +125,22 @@ __global__ void __launch_bounds__(kSconvThreads) sconv_kernel(const SconvDev p) 
       a = fmaf(tap[i][2], h2.v[i], a);
       a = fmaf(tap[i][3], cur.v[i], a);
       y[i] = a;
+    }
+    if (kFp8) {
+      // FP8 cache (one byte per channel): e4m3(y / scale), scale folded into inv_scale
+      const long long slot = p.slot_mapping[tg];
+      if (slot >= p.num_slots) {
+        report(p.status, kErrBadBlock);
+      } else if (slot >= 0) {
+        const long long blk = slot >> 7, off = slot & 127;
+        uint2 o8;
+        o8.x = pack_e4m3x4(y[0] * inv_scale, y[1] * inv_scale, y[2] * inv_scale, y[3] * inv_scale);
+        o8.y = pack_e4m3x4(y[4] * inv_scale, y[5] * inv_scale, y[6] * inv_scale, y[7] * inv_scale);
+        *reinterpret_cast<uint2*>(reinterpret_cast<uint8_t*>(out) +
+                                  (((size_t)blk * p.Hkv + head) * 128 + off) * 128 + d0) = o8;
+      }
+      h0 = h1; h1 = h2; h2 = cur;
+      return;
     }
     uint4 o;
     o.x = pack_bf16(y[0], y[1]);
@@ -180,6 +200,8 @@ sconv_rollback_kernel(const uint16_t* state_before, const uint16_t* __restrict__
                       const uint16_t* __restrict__ x1, const int32_t* __restrict__ cu_q_lens,
                       const int32_t* __restrict__ accepted, uint16_t* state_after, int T,
                       int C, int streams, int* __restrict__ status) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int vecs_per_stream = C / kVec;
   const int vec = blockIdx.x * kSconvThreads + threadIdx.x;
   if (vec >= streams * vecs_per_stream) return;
@@ -231,8 +253,12 @@ cudaError_t launch_sconv_kv(const SconvArgs& a, cudaStream_t stream) {
   p.status = a.dev_status;
   const dim3 grid = sconv_grid(2, p.C, a.max_q_len, a.B, SconvShape<true>::kChunk);
   if (grid.y == 0 || grid.z == 0) return cudaSuccess;
-  sconv_kernel<true><<<grid, kSconvThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+  if (a.fp8) {
+    p.inv_scale[0] = (float)(1.0 / (double)a.k_scale);
+    p.inv_scale[1] = (float)(1.0 / (double)a.v_scale);
+    return launch_pdl(sconv_kernel<true, true>, grid, dim3(kSconvThreads), 0, stream, p);
+  }
+  return launch_pdl(sconv_kernel<true>, grid, dim3(kSconvThreads), 0, stream, p);
 }
 
 cudaError_t launch_sconv_dense(const SconvDenseArgs& a, cudaStream_t stream) {
@@ -249,19 +275,18 @@ cudaError_t launch_sconv_dense(const SconvDenseArgs& a, cudaStream_t stream) {
   p.status = a.dev_status;
   const dim3 grid = sconv_grid(1, a.C, a.max_q_len, a.B, SconvShape<false>::kChunk);
   if (grid.y == 0 || grid.z == 0) return cudaSuccess;
-  sconv_kernel<false><<<grid, kSconvThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(sconv_kernel<false>, grid, dim3(kSconvThreads), 0, stream, p);
 }
 
 cudaError_t launch_sconv_rollback(const SconvRollbackArgs& a, cudaStream_t stream) {
   const int total_vecs = a.streams * a.C / kVec;
   const dim3 grid((total_vecs + kSconvThreads - 1) / kSconvThreads, a.B);
   if (grid.y == 0) return cudaSuccess;
-  sconv_rollback_kernel<<<grid, kSconvThreads, 0, stream>>>(
-      static_cast<const uint16_t*>(a.state_before), static_cast<const uint16_t*>(a.x0),
-      static_cast<const uint16_t*>(a.x1 ? a.x1 : a.x0), a.cu_q_lens, a.accepted,
-      static_cast<uint16_t*>(a.state_after), a.T, a.C, a.streams, a.dev_status);
-  return cudaGetLastError();
+  return launch_pdl(sconv_rollback_kernel, grid, dim3(kSconvThreads), 0, stream,
+                    static_cast<const uint16_t*>(a.state_before),
+                    static_cast<const uint16_t*>(a.x0),
+                    static_cast<const uint16_t*>(a.x1 ? a.x1 : a.x0), a.cu_q_lens, a.accepted,
+                    static_cast<uint16_t*>(a.state_after), a.T, a.C, a.streams, a.dev_status);
 }
 
 }  // namespace ink

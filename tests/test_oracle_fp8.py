@@ -1,6 +1,6 @@
 """Pins for the oracle's FP8 KV cache: the E4M3 codec, the conv written as E4M3 codes, and
-attention over an E4M3 cache (vLLM Day-0 Inkling blog, "Roadmap": FP8 attention and KV
-cache for the full-attention layers).  CPU only."""
+attention over an E4M3 cache (vLLM Day-0 Inkling blog, "Roadmap": FP8 for the global-attention
+layers).  CPU only."""
 import math
 import os
 

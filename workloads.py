@@ -250,3 +250,10 @@ def make_dense(q_lens, C: int, seed: int, device="cpu", w_std: float = 0.5,
     cu[1:] = torch.cumsum(torch.tensor(list(q_lens), dtype=torch.int64), 0).to(torch.int32)
     return DenseCase(x.to(device), w.float().contiguous().to(device),
                      st.to(torch.bfloat16).contiguous().to(device), cu.to(device))
+
+
+def fp8_history(cache: torch.Tensor, scale: float) -> torch.Tensor:
+    """Seeded FP8 cache contents for tests and benches: the bf16 history pages quantized
+    to E4M3 codes of cache / scale with torch's own float8_e4m3fn conversion (input
+    generation only: the kernels and the oracle both consume the codes as given)."""
+    return (cache.float() / scale).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8)
