@@ -32,18 +32,26 @@ namespace ink {
 namespace decode {
 
 constexpr int kStages = 3;
-constexpr int kThreads = 224;
-// FP8 cache: four warpgroups.  Warps 8-11 widen the E4M3 K pages and 12-15 the V pages
-// (32 rows each), warp 7 idles.  Widening a page with two warps took 0.8 us and, with one
-// f16 page per tensor, set the page period (a clock64 trace: widen V(j) -> PV(j) ->
-// widen V(j+1)); four halve it.  Register split (setmaxnreg) like the prefill: built for
-// 128 registers a thread at launch (65536 / 512), the softmax warpgroup grows to 256 and
-// the other three give back down to 80: 128*256 + 384*80 = 63488 <= 512*128.  The host
-// refuses the launch unless the built count is 128.
-constexpr int kThreadsF8 = 512;
-constexpr int kF8LaunchRegs = 128, kF8SoftmaxRegs = 256, kF8OtherRegs = 80;
+// Warps 0-7 softmax (the pair w, w+4 shares TMEM lanes 32(w%4).. and splits the 128
+// columns of those rows), 8 TMA producer, 9 MMA issuer, 10 bias stager, 11 idle.
+// Register split (setmaxnreg): built for 168 registers a thread at launch (65536 / 384),
+// the two softmax warpgroups grow to 216 and the third gives back down to 64:
+// 256*216 + 128*64 = 63488 <= 384*168.  The host refuses the launch unless the built
+// count is 168.
+constexpr int kThreads = 384;
+constexpr int kLaunchRegs = 168, kSoftmaxRegs = 216, kOtherRegs = 64;
+static_assert(256 * kSoftmaxRegs + 128 * kOtherRegs <= kThreads * kLaunchRegs,
+              "register split exceeds the launch allocation");
+constexpr int kWarpTma = 8, kWarpMma = 9, kWarpBias = 10, kWarpConv = 12;
+// FP8 cache: two more warpgroups, warps 12-15 widen the E4M3 K pages and 16-19 the V
+// pages (32 rows each).  Widening a page with two warps took 0.8 us and, with one f16
+// page per tensor, set the page period (a clock64 trace: widen V(j) -> PV(j) -> widen
+// V(j+1)); four halve it.  Built for 96 registers a thread at launch (65536 / 640,
+// rounded down to 8): softmax 152, the rest 56: 256*152 + 384*56 = 60416 <= 640*96.
+constexpr int kThreadsF8 = 640;
+constexpr int kF8LaunchRegs = 96, kF8SoftmaxRegs = 152, kF8OtherRegs = 56;
 constexpr int kConvWarps = 4;  // per tensor
-static_assert(128 * kF8SoftmaxRegs + (kThreadsF8 - 128) * kF8OtherRegs <= kThreadsF8 * kF8LaunchRegs,
+static_assert(256 * kF8SoftmaxRegs + (kThreadsF8 - 256) * kF8OtherRegs <= kThreadsF8 * kF8LaunchRegs,
               "register split exceeds the launch allocation");
 constexpr int kMaxG = 16;
 // floats per staged head (>= 127 + 9); 164 = 4 (mod 32), so the G heads x 4 tokens of a
@@ -65,12 +73,19 @@ struct __align__(1024) Smem {
   // k_full / v_full: kStages bf16 stages or kStagesF8 (4) E4M3 stages
   uint64_t k_full[4], v_full[4], kv_empty[kStages], b_full[kStages], b_empty[kStages];
   uint64_t q_ready, s_full[2], p_full[2], pv_done, o_full, drain;
+  // the two column halves of a row trade partial maxima (per page parity), and at the
+  // end their sums (in the slot of the parity after the last page's)
+  uint64_t x_full[2], l_full;
+  float xm[2][2][128];
   // FP8 cache only: the converters' hand-offs (see convert_rows)
   uint64_t k8_empty[4], v8_empty[4], kh_full[2], kh_empty[2], vh_full[2], vh_empty[2];
   uint32_t tmem_base;
   int abort_flag;
   int bad_block;
 };
+
+// 227 KB per CTA, with 1 KB of slack to align the dynamic buffer to 1024 bytes
+static_assert(sizeof(Smem) + 1024 <= 232448, "decode shared memory exceeds 227 KB");
 
 struct Params {
   const uint16_t* q;
@@ -209,13 +224,16 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
       mbar_init(&s.v_full[i], 1);
       mbar_init(&s.kv_empty[i], 1);
       mbar_init(&s.b_full[i], 32);
-      mbar_init(&s.b_empty[i], nact);
+      mbar_init(&s.b_empty[i], 2 * nact);
     }
-    mbar_init(&s.q_ready, nact);
+    mbar_init(&s.q_ready, 2 * nact);
+    mbar_init(&s.x_full[0], 2 * nact);
+    mbar_init(&s.x_full[1], 2 * nact);
+    mbar_init(&s.l_full, 2 * nact);
     mbar_init(&s.s_full[0], 1);
     mbar_init(&s.s_full[1], 1);
-    mbar_init(&s.p_full[0], nact);
-    mbar_init(&s.p_full[1], nact);
+    mbar_init(&s.p_full[0], 2 * nact);
+    mbar_init(&s.p_full[1], 2 * nact);
     mbar_init(&s.pv_done, 1);
     mbar_init(&s.o_full, 1);
     mbar_init(&s.drain, 1);
@@ -237,7 +255,7 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
     }
     fence_barrier_init();
   }
-  if (warp == 5) {
+  if (warp == kWarpMma) {
     tmem_alloc(&s.tmem_base, 512);
     tmem_relinquish();
   }
@@ -247,9 +265,9 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
   const uint32_t tmem = s.tmem_base;
   volatile int* abort_flag = &s.abort_flag;
 
-  if (warp >= 4) {
-   if constexpr (kFp8) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kF8OtherRegs));
-   if (warp == 4) {
+  if (warp >= 8) {
+   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kFp8 ? kF8OtherRegs : kOtherRegs));
+   if (warp == kWarpTma) {
     // ------------------------------------------------------------ TMA producer ---
     // Lane 0 issues the K/V page loads, up to kStages pages ahead of the softmax.
     const uint64_t pol = l2_policy_evict_first();
@@ -308,11 +326,12 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
         }
       }
     }
-  } else if (kFp8 && warp >= 8) {
+  } else if (kFp8 && warp >= kWarpConv) {
     // ------------------------------------------------------------ FP8 converters ---
-    // Warps 8-11 widen K pages, 12-15 V pages, 32 rows each: page j's K goes to its f16
+    // Warps 12-15 widen K pages, 16-19 V pages, 32 rows each: page j's K goes to its f16
     // page once QK has read the page's previous occupant, its V once PV has.
-    const int which = (warp - 8) / kConvWarps, row_base = ((warp - 8) % kConvWarps) * (128 / kConvWarps);
+    const int which = (warp - kWarpConv) / kConvWarps;
+    const int row_base = ((warp - kWarpConv) % kConvWarps) * (128 / kConvWarps);
     const int r_end = L - pg0 * 128;  // rows of page j at or past r_end - 128 j are empty
     uint64_t* full8 = which == 0 ? s.k_full : s.v_full;
     uint64_t* empty8 = which == 0 ? s.k8_empty : s.v8_empty;
@@ -336,7 +355,7 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
       report(p.status, kErrTimeout);
       s.abort_flag = 1;
     }
-  } else if (warp == 6) {
+  } else if (warp == kWarpBias) {
     // ------------------------------------------------------------ bias stager ---
     // All 32 lanes stage the page's bias slices with 4-byte cp.async copies (no register
     // round trip) and arrive on b_full[slot] when their copies land.  A slot is reused
@@ -373,7 +392,7 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
     }
     // let outstanding copies land before the CTA can exit
     asm volatile("cp.async.wait_all;" ::: "memory");
-  } else if (warp == 5) {
+  } else if (warp == kWarpMma) {
     // ------------------------------------------------------------- MMA issuer ---
     // FP8: K and V come from the converters' f16 pages (f16_page), f16 MMAs
     constexpr uint32_t idQK = kFp8 ? kIdescQK16 : kIdescQK;
@@ -459,37 +478,42 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
     __syncwarp();
    }
   } else {
-   if constexpr (kFp8) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kF8SoftmaxRegs));
-   if (warp * 32 < rows) {
+   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kFp8 ? kF8SoftmaxRegs : kSoftmaxRegs));
+   if ((warp & 3) * 32 < rows) {
     // ------------------------------------------------------------ softmax group ---
-    const int r = threadIdx.x;  // 0..nact-1
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    // Thread (r, hf): packed row r = TMEM lane, columns 64 hf .. 64 hf + 63 of S, P, O.
+    // The two halves of a row trade their partial maxima through shared memory (an
+    // mbarrier per page parity), so both use the same running max; each keeps its own
+    // partial sum, and the sums meet once at the end.
+    const int r = (warp & 3) * 32 + lane;
+    const int hf = warp >> 2, c0 = hf * 64;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const bool valid = r < rows;
     const int t = valid ? r / p.G : 0;
     const int g = valid ? r % p.G : 0;
     const int h = kvh * p.G + g;
 
-    // packed Q rows into TMEM columns [0, 64)
+    // packed Q rows into TMEM columns [0, 64): this thread's half of the d range
     {
-      uint32_t qr[64];
+      uint32_t qr[32];
       if (valid) {
-        const uint4* src = reinterpret_cast<const uint4*>(p.q + ((size_t)(t_seq0 + t) * p.Hq + h) * 128);
+        const uint4* src =
+            reinterpret_cast<const uint4*>(p.q + ((size_t)(t_seq0 + t) * p.Hq + h) * 128 + c0);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
+        for (int j = 0; j < 8; ++j) {
           const uint4 w = __ldg(src + j);
           qr[4 * j] = w.x; qr[4 * j + 1] = w.y; qr[4 * j + 2] = w.z; qr[4 * j + 3] = w.w;
         }
       } else {
 #pragma unroll
-        for (int j = 0; j < 64; ++j) qr[j] = 0u;
+        for (int j = 0; j < 32; ++j) qr[j] = 0u;
       }
       if (kFp8) {  // the f16 MMAs take Q as f16 (exact for |q| < 65504)
 #pragma unroll
-        for (int j = 0; j < 64; ++j)
+        for (int j = 0; j < 32; ++j)
           qr[j] = pack_f16(__uint_as_float(qr[j] << 16), __uint_as_float(qr[j] & 0xffff0000u));
       }
-      tmem_st32(tmem + lane_base + kColQ, qr);
-      tmem_st32(tmem + lane_base + kColQ + 32, qr + 32);
+      tmem_st32(tmem + lane_base + kColQ + hf * 32, qr);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&s.q_ready);
@@ -519,24 +543,21 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
       if (!mbar_wait(&s.s_full[i & 1], (i >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
       tc_fence_after();
       const uint32_t tS = tmem + lane_base + kColS0 + (i & 1) * 128;
-      uint32_t sr[128];  // S row, then packed bf16 P pairs
-      tmem_ld32(tS + 0, sr);
-      tmem_ld32(tS + 32, sr + 32);
-      tmem_ld32(tS + 64, sr + 64);
-      tmem_ld32(tS + 96, sr + 96);
+      uint32_t sr[64];  // this half of the S row, then its packed P pairs
+      tmem_ld32(tS + c0, sr);
+      tmem_ld32(tS + c0 + 32, sr + 32);
       tmem_wait_ld();
-      reg_fence<128>(sr);
-      float2 x[64];  // logits in natural units, pairs of columns
+      reg_fence<64>(sr);
+      float2 x[32];  // logits in natural units, pairs of columns
       if (clamped) {
 #pragma unroll
-        for (int k = 0; k < 64; ++k)
+        for (int k = 0; k < 32; ++k)
           x[k] = __ffma2_rn(make_float2(__uint_as_float(sr[2 * k]), __uint_as_float(sr[2 * k + 1])),
                             sc2, bc2);
       } else {
-        const float* bp = bias_buf + g * kBiasStride + (n - 1 - t);
-        // 32 columns at a time: keeps the compiler from hoisting all 128 bias loads
+        const float* bp = bias_buf + g * kBiasStride + (n - 1 - t) + c0;
 #pragma unroll
-        for (int kb = 0; kb < 64; kb += 16) {
+        for (int kb = 0; kb < 32; kb += 16) {
 #pragma unroll
           for (int k = kb; k < kb + 16; ++k)
             x[k] = __ffma2_rn(make_float2(__uint_as_float(sr[2 * k]), __uint_as_float(sr[2 * k + 1])),
@@ -547,9 +568,9 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
       // this page's bias slot may be refilled (the loads above are ordered before it)
       mbar_arrive(&s.b_empty[i % kStages]);
       if (masked) {
-        const int d0 = pq - k0;
+        const int d0 = pq - k0 - c0;
 #pragma unroll
-        for (int k = 0; k < 64; ++k) {
+        for (int k = 0; k < 32; ++k) {
           const int d = d0 - 2 * k;
           const bool a0 = d >= 0 && (W == 0 || d <= W - 1);
           const bool a1 = d - 1 >= 0 && (W == 0 || d - 1 <= W - 1);
@@ -560,15 +581,20 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
       float mx0 = fmax3(x[0].x, x[0].y, x[1].x), mx1 = fmax3(x[1].y, x[2].x, x[2].y);
       float mx2 = fmax3(x[3].x, x[3].y, x[4].x), mx3 = fmax3(x[4].y, x[5].x, x[5].y);
 #pragma unroll
-      for (int k = 6; k < 62; k += 4) {
+      for (int k = 6; k < 30; k += 4) {
         mx0 = fmax3(mx0, x[k].x, x[k].y);
         mx1 = fmax3(mx1, x[k + 1].x, x[k + 1].y);
         mx2 = fmax3(mx2, x[k + 2].x, x[k + 2].y);
         mx3 = fmax3(mx3, x[k + 3].x, x[k + 3].y);
       }
-      mx0 = fmax3(mx0, x[62].x, x[62].y);
-      mx1 = fmax3(mx1, x[63].x, x[63].y);
-      const float m_new = fmax3(m, fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+      mx0 = fmax3(mx0, x[30].x, x[30].y);
+      mx1 = fmax3(mx1, x[31].x, x[31].y);
+      // the other half's maximum of this page
+      const float pm = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+      s.xm[i & 1][hf][r] = pm;
+      mbar_arrive(&s.x_full[i & 1]);
+      if (!mbar_wait(&s.x_full[i & 1], (i >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
+      const float m_new = fmax3(m, pm, s.xm[i & 1][hf ^ 1][r]);
       const bool need = m_new > m + kRescaleThreshold || (m == -INFINITY && m_new > -INFINITY);
       const float alpha = need ? ex2((m - m_new) * kLog2e) : 1.f;
       if (need) {
@@ -579,21 +605,21 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
       const float nm = m == -INFINITY ? 0.f : -m * kLog2e;  // p = 2^(x log2 e - m log2 e)
       const float2 nm2 = make_float2(nm, nm);
 #pragma unroll
-      for (int k = 0; k < 64; ++k) {
+      for (int k = 0; k < 32; ++k) {
         const float2 d2 = __ffma2_rn(x[k], lg2, nm2);
         const float2 e2 = make_float2(ex2(d2.x), ex2(d2.y));
         l2 = __fadd2_rn(l2, e2);
         sr[k] = kFp8 ? pack_f16(e2.x, e2.y) : pack_bf16(e2.x, e2.y);
       }
-      // rescale O (warp-wide, only when some row's max grew past the threshold)
+      // rescale this half of O (warp-wide, only when some row's max grew past the threshold)
       if (__any_sync(0xffffffffu, need) && i > 0) {
         // O must hold PV(i-1) before it is scaled
         if (!mbar_wait(&s.pv_done, (i - 1) & 1, abort_flag, p.status)) ok = false;
         tc_fence_after();
         uint32_t orr[32];
-        const uint32_t tO = tmem + lane_base + kColO;
+        const uint32_t tO = tmem + lane_base + kColO + c0;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
           tmem_ld32(tO + c * 32, orr);
           tmem_wait_ld();
           reg_fence<32>(orr);
@@ -602,40 +628,49 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
           tmem_st32(tO + c * 32, orr);
         }
       }
-      tmem_st32(tS + 0, sr);
-      tmem_st32(tS + 32, sr + 32);
+      tmem_st32(tS + hf * 32, sr);  // P words 32 hf .. 32 hf + 31 (keys c0 .. c0 + 63)
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&s.p_full[i & 1]);
       if (!ok) break;
     }
-    const float l = l2.x + l2.y;
+    // the two halves' sums
+    const float l_mine = l2.x + l2.y;
+    float l = l_mine;
+    if (ok) {
+      // slot np % 2 was last used by page np - 2, whose reads page np - 1's exchange ordered
+      s.xm[np & 1][hf][r] = l_mine;
+      mbar_arrive(&s.l_full);
+      ok = mbar_wait(&s.l_full, 0, abort_flag, p.status);
+      if (ok) l = l_mine + s.xm[np & 1][hf ^ 1][r];
+    }
     if (ok) ok = mbar_wait(&s.o_full, 0, abort_flag, p.status);
     if (!ok) {
       report(p.status, kErrTimeout);
       s.abort_flag = 1;
     } else {
       tc_fence_after();
-      const uint32_t tO = tmem + lane_base + kColO;
+      const uint32_t tO = tmem + lane_base + kColO + c0;
       const bool direct = nsplit_b == 1;
       // V = code * v_scale for an FP8 cache: scaled here, partials included
       const float inv_l = direct ? p.v_scale / l : p.v_scale;
       const size_t prow = (((size_t)b * p.Hkv + kvh) * p.num_splits + split) * p.rmax + r;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         uint32_t orr[32];
         tmem_ld32(tO + c * 32, orr);
         tmem_wait_ld();
         reg_fence<32>(orr);
         if (!valid) continue;
+        const int col = c0 + c * 32;
         if (!direct) {
-          float4* dst = reinterpret_cast<float4*>(p.part_o + prow * 128 + c * 32);
+          float4* dst = reinterpret_cast<float4*>(p.part_o + prow * 128 + col);
 #pragma unroll
           for (int j = 0; j < 8; ++j)
             dst[j] = make_float4(__uint_as_float(orr[4 * j]) * inv_l, __uint_as_float(orr[4 * j + 1]) * inv_l,
                                  __uint_as_float(orr[4 * j + 2]) * inv_l, __uint_as_float(orr[4 * j + 3]) * inv_l);
         } else {
-          const size_t obase = ((size_t)(t_seq0 + t) * p.Hq + h) * 128 + c * 32;
+          const size_t obase = ((size_t)(t_seq0 + t) * p.Hq + h) * 128 + col;
           if (p.out_dtype == 0) {
             uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + obase);
 #pragma unroll
@@ -656,7 +691,7 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
           }
         }
       }
-      if (valid) {
+      if (valid && hf == 0) {
         if (nsplit_b == 1) {
           if (p.lse != nullptr) p.lse[(size_t)(t_seq0 + t) * p.Hq + h] = m + __log2f(l) * kLn2;
         } else {
@@ -670,7 +705,7 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kWarpMma) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -830,11 +865,12 @@ cudaError_t launch_decode(const AttnArgs& a, const AttnMaps& maps, cudaStream_t 
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid(a.num_splits, a.Hkv, a.B);
-  if (a.kv_fp8) {
+  {
+    // an increase that the launch allocation cannot cover would wait forever
     cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, decode_kernel<true>);
+    e = cudaFuncGetAttributes(&fa, a.kv_fp8 ? decode_kernel<true> : decode_kernel<false>);
     if (e != cudaSuccess) return e;
-    if (fa.numRegs != kF8LaunchRegs) return cudaErrorInvalidConfiguration;  // see kF8LaunchRegs
+    if (fa.numRegs != (a.kv_fp8 ? kF8LaunchRegs : kLaunchRegs)) return cudaErrorInvalidConfiguration;
   }
   e = a.kv_fp8 ? launch_pdl(decode_kernel<true>, grid, dim3(kThreadsF8), smem, stream, maps.k,
                             maps.v, p)
