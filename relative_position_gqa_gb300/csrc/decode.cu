@@ -54,8 +54,9 @@ constexpr int kConvWarps = 4;  // per tensor
 static_assert(256 * kF8SoftmaxRegs + (kThreadsF8 - 256) * kF8OtherRegs <= kThreadsF8 * kF8LaunchRegs,
               "register split exceeds the launch allocation");
 constexpr int kMaxG = 16;
-// floats per staged head (>= 127 + 9); 164 = 4 (mod 32), so the G heads x 4 tokens of a
-// warp (lane = t*G + g) hit distinct banks when they read column c
+// floats per staged head (>= 127 + 9 + 3, a multiple of 4 so that each head's slot is
+// 16-byte aligned); 164 = 4 (mod 32), so the G heads x 4 tokens of a warp
+// (lane = t*G + g) hit distinct banks when they read column c
 constexpr int kBiasStride = 164;
 constexpr uint32_t kIdescQK = idesc_bf16(128, 128, false, false);
 constexpr uint32_t kIdescPV = idesc_bf16(128, 128, false, true);
@@ -69,7 +70,7 @@ constexpr uint32_t kColQ = 0, kColS0 = 128, kColO = 384;
 struct __align__(1024) Smem {
   uint8_t k[kStages][2][16384];
   uint8_t v[kStages][2][16384];
-  float bias[kStages][kMaxG * kBiasStride];  // raw table values, staged per page by the TMA warp
+  float bias[kStages][kMaxG * kBiasStride];  // raw table values, staged per page by the bias warp
   // k_full / v_full: kStages bf16 stages or kStagesF8 (4) E4M3 stages
   uint64_t k_full[4], v_full[4], kv_empty[kStages], b_full[kStages], b_empty[kStages];
   uint64_t q_ready, s_full[2], p_full[2], pv_done, o_full, drain;
@@ -357,10 +358,15 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
     }
   } else if (warp == kWarpBias) {
     // ------------------------------------------------------------ bias stager ---
-    // All 32 lanes stage the page's bias slices with 4-byte cp.async copies (no register
-    // round trip) and arrive on b_full[slot] when their copies land.  A slot is reused
-    // once every softmax thread has added the slice it held (b_empty).
-    const int R = p.R, span = 127 + n;
+    // Slot m of head g's slice holds b[kvh*G + g][a0 + m], a0 = the page's smallest
+    // distance rounded down to a multiple of 4, so the slice is one aligned run of the
+    // table: lane 0 fetches it with one bulk copy per head.  Slices that need clamping
+    // (distances below 0 or past R-1) are staged by all lanes with 4-byte cp.async
+    // copies of the clamped entries.  Both ways 32 arrivals complete b_full[slot]; a
+    // slot is reused once every softmax thread has added the slice it held (b_empty).
+    const int R = p.R;
+    const bool bulk_ok = ((reinterpret_cast<uintptr_t>(p.bias) & 15) == 0) && (R & 3) == 0;
+    int staged = 0;
     for (int i = 0; i < np; ++i) {
       const int st = i % kStages;
       int ok = 1;
@@ -374,23 +380,44 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
         }
         break;
       }
+      staged = i + 1;
       const int k0 = (pg0 + i) * 128;
-      const int dmax = (L - 1) - k0;                 // largest distance in the page
-      if ((L - n) - k0 - 127 < R - 1) {              // not every distance clamped
-        // head g: slot j holds b[kvh*G + g][clamp(dmax - j, 0, R-1)], j < 127 + n
+      const int dmax = (L - 1) - k0;    // largest distance in the page
+      const int dmin = (L - n) - k0 - 127;  // smallest, over all rows
+      const int a0 = dmin & ~3;
+      const int cnt = (dmax - a0 + 4) & ~3;  // <= 127 + 9 + 3, rounded up to 4: fits the stride
+      if (dmin < R - 1) {                    // not every distance clamped
+        if (bulk_ok && a0 >= 0 && a0 + cnt <= R) {
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&s.b_full[st], (uint32_t)(p.G * cnt * 4));
+            for (int gg = 0; gg < p.G; ++gg)
+              bulk_g2s(s.bias[st] + gg * kBiasStride, p.bias + (size_t)(kvh * p.G + gg) * R + a0,
+                       (uint32_t)(cnt * 4), &s.b_full[st]);
+          } else {
+            mbar_arrive(&s.b_full[st]);
+          }
+          continue;
+        }
         for (int gg = 0; gg < p.G; ++gg) {
           float* dst = s.bias[st] + gg * kBiasStride;
           const float* src = p.bias + (size_t)(kvh * p.G + gg) * R;
-          for (int j = lane; j < span; j += 32) {
-            int d = dmax - j;
+          for (int m = lane; m < cnt; m += 32) {
+            int d = a0 + m;
             d = d < 0 ? 0 : (d > R - 1 ? R - 1 : d);
-            cp_async_4(dst + j, src + d);
+            cp_async_4(dst + m, src + d);
           }
         }
       }
       cp_async_mbar_arrive(&s.b_full[st]);
     }
-    // let outstanding copies land before the CTA can exit
+    // let outstanding copies land before the CTA can exit (bulk copies: their b_full)
+    if (lane == 0) {
+      for (int i = max(0, staged - kStages); i < staged; ++i) {
+        volatile int never = 0;
+        mbar_wait(&s.b_full[i % kStages], (i / kStages) & 1, &never);
+      }
+    }
+    __syncwarp();
     asm volatile("cp.async.wait_all;" ::: "memory");
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------- MMA issuer ---
@@ -555,13 +582,14 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
           x[k] = __ffma2_rn(make_float2(__uint_as_float(sr[2 * k]), __uint_as_float(sr[2 * k + 1])),
                             sc2, bc2);
       } else {
-        const float* bp = bias_buf + g * kBiasStride + (n - 1 - t) + c0;
+        // slot of column c: distance pq - k0 - c minus the slice start a0
+        const float* bp = bias_buf + g * kBiasStride + (pq - k0 - (dmin & ~3)) - c0;
 #pragma unroll
         for (int kb = 0; kb < 32; kb += 16) {
 #pragma unroll
           for (int k = kb; k < kb + 16; ++k)
             x[k] = __ffma2_rn(make_float2(__uint_as_float(sr[2 * k]), __uint_as_float(sr[2 * k + 1])),
-                              sc2, make_float2(bp[2 * k], bp[2 * k + 1]));
+                              sc2, make_float2(bp[-2 * k], bp[-2 * k - 1]));
           asm volatile("" ::: "memory");
         }
       }

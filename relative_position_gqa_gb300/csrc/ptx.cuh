@@ -97,6 +97,16 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
 
 // 4-byte asynchronous global -> shared copy (no register round trip); pair with
 // cp_async_mbar_arrive so an mbarrier tracks its completion.
+// Bulk copy global -> shared (no tensor map): both addresses 16-byte aligned, bytes a
+// multiple of 16; completion is counted on the mbarrier's transaction bytes.
+__device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src, uint32_t bytes,
+                                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst_smem)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
 __device__ __forceinline__ void cp_async_4(void* dst_smem, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst_smem)), "l"(src)
                : "memory");
