@@ -81,11 +81,13 @@ struct __align__(1024) Smem {
   uint8_t v[kStages][2][16384];
   // [stage][head slot][copy layout]: rev[j] = b[h][clamp(delta + 127 - j)], four shifted copies
   float bias[kStages][2][kBiasWords];
+  float bias_raw[kStages][2][264];  // the tile's run of the table, as one bulk copy landed it
   uint64_t q_full;
   // a K stage is free once the tile's last QK^T is done, a V stage once its last PV is
   // done: K for the next tile is fetched while the current tile's softmax and PV run
   uint64_t k_full[kStages], v_full[kStages], k_empty[kStages], v_empty[kStages];
   uint64_t s_full[2], p_full[2], o_full, drain, b_full[kStages];
+  uint64_t raw_full[kStages][2];
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -160,6 +162,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_q,
       mbar_init(&s.k_empty[i], 1);
       mbar_init(&s.v_empty[i], 1);
       mbar_init(&s.b_full[i], 64);
+      mbar_init(&s.raw_full[i][0], 1);
+      mbar_init(&s.raw_full[i][1], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s.s_full[i], 1);
@@ -248,14 +252,22 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_q,
     }
    } else if (warp >= 10) {
     // ---------------------------------------------------------- bias stagers ---
-    // warp 10 stages head A's slice, warp 11 head B's, with 4-byte cp.async copies:
-    // rev[j] = b[h][clamp(delta + 127 - j, 0, R-1)], j < 256, written to the four shifted
-    // copies, so softmax thread r reads its run rev[127 - r + c], c = 0..127, four values
-    // at a time.  Both warps arrive on b_full[stage] for every tile (count 64).
+    // warp 10 stages head A's slice, warp 11 head B's: rev[j] = b[h][min(d, R-1)] at
+    // distance d = delta + 127 - j, j < 256, or -inf where d is not attended (d < 0, or
+    // past the window), written to the four shifted copies, so softmax thread r reads
+    // its run rev[127 - r + c], c = 0..127, four values at a time.  When the tile's
+    // distances need no clamping, lane 0 fetches their run of the table with one
+    // 16-byte-aligned bulk copy and the warp expands it into the copies from shared
+    // memory; otherwise all lanes copy the clamped entries with 4-byte cp.async.  Both
+    // warps arrive on b_full[stage] for every tile (count 64).
     const int slot = warp - 10;
     const bool mine = slot == 0 || has_b;
     const float* brow = p.bias + (size_t)(h0 + slot) * p.R;
     const int R = p.R, W = p.window;
+    const bool bulk_ok = ((reinterpret_cast<uintptr_t>(p.bias) & 15) == 0) && (R & 3) == 0;
+    // raw_full[stage] completes once per bulk copy into that stage, and only some tiles
+    // take the bulk path: count the uses per stage to know which phase to wait for
+    uint32_t raw_uses = 0;  // bit st: parity of the next use of stage st (kStages <= 32)
     for (int i = 0; i < ntiles; ++i) {
       const int st = i % kStages;
       int ok = 1;
@@ -265,10 +277,38 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_q,
       if (!ok) break;
       const int delta = P0 - (kt_hi - i) * kTile;
       const bool masked = delta < 127 || (W > 0 && delta + 127 > W - 1);
+      const int a0 = (delta - 127) & ~3;              // the run starts 16-byte aligned
+      const int cnt = (delta + 127 - a0 + 4) & ~3;    // <= 258, rounded up to 4
+      float* dst = &s.bias[st][slot][0];
+      if (mine && (delta - 127 < R - 1 || masked) && bulk_ok && a0 >= 0 && a0 + cnt <= R) {
+        float* raw = &s.bias_raw[st][slot][0];
+        uint64_t* rf = &s.raw_full[st][slot];
+        if (lane == 0) {
+          mbar_arrive_expect_tx(rf, (uint32_t)(cnt * 4));
+          bulk_g2s(raw, brow + a0, (uint32_t)(cnt * 4), rf);
+        }
+        const uint32_t par = (raw_uses >> st) & 1u;
+        raw_uses ^= 1u << st;
+        if (!mbar_wait(rf, par, abort_flag, p.status)) {
+          volatile int never = 0;  // the copy may still be in flight: let it land
+          if (lane == 0) mbar_wait(rf, par, &never);
+          __syncwarp();
+          break;
+        }
+#pragma unroll
+        for (int j = lane; j < 256; j += 32) {
+          const int d = delta + 127 - j;
+          const bool off = d < 0 || (W > 0 && d > W - 1);
+          const float v = off ? -INFINITY : raw[d - a0];
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            if (j >= c) dst[c * kBiasCopyStride + j - c] = v;
+        }
+        __syncwarp();
+        mbar_arrive(&s.b_full[st]);  // release: the stores above are seen by the waiters
+        continue;
+      }
       if (mine && (delta - 127 < R - 1 || masked)) {
-        // rev[j] at distance d = delta + 127 - j: b[h][min(d, R-1)], or -inf where d is
-        // not attended (d < 0, or past the window), so the mask rides on the bias
-        float* dst = &s.bias[st][slot][0];
 #pragma unroll
         for (int j = lane; j < 256; j += 32) {
           const int d = delta + 127 - j;

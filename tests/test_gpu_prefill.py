@@ -48,6 +48,12 @@ CASES = {
     "gqa8": W.small(q_lens=(384,), hq=8, hkv=1, r=200, window=256),
     "empty_seq": W.small(q_lens=(0, 70, 0, 5), seq_lens=(10, 70, 0, 300), hq=2, hkv=1, r=32),
     "bias_r_mid_tile": W.small(q_lens=(513,), hq=2, hkv=1, r=300),
+    # tables long enough that interior tiles fetch their bias run with one bulk copy,
+    # mixed with diagonal and clamped tiles that take the per-element path
+    "bulk_bias_full": W.small(q_lens=(900,), hq=4, hkv=2, r=1024),
+    "bulk_bias_window": W.small(q_lens=(1000, 300), seq_lens=(1200, 300), hq=2, hkv=1, r=2048,
+                                window=420),
+    "bulk_bias_clamp_edge": W.small(q_lens=(700,), hq=2, hkv=1, r=520),
 }
 
 
