@@ -114,6 +114,18 @@ __device__ __forceinline__ uint64_t desc_v(const uint8_t (*atoms)[16384], int ks
   // 16 keys per MMA = 2048 bytes, the two d halves 16 KB apart.
   return sdesc_sw128(smem_u32(atoms[0]) + ks * 2048, 16384, 1024);
 }
+// The descriptor of k-step ks from that of k-step 0: only the start address moves, and
+// the address field counts 16-byte units (shared addresses stay far below its 2^18 B).
+__device__ __forceinline__ uint64_t step_kmajor(uint64_t d0, int ks) {
+  return d0 + (uint64_t)((ks >> 2) * 1024 + (ks & 3) * 2);
+}
+__device__ __forceinline__ uint64_t step_v(uint64_t d0, int ks) { return d0 + (uint64_t)(ks * 128); }
+// A value the compiler must treat as new at this point: keeps it from precomputing, and
+// holding in the issuer's few registers, all sixteen k-step descriptors of the Q tiles.
+__device__ __forceinline__ uint64_t opaque(uint64_t x) {
+  asm volatile("" : "+l"(x));
+  return x;
+}
 
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap map_q,
@@ -325,6 +337,21 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_q,
     asm volatile("cp.async.wait_all;" ::: "memory");
   } else if (warp == 9) {
     // ------------------------------------------------------------- MMA issuer ---
+    const uint64_t dq0 = desc_kmajor(s.q[0], 0), dq1 = desc_kmajor(s.q[1], 0);
+    // S[tmem_d] = Q K^T over the eight 16-wide k-steps of d = 128
+    auto qk = [&](uint32_t tmem_d, uint64_t dq, const uint8_t (*k_atoms)[16384]) {
+      const uint64_t a = opaque(dq), b = desc_kmajor(k_atoms, 0);
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks)
+        umma_ss(tmem_d, step_kmajor(a, ks), step_kmajor(b, ks), kIdescQK, ks > 0);
+    };
+    // O[tmem_d] (+)= P V over eight 16-key k-steps, P read from TMEM columns tmem_p
+    auto pv = [&](uint32_t tmem_d, uint32_t tmem_p, const uint8_t (*v_atoms)[16384], bool acc) {
+      const uint64_t b = desc_v(v_atoms, 0);
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks)
+        umma_ts(tmem_d, tmem_p + ks * 8, step_v(b, ks), kIdescPV, acc || ks > 0);
+    };
     bool ok = mbar_wait(&s.q_full, 0, abort_flag, p.status) && mbar_wait(&s.k_full[0], 0, abort_flag, p.status);
     bool issued_any = false;
     if (ok) {
@@ -332,15 +359,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_q,
       if ((kt_hi + 1) * kTile > L) zero_tail_rows(s.k[0], L - kt_hi * kTile, lane);
       tc_fence_after();
       if (lane == 0) {
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks)
-          umma_ss(tmem + 0, desc_kmajor(s.q[0], ks), desc_kmajor(s.k[0], ks), kIdescQK, ks > 0);
+        qk(tmem + 0, dq0, s.k[0]);
         umma_commit(&s.s_full[0]);
         if (has_b) {
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks)
-            umma_ss(tmem + 128, desc_kmajor(s.q[1], ks), desc_kmajor(s.k[0], ks), kIdescQK,
-                    ks > 0);
+          qk(tmem + 128, dq1, s.k[0]);
           umma_commit(&s.s_full[1]);
         }
         umma_commit(&s.k_empty[0]);  // tile 0's K has been read by both QK^T
@@ -356,11 +378,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_q,
       // keys past the end of the sequence: their P is 0, but junk V could be NaN
       if (i == 0 && (kt_hi + 1) * kTile > L) zero_tail_rows(s.v[st], L - kt_hi * kTile, lane);
       tc_fence_after();
-      if (lane == 0) {
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks)
-          umma_ts(tmem + 256, tmem + 0 + ks * 8, desc_v(s.v[st], ks), kIdescPV, (i > 0 || ks > 0));
-      }
+      if (lane == 0) pv(tmem + 256, tmem + 0, s.v[st], i > 0);
       __syncwarp();
       const bool more = i + 1 < ntiles;
       const int st1 = (i + 1) % kStages;
@@ -369,9 +387,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_q,
         if (!ok) break;
         tc_fence_after();
         if (lane == 0) {
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks)
-            umma_ss(tmem + 0, desc_kmajor(s.q[0], ks), desc_kmajor(s.k[st1], ks), kIdescQK, ks > 0);
+          qk(tmem + 0, dq0, s.k[st1]);
           umma_commit(&s.s_full[0]);
         }
         __syncwarp();
@@ -380,21 +396,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_q,
         ok = mbar_wait(&s.p_full[1], i & 1, abort_flag, p.status);
         if (!ok) break;
         tc_fence_after();
-        if (lane == 0) {
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks)
-            umma_ts(tmem + 384, tmem + 128 + ks * 8, desc_v(s.v[st], ks), kIdescPV,
-                    (i > 0 || ks > 0));
-        }
+        if (lane == 0) pv(tmem + 384, tmem + 128, s.v[st], i > 0);
         __syncwarp();
       }
       if (lane == 0) {
         umma_commit(&s.v_empty[st]);  // both PV of tile i are issued
         if (has_b && more) {
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks)
-            umma_ss(tmem + 128, desc_kmajor(s.q[1], ks), desc_kmajor(s.k[st1], ks), kIdescQK,
-                    ks > 0);
+          qk(tmem + 128, dq1, s.k[st1]);
           umma_commit(&s.s_full[1]);
         }
         if (more) umma_commit(&s.k_empty[st1]);  // both QK^T of tile i+1 are issued
