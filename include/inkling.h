@@ -270,6 +270,54 @@ INKLING_API int inkling_rel_attn_decode_noalloc(
     int32_t T, int32_t Hq, int32_t Hkv, int64_t num_blocks, int32_t max_q_len,
     int32_t max_seq_len, int32_t num_splits, int32_t *dev_status, inkling_stream_t stream);
 
+/*
+ * inkling_prefill_step_host / inkling_decode_step_host — one whole step, the sconv of the
+ * new tokens (inkling_sconv_kv) then the attention (inkling_rel_attn_prefill, or
+ * inkling_rel_attn_decode with its workspace and split arguments), for a caller whose
+ * per-step tensors live in page-locked host memory:
+ *   q_host [T][Hq][128] bf16, k_raw_host / v_raw_host [T][Hkv*128] bf16   (read)
+ *   out_host [T][Hq][128], bf16 or f32 by out_dtype                       (written)
+ * q_dev, k_raw_dev, v_raw_dev, out_dev are device staging buffers of the same shapes,
+ * owned by the caller; every other pointer is the device pointer the separate calls take
+ * (cu_q_lens on the device, and cu_q_lens_host, its host copy, which gives the sequence
+ * boundaries).  The step is cut into `chunks` groups of whole sequences with about T /
+ * chunks tokens each.  Group g's rows go up on h2d_stream, group g is computed on
+ * `stream` once they have landed, and its output rows come down on d2h_stream, so the
+ * host link carries one group while the GPU computes another (groups are independent:
+ * a sequence's attention reads only its own pages).  h2d_stream first waits for the work
+ * already on `stream` (the staging buffers may still be in use), and `stream` ends
+ * waiting for the last copy down, so an event recorded on `stream` after the call marks
+ * the end of the whole step.  The three streams must be distinct; chunks >= 1 (more
+ * chunks than sequences are capped at B).  Nothing is synchronised: the call returns
+ * once everything is enqueued, and out_host is complete when `stream` reaches that point.
+ * Host-side argument errors are returned before anything is enqueued; an error from one
+ * group's launch stops the enqueueing and is returned (earlier groups stay enqueued).
+ * Device-side errors land in dev_status as for the separate calls.  The decode form takes
+ * a workspace sized for all B sequences (inkling_rel_attn_decode_workspace_size); the
+ * groups reuse it one after another on `stream`, all with the split count the whole batch
+ * would get (num_splits = 0) or the one given.
+ */
+INKLING_API int inkling_prefill_step_host(
+    const void *q_host, const void *k_raw_host, const void *v_raw_host, void *out_host,
+    void *q_dev, void *k_raw_dev, void *v_raw_dev, void *out_dev, const int32_t *cu_q_lens_host,
+    const float *w_k, const float *w_v, void *sconv_state, const int32_t *cu_q_lens,
+    const int64_t *slot_mapping, void *k_cache, void *v_cache, const int32_t *block_table,
+    int32_t max_blocks, const int32_t *seq_lens, const float *bias, int32_t R, float scale,
+    int32_t window, int32_t out_dtype, float *lse, int32_t B, int32_t T, int32_t Hq,
+    int32_t Hkv, int64_t num_blocks, int32_t max_q_len, int32_t chunks, int32_t *dev_status,
+    inkling_stream_t stream, inkling_stream_t h2d_stream, inkling_stream_t d2h_stream);
+INKLING_API int inkling_decode_step_host(
+    const void *q_host, const void *k_raw_host, const void *v_raw_host, void *out_host,
+    void *q_dev, void *k_raw_dev, void *v_raw_dev, void *out_dev, const int32_t *cu_q_lens_host,
+    const float *w_k, const float *w_v, void *sconv_state, const int32_t *cu_q_lens,
+    const int64_t *slot_mapping, void *k_cache, void *v_cache, const int32_t *block_table,
+    int32_t max_blocks, const int32_t *seq_lens, const float *bias, int32_t R, float scale,
+    int32_t window, int32_t out_dtype, float *lse, int32_t B, int32_t T, int32_t Hq,
+    int32_t Hkv, int64_t num_blocks, int32_t max_q_len, int32_t max_seq_len,
+    int32_t num_splits, void *workspace, size_t workspace_bytes, int32_t chunks,
+    int32_t *dev_status, inkling_stream_t stream, inkling_stream_t h2d_stream,
+    inkling_stream_t d2h_stream);
+
 #ifdef __cplusplus
 }
 #endif

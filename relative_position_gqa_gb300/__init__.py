@@ -230,3 +230,81 @@ def rel_attn_decode_noalloc(q, k_cache, v_cache, block_table, cu_q_lens, seq_len
                   int(window), out, out_dtype, lse, cu_q_lens.shape[0] - 1, T, hq,
                   k_cache.shape[1], k_cache.shape[0], int(max_q_len), int(max_seq_len),
                   int(num_splits), dev_status, _stream(stream))
+
+
+def _check_host(*ts):
+    for t in ts:
+        if t.is_cuda or not t.is_pinned() or not t.is_contiguous():
+            raise ValueError("host buffers must be contiguous page-locked CPU tensors")
+
+
+def _step_args(q_host, k_raw_host, v_raw_host, out_host, staging, cu_q_lens_host, w_k, w_v,
+               sconv_state, cu_q_lens, slot_mapping, k_cache, v_cache, block_table, seq_lens,
+               bias, lse, dev_status):
+    q_dev, k_dev, v_dev, out_dev = staging
+    _check_host(q_host, k_raw_host, v_raw_host, out_host)
+    if cu_q_lens_host.is_cuda or cu_q_lens_host.dtype != torch.int32:
+        raise ValueError("cu_q_lens_host must be an int32 CPU tensor")
+    cu_host = cu_q_lens_host.contiguous()
+    dev, out_dtype = _attn_common(q_dev, k_cache, v_cache, block_table, cu_q_lens, seq_lens,
+                                  bias, out_dev, lse, dev_status)
+    _check_cuda(q_dev, k_dev, v_dev, out_dev, w_k, w_v, sconv_state, cu_q_lens, slot_mapping,
+                k_cache, v_cache, block_table, seq_lens, bias, lse, dev_status)
+    for h, d in ((q_host, q_dev), (k_raw_host, k_dev), (v_raw_host, v_dev), (out_host, out_dev)):
+        if h.shape != d.shape or h.dtype != d.dtype:
+            raise ValueError("each host buffer must match its device staging buffer")
+    return dev, out_dtype, cu_host
+
+
+def prefill_step_host(q_host, k_raw_host, v_raw_host, out_host, staging, cu_q_lens_host, w_k,
+                      w_v, sconv_state, cu_q_lens, slot_mapping, k_cache, v_cache, block_table,
+                      seq_lens, bias, *, scale: float, window: int, max_q_len: int,
+                      h2d_stream, d2h_stream, chunks: int = 4, lse=None, dev_status=None,
+                      stream=None) -> None:
+    """inkling_prefill_step_host: sconv_kv + rel_attn_prefill for a step whose Q, raw K/V
+    and output live in page-locked host memory.  `staging` = (q_dev, k_raw_dev, v_raw_dev,
+    out_dev), device buffers of the host buffers' shapes; the copies of one group of
+    sequences run on h2d_stream / d2h_stream while another group is computed."""
+    dev, out_dtype, cu_host = _step_args(q_host, k_raw_host, v_raw_host, out_host, staging,
+                                         cu_q_lens_host, w_k, w_v, sconv_state, cu_q_lens,
+                                         slot_mapping, k_cache, v_cache, block_table, seq_lens,
+                                         bias, lse, dev_status)
+    q_dev, k_dev, v_dev, out_dev = staging
+    with torch.cuda.device(dev):
+        _lib.call("inkling_prefill_step_host", q_host, k_raw_host, v_raw_host, out_host, q_dev,
+                  k_dev, v_dev, out_dev, cu_host, w_k, w_v, sconv_state, cu_q_lens,
+                  slot_mapping, k_cache, v_cache, block_table, block_table.shape[1], seq_lens,
+                  bias, bias.shape[1], float(scale), int(window), out_dtype, lse,
+                  cu_q_lens.shape[0] - 1, q_dev.shape[0], q_dev.shape[1], k_cache.shape[1],
+                  k_cache.shape[0], int(max_q_len), int(chunks), dev_status, _stream(stream),
+                  h2d_stream.cuda_stream, d2h_stream.cuda_stream)
+
+
+def decode_step_host(q_host, k_raw_host, v_raw_host, out_host, staging, cu_q_lens_host, w_k,
+                     w_v, sconv_state, cu_q_lens, slot_mapping, k_cache, v_cache, block_table,
+                     seq_lens, bias, *, scale: float, window: int, max_q_len: int,
+                     max_seq_len: int, h2d_stream, d2h_stream, num_splits: int = 0,
+                     workspace: Optional[torch.Tensor] = None, chunks: int = 1, lse=None,
+                     dev_status=None, stream=None) -> None:
+    """inkling_decode_step_host: sconv_kv + rel_attn_decode over host buffers, as
+    prefill_step_host.  `workspace` is sized for all B sequences (allocated when omitted)."""
+    dev, out_dtype, cu_host = _step_args(q_host, k_raw_host, v_raw_host, out_host, staging,
+                                         cu_q_lens_host, w_k, w_v, sconv_state, cu_q_lens,
+                                         slot_mapping, k_cache, v_cache, block_table, seq_lens,
+                                         bias, lse, dev_status)
+    q_dev, k_dev, v_dev, out_dev = staging
+    B = cu_q_lens.shape[0] - 1
+    hkv = k_cache.shape[1]
+    with torch.cuda.device(dev):
+        need = _lib.workspace_size(B, q_dev.shape[1], hkv, int(max_q_len), int(max_seq_len),
+                                   int(window), int(num_splits))
+        if workspace is None and need > 0:
+            workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+        ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+        _lib.call("inkling_decode_step_host", q_host, k_raw_host, v_raw_host, out_host, q_dev,
+                  k_dev, v_dev, out_dev, cu_host, w_k, w_v, sconv_state, cu_q_lens,
+                  slot_mapping, k_cache, v_cache, block_table, block_table.shape[1], seq_lens,
+                  bias, bias.shape[1], float(scale), int(window), out_dtype, lse, B,
+                  q_dev.shape[0], q_dev.shape[1], hkv, k_cache.shape[0], int(max_q_len),
+                  int(max_seq_len), int(num_splits), workspace, ws_bytes, int(chunks),
+                  dev_status, _stream(stream), h2d_stream.cuda_stream, d2h_stream.cuda_stream)

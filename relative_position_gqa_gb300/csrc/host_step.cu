@@ -1,0 +1,243 @@
+// Whole steps (the sconv of the new tokens, then the attention) over page-locked host
+// buffers.  The step is cut into groups of whole sequences; the copies of one group cross
+// the host link while another group is computed (three streams, events between them).
+// The host link of GB300 moves about 200 GB/s each way, so a prefill step whose Q and
+// output are a few hundred MB spends longer copying than computing unless the two overlap.
+// Host code only: the kernels are the ones the separate calls launch.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <vector>
+
+#include "../../include/inkling.h"
+#include "kernels.h"
+
+namespace {
+
+struct Group {
+  int b0, b1;      // sequences [b0, b1)
+  int64_t t0, t1;  // their new tokens [t0, t1)
+  int max_n;       // longest n_b in the group
+};
+
+// Groups of whole sequences with about T / chunks new tokens each: a group closes once the
+// tokens seen reach its share of T.  Sequences with no new token join their neighbours.
+std::vector<Group> make_groups(const int32_t* cu, int B, int chunks) {
+  std::vector<Group> g;
+  const int64_t T = cu[B];
+  int b0 = 0, max_n = 0;
+  for (int b = 0; b < B; ++b) {
+    const int n = cu[b + 1] - cu[b];
+    if (n > max_n) max_n = n;
+    const int k = (int)g.size() + 1;  // this group's index + 1
+    const bool last = b + 1 == B;
+    if (last || (k < chunks && (int64_t)cu[b + 1] * chunks >= T * k)) {
+      g.push_back(Group{b0, b + 1, cu[b0], cu[b + 1], max_n});
+      b0 = b + 1;
+      max_n = 0;
+    }
+  }
+  return g;
+}
+
+struct Events {
+  std::vector<cudaEvent_t> ev;
+  ~Events() {
+    for (cudaEvent_t e : ev) cudaEventDestroy(e);  // safe while still pending
+  }
+  cudaEvent_t make() {
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return nullptr;
+    ev.push_back(e);
+    return e;
+  }
+};
+
+struct HostRows {
+  const uint8_t* q_host;
+  const uint8_t* k_host;
+  const uint8_t* v_host;
+  uint8_t* out_host;
+  uint8_t* q_dev;
+  uint8_t* k_dev;
+  uint8_t* v_dev;
+  uint8_t* out_dev;
+  size_t q_row, kv_row, out_row;  // bytes per token
+};
+
+int copy_rows(void* dst, const void* src, int64_t t0, int64_t t1, size_t row, cudaMemcpyKind kind,
+              cudaStream_t st) {
+  if (t1 <= t0) return INKLING_OK;
+  return cudaMemcpyAsync(static_cast<uint8_t*>(dst) + t0 * row,
+                         static_cast<const uint8_t*>(src) + t0 * row, (size_t)(t1 - t0) * row,
+                         kind, st) == cudaSuccess
+             ? INKLING_OK
+             : INKLING_ERR_CUDA;
+}
+
+// The pipeline shared by both step forms: `launch(group)` enqueues one group's sconv and
+// attention on `s` and returns an inkling status.
+template <class Launch>
+int run_groups(const HostRows& h, const std::vector<Group>& groups, cudaStream_t s,
+               cudaStream_t up, cudaStream_t down, Launch launch) {
+  Events evs;
+  cudaEvent_t start = evs.make();
+  if (!start) return INKLING_ERR_CUDA;
+  // the staging buffers may still be read by work already on `s`
+  if (cudaEventRecord(start, s) != cudaSuccess || cudaStreamWaitEvent(up, start, 0) != cudaSuccess)
+    return INKLING_ERR_CUDA;
+  std::vector<cudaEvent_t> landed(groups.size());
+  for (size_t i = 0; i < groups.size(); ++i) {
+    const Group& g = groups[i];
+    int rc = copy_rows(h.q_dev, h.q_host, g.t0, g.t1, h.q_row, cudaMemcpyHostToDevice, up);
+    if (rc == INKLING_OK) rc = copy_rows(h.k_dev, h.k_host, g.t0, g.t1, h.kv_row, cudaMemcpyHostToDevice, up);
+    if (rc == INKLING_OK) rc = copy_rows(h.v_dev, h.v_host, g.t0, g.t1, h.kv_row, cudaMemcpyHostToDevice, up);
+    if (rc != INKLING_OK) return rc;
+    landed[i] = evs.make();
+    if (!landed[i] || cudaEventRecord(landed[i], up) != cudaSuccess) return INKLING_ERR_CUDA;
+  }
+  for (size_t i = 0; i < groups.size(); ++i) {
+    const Group& g = groups[i];
+    if (cudaStreamWaitEvent(s, landed[i], 0) != cudaSuccess) return INKLING_ERR_CUDA;
+    const int rc = launch(g);
+    if (rc != INKLING_OK) return rc;
+    cudaEvent_t done = evs.make();
+    if (!done || cudaEventRecord(done, s) != cudaSuccess ||
+        cudaStreamWaitEvent(down, done, 0) != cudaSuccess)
+      return INKLING_ERR_CUDA;
+    const int crc = copy_rows(h.out_host, h.out_dev, g.t0, g.t1, h.out_row, cudaMemcpyDeviceToHost, down);
+    if (crc != INKLING_OK) return crc;
+  }
+  cudaEvent_t end = evs.make();
+  if (!end || cudaEventRecord(end, down) != cudaSuccess || cudaStreamWaitEvent(s, end, 0) != cudaSuccess)
+    return INKLING_ERR_CUDA;
+  return INKLING_OK;
+}
+
+// Host-side checks shared by both forms; fills rows and groups.
+int prepare(const void* q_host, const void* k_raw_host, const void* v_raw_host, void* out_host,
+            void* q_dev, void* k_raw_dev, void* v_raw_dev, void* out_dev,
+            const int32_t* cu_host, int32_t out_dtype, int32_t B, int32_t T, int32_t Hq,
+            int32_t Hkv, int32_t max_q_len, int32_t chunks, inkling_stream_t stream,
+            inkling_stream_t h2d, inkling_stream_t d2h, HostRows* h, std::vector<Group>* groups) {
+  if (!q_host || !k_raw_host || !v_raw_host || !out_host || !q_dev || !k_raw_dev || !v_raw_dev ||
+      !out_dev || !cu_host)
+    return INKLING_ERR_INVALID_ARG;
+  if (B < 0 || T < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || chunks < 1 || max_q_len < 0)
+    return INKLING_ERR_INVALID_ARG;
+  if (out_dtype != INKLING_OUT_BF16 && out_dtype != INKLING_OUT_F32) return INKLING_ERR_INVALID_ARG;
+  if (h2d == nullptr || d2h == nullptr || h2d == d2h || h2d == stream || d2h == stream)
+    return INKLING_ERR_INVALID_ARG;
+  if (cu_host[0] != 0 || (B >= 0 && cu_host[B] != T)) return INKLING_ERR_INVALID_ARG;
+  for (int b = 0; b < B; ++b) {
+    const int n = cu_host[b + 1] - cu_host[b];
+    if (n < 0 || n > max_q_len) return INKLING_ERR_INVALID_ARG;
+  }
+  h->q_host = static_cast<const uint8_t*>(q_host);
+  h->k_host = static_cast<const uint8_t*>(k_raw_host);
+  h->v_host = static_cast<const uint8_t*>(v_raw_host);
+  h->out_host = static_cast<uint8_t*>(out_host);
+  h->q_dev = static_cast<uint8_t*>(q_dev);
+  h->k_dev = static_cast<uint8_t*>(k_raw_dev);
+  h->v_dev = static_cast<uint8_t*>(v_raw_dev);
+  h->out_dev = static_cast<uint8_t*>(out_dev);
+  h->q_row = (size_t)Hq * 128 * 2;
+  h->kv_row = (size_t)Hkv * 128 * 2;
+  h->out_row = (size_t)Hq * 128 * (out_dtype == INKLING_OUT_F32 ? 4 : 2);
+  *groups = B > 0 ? make_groups(cu_host, B, chunks < B ? chunks : B) : std::vector<Group>{};
+  return INKLING_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int inkling_prefill_step_host(
+    const void* q_host, const void* k_raw_host, const void* v_raw_host, void* out_host,
+    void* q_dev, void* k_raw_dev, void* v_raw_dev, void* out_dev, const int32_t* cu_q_lens_host,
+    const float* w_k, const float* w_v, void* sconv_state, const int32_t* cu_q_lens,
+    const int64_t* slot_mapping, void* k_cache, void* v_cache, const int32_t* block_table,
+    int32_t max_blocks, const int32_t* seq_lens, const float* bias, int32_t R, float scale,
+    int32_t window, int32_t out_dtype, float* lse, int32_t B, int32_t T, int32_t Hq,
+    int32_t Hkv, int64_t num_blocks, int32_t max_q_len, int32_t chunks, int32_t* dev_status,
+    inkling_stream_t stream, inkling_stream_t h2d_stream, inkling_stream_t d2h_stream) {
+  HostRows h;
+  std::vector<Group> groups;
+  int rc = prepare(q_host, k_raw_host, v_raw_host, out_host, q_dev, k_raw_dev, v_raw_dev,
+                   out_dev, cu_q_lens_host, out_dtype, B, T, Hq, Hkv, max_q_len, chunks, stream,
+                   h2d_stream, d2h_stream, &h, &groups);
+  if (rc != INKLING_OK) return rc;
+  if (!w_k || !w_v || !sconv_state || !cu_q_lens || !slot_mapping || !block_table || !seq_lens)
+    return INKLING_ERR_INVALID_ARG;
+  if (B == 0 || T == 0) return INKLING_OK;
+  const size_t state_seq = (size_t)2 * 3 * Hkv * 128 * 2;  // bytes of one sequence's state
+  auto launch = [&](const Group& g) {
+    const int nb = g.b1 - g.b0;
+    int r = inkling_sconv_kv(k_raw_dev, v_raw_dev, w_k, w_v,
+                             static_cast<uint8_t*>(sconv_state) + g.b0 * state_seq,
+                             cu_q_lens + g.b0, slot_mapping, k_cache, v_cache, nb, T, Hkv,
+                             num_blocks, g.max_n, dev_status, stream);
+    if (r != INKLING_OK) return r;
+    return inkling_rel_attn_prefill(q_dev, k_cache, v_cache,
+                                    block_table + (size_t)g.b0 * max_blocks, max_blocks,
+                                    cu_q_lens + g.b0, seq_lens + g.b0, bias, R, scale, window,
+                                    out_dev, out_dtype, lse, nb, T, Hq, Hkv, num_blocks, g.max_n,
+                                    dev_status, stream);
+  };
+  return run_groups(h, groups, reinterpret_cast<cudaStream_t>(stream),
+                    reinterpret_cast<cudaStream_t>(h2d_stream),
+                    reinterpret_cast<cudaStream_t>(d2h_stream), launch);
+}
+
+int inkling_decode_step_host(
+    const void* q_host, const void* k_raw_host, const void* v_raw_host, void* out_host,
+    void* q_dev, void* k_raw_dev, void* v_raw_dev, void* out_dev, const int32_t* cu_q_lens_host,
+    const float* w_k, const float* w_v, void* sconv_state, const int32_t* cu_q_lens,
+    const int64_t* slot_mapping, void* k_cache, void* v_cache, const int32_t* block_table,
+    int32_t max_blocks, const int32_t* seq_lens, const float* bias, int32_t R, float scale,
+    int32_t window, int32_t out_dtype, float* lse, int32_t B, int32_t T, int32_t Hq,
+    int32_t Hkv, int64_t num_blocks, int32_t max_q_len, int32_t max_seq_len,
+    int32_t num_splits, void* workspace, size_t workspace_bytes, int32_t chunks,
+    int32_t* dev_status, inkling_stream_t stream, inkling_stream_t h2d_stream,
+    inkling_stream_t d2h_stream) {
+  HostRows h;
+  std::vector<Group> groups;
+  int rc = prepare(q_host, k_raw_host, v_raw_host, out_host, q_dev, k_raw_dev, v_raw_dev,
+                   out_dev, cu_q_lens_host, out_dtype, B, T, Hq, Hkv, max_q_len, chunks, stream,
+                   h2d_stream, d2h_stream, &h, &groups);
+  if (rc != INKLING_OK) return rc;
+  if (!w_k || !w_v || !sconv_state || !cu_q_lens || !slot_mapping || !block_table || !seq_lens)
+    return INKLING_ERR_INVALID_ARG;
+  if (max_q_len > INKLING_MAX_DECODE_Q || num_splits < 0 || max_seq_len < 0)
+    return INKLING_ERR_INVALID_ARG;
+  if (B == 0 || T == 0) return INKLING_OK;
+  // One split count for every group, the one the whole batch would get: a group's
+  // partials then fit in a workspace sized for all B sequences.
+  if (num_splits == 0 && groups.size() > 1) {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+      return INKLING_ERR_CUDA;
+    num_splits = ink::decode_split(B, Hkv, max_q_len, max_seq_len, window, 0, sms).num_splits;
+  }
+  const size_t state_seq = (size_t)2 * 3 * Hkv * 128 * 2;
+  auto launch = [&](const Group& g) {
+    const int nb = g.b1 - g.b0;
+    int r = inkling_sconv_kv(k_raw_dev, v_raw_dev, w_k, w_v,
+                             static_cast<uint8_t*>(sconv_state) + g.b0 * state_seq,
+                             cu_q_lens + g.b0, slot_mapping, k_cache, v_cache, nb, T, Hkv,
+                             num_blocks, g.max_n, dev_status, stream);
+    if (r != INKLING_OK) return r;
+    return inkling_rel_attn_decode(q_dev, k_cache, v_cache,
+                                   block_table + (size_t)g.b0 * max_blocks, max_blocks,
+                                   cu_q_lens + g.b0, seq_lens + g.b0, bias, R, scale, window,
+                                   out_dev, out_dtype, lse, nb, T, Hq, Hkv, num_blocks, g.max_n,
+                                   max_seq_len, num_splits, workspace, workspace_bytes,
+                                   dev_status, stream);
+  };
+  return run_groups(h, groups, reinterpret_cast<cudaStream_t>(stream),
+                    reinterpret_cast<cudaStream_t>(h2d_stream),
+                    reinterpret_cast<cudaStream_t>(d2h_stream), launch);
+}
+
+}  // extern "C"

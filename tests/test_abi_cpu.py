@@ -124,3 +124,33 @@ def test_rollback_host_checks(lib):
     assert call(sa=FAKE + 2) == 1
     assert call(C=4) == 1
     assert call(B=0) == 0
+
+
+def _step(lib, name, **over):
+    cu = (ctypes.c_int32 * 3)(0, 5, 10)  # the host copy of cu_q_lens is read by the checks
+    a = dict(qh=FAKE, kh=FAKE, vh=FAKE, oh=FAKE, qd=FAKE, kd=FAKE, vd=FAKE, od=FAKE,
+             cu_h=ctypes.cast(cu, ctypes.c_void_p), wk=FAKE, wv=FAKE, st=FAKE, cu=FAKE,
+             slot=FAKE, kc=FAKE, vc=FAKE, bt=FAKE, maxb=4, sl=FAKE, bias=FAKE, R=64, scale=0.1,
+             window=0, odt=0, lse=None, B=2, T=10, Hq=4, Hkv=2, nb=4, mq=5)
+    if name == "inkling_decode_step_host":
+        a.update(msl=500, ns=0, ws=None, wsb=0)
+    a.update(chunks=2, ds=None, s=None, up=0x20000, down=0x30000)
+    a.update(over)
+    rc = getattr(lib, name)(*a.values())
+    del cu
+    return rc
+
+
+@pytest.mark.parametrize("name", ["inkling_prefill_step_host", "inkling_decode_step_host"])
+@pytest.mark.parametrize("over", [dict(chunks=0), dict(up=0x30000), dict(down=None),
+                                  dict(qh=None), dict(od=None), dict(odt=3), dict(mq=4),
+                                  dict(T=11), dict(Hq=5), dict(wk=None), dict(B=-1)])
+def test_step_host_checks(lib, name, over):
+    """Host-buffer steps reject bad arguments before enqueueing anything: missing buffers,
+    chunks < 1, copy streams that coincide, lengths that disagree with cu_q_lens_host."""
+    assert _step(lib, name, **over) == 1
+
+
+def test_decode_step_host_checks(lib):
+    assert _step(lib, "inkling_decode_step_host", mq=10) == 1   # more than 9 tokens
+    assert _step(lib, "inkling_decode_step_host", ns=-1) == 1

@@ -1,0 +1,82 @@
+"""GPU: the host-buffer step entry points (inkling_prefill_step_host /
+inkling_decode_step_host) launch the same kernels as the separate calls, one group of
+sequences at a time, so their outputs, caches and sconv states are bit-identical to
+sconv_kv followed by the attention call on device buffers, for any number of groups."""
+import pytest
+import torch
+
+import workloads as W
+from harness import gpu_attn, gpu_sconv
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ink():
+    import relative_position_gqa_gb300 as m
+    m._lib.load()
+    return m
+
+
+def _host_step(ink, g, *, decode, out_dtype, chunks, num_splits=0):
+    spec = g.spec
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    host = [t.cpu().pin_memory() for t in (g.q, g.k_raw, g.v_raw)]
+    out_h = torch.full((spec.total_q, spec.hq, 128), float("nan"), dtype=out_dtype).pin_memory()
+    staging = (torch.empty_like(g.q), torch.empty_like(g.k_raw), torch.empty_like(g.v_raw),
+               torch.empty(out_h.shape, dtype=out_dtype, device="cuda"))
+    lse = torch.full((spec.total_q, spec.hq), float("nan"), dtype=torch.float32, device="cuda")
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+    args = (host[0], host[1], host[2], out_h, staging, g.cu_q_lens.cpu(), g.w_k, g.w_v, g.state,
+            g.cu_q_lens, g.slot_mapping, g.k_cache, g.v_cache, g.block_table, g.seq_lens, g.bias)
+    if decode:
+        ink.decode_step_host(*args, scale=spec.scale, window=spec.window,
+                             max_q_len=spec.max_q_len, max_seq_len=spec.max_seq_len,
+                             num_splits=num_splits, h2d_stream=up, d2h_stream=down,
+                             chunks=chunks, lse=lse, dev_status=st)
+    else:
+        ink.prefill_step_host(*args, scale=spec.scale, window=spec.window,
+                              max_q_len=spec.max_q_len, h2d_stream=up, d2h_stream=down,
+                              chunks=chunks, lse=lse, dev_status=st)
+    torch.cuda.current_stream().synchronize()
+    assert int(st.item()) == 0, ink.status_string(int(st.item()))
+    return out_h, lse
+
+
+def _device_step(ink, g, *, decode, out_dtype, num_splits=0):
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    gpu_sconv(ink, g, st)
+    out, lse = gpu_attn(ink, g, st, decode=decode, out_dtype=out_dtype, num_splits=num_splits)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0, ink.status_string(int(st.item()))
+    return out.cpu(), lse
+
+
+PREFILL = W.small(q_lens=(150, 37, 0, 300, 9), seq_lens=(150, 200, 40, 300, 600), hq=4, hkv=2,
+                  r=64, window=100)
+DECODE = W.small(q_lens=(9, 9, 3, 1), seq_lens=(500, 700, 129, 1000), hq=8, hkv=1, r=64)
+
+
+@pytest.mark.parametrize("chunks", [1, 2, 3, 8])
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_prefill_step_host_bit_identical(ink, chunks, out_dtype):
+    a = W.make_case(PREFILL, seed=5, device="cuda")
+    b = W.make_case(PREFILL, seed=5, device="cuda")
+    ref, ref_lse = _device_step(ink, a, decode=False, out_dtype=out_dtype)
+    got, got_lse = _host_step(ink, b, decode=False, out_dtype=out_dtype, chunks=chunks)
+    assert torch.equal(got.view(torch.uint8), ref.view(torch.uint8))
+    assert torch.equal(got_lse.view(torch.int32), ref_lse.view(torch.int32))
+    assert torch.equal(b.k_cache, a.k_cache) and torch.equal(b.v_cache, a.v_cache)
+    assert torch.equal(b.state, a.state)
+
+
+@pytest.mark.parametrize("chunks", [1, 2, 4])
+def test_decode_step_host_bit_identical(ink, chunks):
+    a = W.make_case(DECODE, seed=6, device="cuda")
+    b = W.make_case(DECODE, seed=6, device="cuda")
+    ref, ref_lse = _device_step(ink, a, decode=True, out_dtype=torch.float32, num_splits=2)
+    got, got_lse = _host_step(ink, b, decode=True, out_dtype=torch.float32, chunks=chunks,
+                              num_splits=2)
+    assert torch.equal(got.view(torch.uint8), ref.view(torch.uint8))
+    assert torch.equal(got_lse.view(torch.int32), ref_lse.view(torch.int32))
+    assert torch.equal(b.state, a.state)
