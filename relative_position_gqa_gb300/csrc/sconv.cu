@@ -191,6 +191,110 @@ __global__ void __launch_bounds__(kSconvThreads) sconv_kernel(const SconvDev p) 
   }
 }
 
+// Step form of the paged conv, for batches whose sequences all have at most kStepRows new
+// tokens (a decode or MTP-verify step): one thread takes every new row of its sequence for
+// 8 channels of K or of V.  Such a step moves a few MB and is bound by load latency, so
+// each thread issues its loads in two rounds only: the lengths, taps and old state; then
+// all its raw rows and their slots at once.  The new state is written from registers.
+// Same arithmetic, in the same order, as sconv_kernel: the outputs are bit-identical.
+constexpr int kStepRows = 16;
+
+template <bool kFp8>
+__global__ void __launch_bounds__(kSconvThreads) sconv_step_kernel(const SconvDev p) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int C = p.C;
+  const int vecs_per_stream = C / kVec;
+  const int vec = blockIdx.x * kSconvThreads + threadIdx.x;
+  if (vec >= p.streams * vecs_per_stream) return;
+  const int which = vec / vecs_per_stream;
+  const int c0 = (vec % vecs_per_stream) * kVec;
+  const int b = blockIdx.y;
+  const uint16_t* x = which == 0 ? p.x[0] : p.x[1];
+  const float* w = which == 0 ? p.w[0] : p.w[1];
+  uint16_t* out = which == 0 ? p.out[0] : p.out[1];
+  const float inv_scale = which == 0 ? p.inv_scale[0] : p.inv_scale[1];
+  uint16_t* st = p.state + ((size_t)b * p.streams + which) * 3 * C + c0;
+
+  // round 1: lengths, taps, the three rows before the step
+  const int t_begin = p.cu_q_lens[b];
+  const int t_end = p.cu_q_lens[b + 1];
+  float tap[kVec][4];
+#pragma unroll
+  for (int i = 0; i < kVec; ++i) {
+    const float4 t4 = __ldg(reinterpret_cast<const float4*>(w + (size_t)(c0 + i) * 4));
+    tap[i][0] = t4.x; tap[i][1] = t4.y; tap[i][2] = t4.z; tap[i][3] = t4.w;
+  }
+  uint4 hist[3];
+#pragma unroll
+  for (int r = 0; r < 3; ++r) hist[r] = *reinterpret_cast<const uint4*>(st + (size_t)r * C);
+  const int n = t_end - t_begin;
+  if (t_begin < 0 || n < 0 || n > p.max_q_len || n > kStepRows || t_end > p.T) {
+    if (threadIdx.x == 0) report(p.status, kErrBadInput);
+    return;
+  }
+  // round 2: every raw row of the step and its slot
+  uint4 raw[kStepRows];
+  long long slot[kStepRows];
+#pragma unroll
+  for (int u = 0; u < kStepRows; ++u) {
+    if (u < n) {
+      raw[u] = __ldg(reinterpret_cast<const uint4*>(x + (size_t)(t_begin + u) * C + c0));
+      slot[u] = p.slot_mapping[t_begin + u];
+    } else {
+      raw[u] = make_uint4(0, 0, 0, 0);
+      slot[u] = -1;
+    }
+  }
+  F8 h0 = unpack8(hist[0]), h1 = unpack8(hist[1]), h2 = unpack8(hist[2]);
+  const int head = c0 >> 7, d0 = c0 & 127;
+#pragma unroll
+  for (int u = 0; u < kStepRows; ++u) {
+    if (u >= n) break;
+    const F8 cur = unpack8(raw[u]);
+    float y[kVec];
+#pragma unroll
+    for (int i = 0; i < kVec; ++i) {
+      float a = tap[i][0] * h0.v[i];
+      a = fmaf(tap[i][1], h1.v[i], a);
+      a = fmaf(tap[i][2], h2.v[i], a);
+      a = fmaf(tap[i][3], cur.v[i], a);
+      y[i] = a;
+    }
+    if (slot[u] >= p.num_slots) {
+      report(p.status, kErrBadBlock);
+    } else if (slot[u] >= 0) {
+      const long long blk = slot[u] >> 7, off = slot[u] & 127;
+      const size_t row = (((size_t)blk * p.Hkv + head) * 128 + off) * 128 + d0;
+      if (kFp8) {
+        uint2 o8;
+        o8.x = pack_e4m3x4(y[0] * inv_scale, y[1] * inv_scale, y[2] * inv_scale, y[3] * inv_scale);
+        o8.y = pack_e4m3x4(y[4] * inv_scale, y[5] * inv_scale, y[6] * inv_scale, y[7] * inv_scale);
+        *reinterpret_cast<uint2*>(reinterpret_cast<uint8_t*>(out) + row) = o8;
+      } else {
+        uint4 o;
+        o.x = pack_bf16(y[0], y[1]);
+        o.y = pack_bf16(y[2], y[3]);
+        o.z = pack_bf16(y[4], y[5]);
+        o.w = pack_bf16(y[6], y[7]);
+        *reinterpret_cast<uint4*>(out + row) = o;
+      }
+    }
+    h0 = h1; h1 = h2; h2 = cur;
+  }
+  // new state = last three rows of [old state ; new rows], picked by selects (no dynamic
+  // register index)
+#pragma unroll
+  for (int r = 0; r < 3; ++r) {
+    const int idx = n - 3 + r;  // index among the new rows
+    uint4 v = idx == -1 ? hist[2] : (idx == -2 ? hist[1] : hist[0]);
+#pragma unroll
+    for (int u = 0; u < kStepRows; ++u)
+      if (u == idx) v = raw[u];
+    *reinterpret_cast<uint4*>(st + (size_t)r * C) = v;
+  }
+}
+
 // State after a speculative step of which only the first accepted[b] new tokens stay:
 // the last three rows of [state_before ; first accepted[b] raw rows].  One thread per
 // (sequence, stream, 8 channels); it reads all three of its rows before writing any, so
@@ -251,6 +355,16 @@ cudaError_t launch_sconv_kv(const SconvArgs& a, cudaStream_t stream) {
   p.max_q_len = a.max_q_len;
   p.num_slots = (long long)a.num_blocks * 128;
   p.status = a.dev_status;
+  if (a.max_q_len <= kStepRows) {
+    if (a.B == 0 || a.max_q_len == 0) return cudaSuccess;
+    const dim3 sg((2 * p.C / kVec + kSconvThreads - 1) / kSconvThreads, a.B);
+    if (a.fp8) {
+      p.inv_scale[0] = (float)(1.0 / (double)a.k_scale);
+      p.inv_scale[1] = (float)(1.0 / (double)a.v_scale);
+      return launch_pdl(sconv_step_kernel<true>, sg, dim3(kSconvThreads), 0, stream, p);
+    }
+    return launch_pdl(sconv_step_kernel<false>, sg, dim3(kSconvThreads), 0, stream, p);
+  }
   const dim3 grid = sconv_grid(2, p.C, a.max_q_len, a.B, SconvShape<true>::kChunk);
   if (grid.y == 0 || grid.z == 0) return cudaSuccess;
   if (a.fp8) {

@@ -103,3 +103,24 @@ def test_skip_slot_and_bad_slot(ink):
     gpu_sconv(ink, g, st)
     torch.cuda.synchronize()
     assert int(st.item()) == 5  # INKLING_ERR_BAD_BLOCK
+
+
+def test_step_form_bit_identical_to_run_form(ink):
+    """A host bound max_q_len <= 16 selects the step form of the kernel (one thread takes
+    all of its sequence's new rows, loads issued in two rounds); a larger bound selects the
+    run form.  They do the same arithmetic in the same order: caches and state agree bit
+    for bit."""
+    spec = W.small(q_lens=(9, 3, 0, 16, 1, 2), seq_lens=(100, 3, 5, 400, 129, 2), hq=2, hkv=2,
+                   history_random=True, state_random=True)
+    out = []
+    for bound in (16, 64):
+        g = W.make_case(spec, seed=43, device="cuda")
+        st = _status()
+        ink.sconv_kv(g.k_raw, g.v_raw, g.w_k, g.w_v, g.state, g.cu_q_lens, g.slot_mapping,
+                     g.k_cache, g.v_cache, max_q_len=bound, dev_status=st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        out.append(g)
+    a, b = out
+    assert torch.equal(a.k_cache, b.k_cache) and torch.equal(a.v_cache, b.v_cache)
+    assert torch.equal(a.state, b.state)
