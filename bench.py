@@ -167,16 +167,24 @@ class ClockSampler:
 
 
 # DRAM bytes (read + write) per launch of the dominant kernel, from one ncu capture of
-# `python bench.py --steps 2 --warmup 3 --no-cpu-baseline` (see profiles/), keyed by the
-# workload and by the SHA-256 of the kernel source it was taken on: when that source has
-# changed since, the figure no longer applies and the line reports null.
+# `python bench.py [--workload W --variant V] --steps 2 --warmup 3 --no-cpu-baseline` (see
+# profiles/), keyed by (workload, variant) and by the SHA-256 of the kernel source it was
+# taken on: when that source has changed since, the figure no longer applies and the line
+# reports null.
 TRAFFIC = {
-    2: ("prefill.cu", "f9c989910fdf43d9300961c5faa69cd49f25df2849c5f71b2e0df68d618f8bca", 613.3e6),
+    (2, None): ("prefill.cu", "f9c989910fdf43d9300961c5faa69cd49f25df2849c5f71b2e0df68d618f8bca",
+                613.3e6),
+    (5, "n1"): ("decode.cu", "cc12c06b99a34b1014eef848ca26221944e8bdd7ff3ac96e9a0f814361e0669d",
+                4301.1e6),
 }
 
 
-def kernel_traffic(workload: int):
-    entry = TRAFFIC.get(workload)
+def kernel_traffic(workload: int, variant=None, fp8: bool = False):
+    if fp8:
+        return None
+    if workload == 5 and variant is None:
+        variant = "n1"
+    entry = TRAFFIC.get((workload, variant))
     if entry is None:
         return None
     import hashlib
@@ -408,7 +416,7 @@ def run_ours(args, ws, rank, local):
                 "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
                 "peak_source": f"{peak_src} bf16_tflops (burst; kernel timed per launch)",
                 "kernel": "prefill_kernel"}
-    roof["traffic"] = args.traffic if args.traffic is not None else kernel_traffic(args.workload)
+    roof["traffic"] = args.traffic if args.traffic is not None else kernel_traffic(args.workload, args.variant, fp8)
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": unit, "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 4),
