@@ -8,8 +8,9 @@ Default workload (one step = the whole hot path over one batch):
 Metric: attention TFLOP/s counting only allowed (query, key) pairs, 4*D flops per pair
 per head (QK^T and PV).  Other workloads (--workload 1..5) print the same line shape;
 the decode ones report KV-read GB/s (algorithmic K/V bytes inside the causal/window range).
---kv fp8 (decode workloads) runs the FP8 KV cache path (inkling_sconv_kv_fp8 +
-inkling_rel_attn_decode_fp8); its GB/s count the E4M3 bytes, half of the bf16 cache's.
+--kv fp8 runs the FP8 KV cache path (inkling_sconv_kv_fp8, then inkling_rel_attn_decode_fp8
+or inkling_rel_attn_prefill_fp8); decode GB/s count the E4M3 bytes, half of the bf16
+cache's; prefill TFLOP/s count the same flops as the bf16 cache.
 --workload 4 also times the sconv-state rollback after the verify step on its own
 (config.rollback_us, not part of the step).  --workload 6 is the conv on a dense stream
 (inkling_sconv on the sliding-window prefill's attention output, 32768 tokens x 4096
@@ -216,8 +217,6 @@ def run_ours(args, ws, rank, local):
     spec = workload_spec(args.workload, args.variant)
     decode = is_decode(args.workload)
     fp8 = args.kv == "fp8"
-    if fp8 and not decode:
-        raise SystemExit("--kv fp8 applies to the decode workloads (4, 5)")
     g = W.make_case(spec, seed=args.workload + 1000 * rank, device=dev)
     K_SCALE, V_SCALE = 0.0625, 0.0625
     if fp8:
@@ -233,10 +232,20 @@ def run_ours(args, ws, rank, local):
         ws_bytes = ink.decode_workspace_size(spec.batch, spec.hq, spec.hkv, spec.max_q_len,
                                              spec.max_seq_len, spec.window)
         workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    elif fp8:  # the widened bf16 pages of the FP8 prefill
+        ws_bytes = ink.prefill_fp8_workspace_size(spec.batch, spec.hkv, g.block_table.shape[1],
+                                                  spec.max_q_len, spec.max_seq_len, spec.window)
+        workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
     def attn(q, o):
-        if fp8:
+        if fp8 and not decode:
+            ink.rel_attn_prefill_fp8(q, g.k_cache, g.v_cache, g.block_table, g.cu_q_lens,
+                                     g.seq_lens, g.bias, k_scale=K_SCALE, v_scale=V_SCALE,
+                                     scale=spec.scale, window=spec.window,
+                                     max_q_len=spec.max_q_len, max_seq_len=spec.max_seq_len,
+                                     out=o, workspace=workspace, dev_status=status)
+        elif fp8:
             ink.rel_attn_decode_fp8(q, g.k_cache, g.v_cache, g.block_table, g.cu_q_lens,
                                     g.seq_lens, g.bias, k_scale=K_SCALE, v_scale=V_SCALE,
                                     scale=spec.scale, window=spec.window,
@@ -348,7 +357,8 @@ def run_ours(args, ws, rank, local):
     # measured 1.66 ms on the full MTP decode against 1.41 ms for one)
     e2e_chunks = 1 if decode else min(4, spec.batch)
     if fp8:
-        e2e_path = "copies + sconv_kv_fp8 + rel_attn_decode_fp8, serial"
+        e2e_path = (f"copies + sconv_kv_fp8 + rel_attn_{'decode' if decode else 'prefill'}_fp8, "
+                    "serial")
     else:
         e2e_path = (f"inkling_{'decode' if decode else 'prefill'}_step_host, "
                     f"{e2e_chunks} groups of sequences")
@@ -415,13 +425,14 @@ def run_ours(args, ws, rank, local):
         roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
                 "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
                 "peak_source": f"{peak_src} bf16_tflops (burst; kernel timed per launch)",
-                "kernel": "prefill_kernel"}
+                "kernel": "widen_pages_kernel + prefill_kernel" if fp8 else "prefill_kernel"}
     roof["traffic"] = args.traffic if args.traffic is not None else kernel_traffic(args.workload, args.variant, fp8)
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": unit, "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16 (KV cache e4m3, f16 MMA)" if fp8 else "bf16",
+        "dtype": ("bf16 (KV cache e4m3, f16 MMA)" if decode else "bf16 (KV cache e4m3 widened to bf16)")
+                 if fp8 else "bf16",
         "data": "synthetic (seeded N(0,1) Q/K/V, N(0,0.5) sconv taps, N(0,sd) bias)",
         "config": {"workload": workload_name(spec) + (" kv=e4m3" if fp8 else ""),
                    "global_batch": spec.batch * ws,
@@ -430,7 +441,8 @@ def run_ours(args, ws, rank, local):
                    "attn_ms": round(attn_ms, 4), "sconv_ms": round(sconv_ms, 4)},
         "e2e": {"value": round(e2e_value, 3), "unit": unit, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4), "path": e2e_path},
-        "gpu_launches": args.steps * (2 + (1 if decode and ws_bytes > 0 else 0)),
+        "gpu_launches": args.steps * (2 + (1 if (decode and ws_bytes > 0) or (fp8 and not decode)
+                                           else 0)),
         "roofline": roof,
         "clocks": clocks.summary(),
     }

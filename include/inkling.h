@@ -193,6 +193,33 @@ INKLING_API int inkling_rel_attn_prefill(const void *q, const void *k_cache, con
                              int32_t *dev_status, inkling_stream_t stream);
 
 /*
+ * inkling_rel_attn_prefill_fp8 — inkling_rel_attn_prefill over the FP8 (E4M3) caches that
+ * inkling_sconv_kv_fp8 writes (blog, "Roadmap": FP8 for the global-attention layers):
+ * K = code * k_scale, V = code * v_scale, same page layout as the decode's FP8 caches.
+ * The call first widens every page that a step's query can see (window-aware) into a
+ * bf16 page pool in the caller's workspace, exactly (E4M3 values are bf16 values), then
+ * runs the bf16 prefill on that pool with scale * k_scale as the logit scale and v_scale
+ * applied to the output.  max_seq_len >= every seq_lens[b] (host bound that sizes the
+ * pool).  workspace: 16-byte aligned device memory of at least
+ * inkling_rel_attn_prefill_fp8_workspace_size(B, Hkv, max_blocks, max_q_len, max_seq_len,
+ * window) bytes, owned by the caller, reused by the next call on the stream; too small ->
+ * INKLING_ERR_WORKSPACE, nothing launched.  Device errors as for the prefill (a sequence
+ * whose pages exceed the max_seq_len bound -> INKLING_ERR_BAD_INPUT).
+ */
+INKLING_API size_t inkling_rel_attn_prefill_fp8_workspace_size(int32_t B, int32_t Hkv,
+                                                               int32_t max_blocks,
+                                                               int32_t max_q_len,
+                                                               int32_t max_seq_len,
+                                                               int32_t window);
+INKLING_API int inkling_rel_attn_prefill_fp8(
+    const void *q, const void *k_cache, const void *v_cache, float k_scale, float v_scale,
+    const int32_t *block_table, int32_t max_blocks, const int32_t *cu_q_lens,
+    const int32_t *seq_lens, const float *bias, int32_t R, float scale, int32_t window,
+    void *out, int32_t out_dtype, float *lse, int32_t B, int32_t T, int32_t Hq, int32_t Hkv,
+    int64_t num_blocks, int32_t max_q_len, int32_t max_seq_len, void *workspace,
+    size_t workspace_bytes, int32_t *dev_status, inkling_stream_t stream);
+
+/*
  * inkling_rel_attn_decode_workspace_size — bytes of device workspace that
  * inkling_rel_attn_decode needs for these limits (0 when no split is needed).
  * num_splits: 0 = the library's choice for this device (same rule as the decode call).

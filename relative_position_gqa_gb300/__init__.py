@@ -208,6 +208,43 @@ def rel_attn_decode_fp8(q, k_cache, v_cache, block_table, cu_q_lens, seq_lens, b
                   ws_bytes, dev_status, _stream(stream))
 
 
+def prefill_fp8_workspace_size(B: int, hkv: int, max_blocks: int, max_q_len: int,
+                               max_seq_len: int, window: int) -> int:
+    """Bytes of workspace inkling_rel_attn_prefill_fp8 needs (the widened bf16 pages)."""
+    return int(_lib.load().inkling_rel_attn_prefill_fp8_workspace_size(
+        int(B), int(hkv), int(max_blocks), int(max_q_len), int(max_seq_len), int(window)))
+
+
+def rel_attn_prefill_fp8(q, k_cache, v_cache, block_table, cu_q_lens, seq_lens, bias, *,
+                         k_scale: float, v_scale: float, scale: float, window: int,
+                         max_q_len: int, max_seq_len: int, out: torch.Tensor,
+                         lse: Optional[torch.Tensor] = None,
+                         workspace: Optional[torch.Tensor] = None, dev_status=None,
+                         stream=None) -> None:
+    """inkling_rel_attn_prefill_fp8: prefill over FP8 (E4M3, uint8) caches, K = code *
+    k_scale, V = code * v_scale.  `workspace` holds the widened bf16 pages (allocated here
+    when omitted)."""
+    dev = _check_cuda(q, k_cache, v_cache, block_table, cu_q_lens, seq_lens, bias, out, lse,
+                      dev_status, workspace)
+    assert q.dtype == torch.bfloat16 and k_cache.dtype == v_cache.dtype == torch.uint8
+    assert block_table.dtype == cu_q_lens.dtype == seq_lens.dtype == torch.int32
+    out_dtype = OUT_BF16 if out.dtype == torch.bfloat16 else OUT_F32
+    T, hq = q.shape[0], q.shape[1]
+    B = cu_q_lens.shape[0] - 1
+    hkv = k_cache.shape[1]
+    with torch.cuda.device(dev):
+        if workspace is None:
+            need = prefill_fp8_workspace_size(B, hkv, block_table.shape[1], max_q_len,
+                                              max_seq_len, window)
+            workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+        ws_bytes = workspace.numel() * workspace.element_size()
+        _lib.call("inkling_rel_attn_prefill_fp8", q, k_cache, v_cache, float(k_scale),
+                  float(v_scale), block_table, block_table.shape[1], cu_q_lens, seq_lens, bias,
+                  bias.shape[1], float(scale), int(window), out, out_dtype, lse, B, T, hq, hkv,
+                  k_cache.shape[0], int(max_q_len), int(max_seq_len), workspace, ws_bytes,
+                  dev_status, _stream(stream))
+
+
 def decode_noalloc_capacity() -> int:
     """Bytes of the library's static decode scratch (per device)."""
     return int(_lib.load().inkling_rel_attn_decode_noalloc_capacity())

@@ -23,6 +23,9 @@ SIGNATURES = {
     "inkling_sconv_state_rollback": [P, P, P, P, P, P, I32, I32, I32, I32, P, P],
     "inkling_rel_attn_prefill": [P, P, P, P, I32, P, P, P, I32, F32, I32, P, I32, P, I32, I32,
                                  I32, I32, I64, I32, P, P],
+    "inkling_rel_attn_prefill_fp8_workspace_size": [I32, I32, I32, I32, I32, I32],
+    "inkling_rel_attn_prefill_fp8": [P, P, P, F32, F32, P, I32, P, P, P, I32, F32, I32, P, I32,
+                                     P, I32, I32, I32, I32, I64, I32, I32, P, SZ, P, P],
     "inkling_rel_attn_decode_workspace_size": [I32, I32, I32, I32, I32, I32, I32],
     "inkling_rel_attn_decode": [P, P, P, P, I32, P, P, P, I32, F32, I32, P, I32, P, I32, I32,
                                 I32, I32, I64, I32, I32, I32, P, SZ, P, P],
@@ -40,7 +43,8 @@ SIGNATURES = {
     "inkling_status_string": [ctypes.c_int],
     "inkling_version": [],
 }
-RESTYPES = {"inkling_rel_attn_decode_workspace_size": SZ, "inkling_status_string": ctypes.c_char_p,
+RESTYPES = {"inkling_rel_attn_decode_workspace_size": SZ,
+            "inkling_rel_attn_prefill_fp8_workspace_size": SZ, "inkling_status_string": ctypes.c_char_p,
             "inkling_rel_attn_decode_noalloc_capacity": SZ}
 
 _lib = None

@@ -226,6 +226,62 @@ int inkling_rel_attn_prefill(const void* q, const void* k_cache, const void* v_c
              : INKLING_ERR_CUDA;
 }
 
+size_t inkling_rel_attn_prefill_fp8_workspace_size(int32_t B, int32_t Hkv, int32_t max_blocks,
+                                                   int32_t max_q_len, int32_t max_seq_len,
+                                                   int32_t window) {
+  if (B <= 0 || Hkv <= 0 || max_blocks <= 0 || max_q_len <= 0 || max_seq_len <= 0 || window < 0)
+    return 0;
+  return ink::prefill_fp8_workspace_bytes(B, Hkv, max_blocks, max_q_len, max_seq_len, window);
+}
+
+int inkling_rel_attn_prefill_fp8(const void* q, const void* k_cache, const void* v_cache,
+                                 float k_scale, float v_scale, const int32_t* block_table,
+                                 int32_t max_blocks, const int32_t* cu_q_lens,
+                                 const int32_t* seq_lens, const float* bias, int32_t R,
+                                 float scale, int32_t window, void* out, int32_t out_dtype,
+                                 float* lse, int32_t B, int32_t T, int32_t Hq, int32_t Hkv,
+                                 int64_t num_blocks, int32_t max_q_len, int32_t max_seq_len,
+                                 void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                 inkling_stream_t stream) {
+  AttnArgs a{};
+  a.q = q; a.k_cache = k_cache; a.v_cache = v_cache; a.block_table = block_table;
+  a.max_blocks = max_blocks; a.cu_q_lens = cu_q_lens; a.seq_lens = seq_lens; a.bias = bias;
+  a.R = R; a.scale = scale; a.window = window; a.out = out; a.out_dtype = out_dtype; a.lse = lse;
+  a.B = B; a.T = T; a.Hq = Hq; a.Hkv = Hkv; a.num_blocks = num_blocks; a.max_q_len = max_q_len;
+  a.dev_status = dev_status; a.max_seq_len = max_seq_len;
+  if (!(k_scale > 0.f) || !(v_scale > 0.f) || !std::isfinite(k_scale) || !std::isfinite(v_scale))
+    return INKLING_ERR_INVALID_ARG;
+  const int rc = check_attn(a);
+  if (rc != INKLING_OK) return rc;
+  if (max_seq_len < 0) return INKLING_ERR_INVALID_ARG;
+  if (B == 0 || T == 0 || max_q_len == 0 || max_seq_len == 0) return INKLING_OK;
+  if (B > 65535 || Hkv > 65535) return INKLING_ERR_UNSUPPORTED;
+  const size_t rp = ink::prefill_fp8_range_pages(max_q_len, max_seq_len, window);
+  if (rp > 0x7fffffff || (size_t)B * rp * (size_t)Hkv > 0x7fffffff) return INKLING_ERR_UNSUPPORTED;
+  const size_t need = ink::prefill_fp8_workspace_bytes(B, Hkv, max_blocks, max_q_len,
+                                                       max_seq_len, window);
+  if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace))
+    return INKLING_ERR_WORKSPACE;
+  // the bf16 pool: K pages, V pages, then the pool's block table
+  const size_t pool_pages = (size_t)B * rp;
+  const size_t pool_bytes = pool_pages * (size_t)Hkv * 128 * 128 * 2;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  void* k16 = ws;
+  void* v16 = ws + pool_bytes;
+  int32_t* table16 = reinterpret_cast<int32_t*>(ws + 2 * pool_bytes);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (ink::launch_widen_pages(a, k16, v16, table16, (int)rp, st) != cudaSuccess)
+    return INKLING_ERR_CUDA;
+  AttnArgs b = a;  // the bf16 prefill on the pool
+  b.k_cache = k16; b.v_cache = v16; b.block_table = table16; b.num_blocks = (long long)pool_pages;
+  b.scale = scale * k_scale;
+  b.out_scale = v_scale;
+  AttnMaps maps;
+  const int mrc = build_maps(b, &maps, true);
+  if (mrc != INKLING_OK) return mrc;
+  return ink::launch_prefill(b, maps, st) == cudaSuccess ? INKLING_OK : INKLING_ERR_CUDA;
+}
+
 size_t inkling_rel_attn_decode_workspace_size(int32_t B, int32_t Hq, int32_t Hkv,
                                               int32_t max_q_len, int32_t max_seq_len,
                                               int32_t window, int32_t num_splits) {

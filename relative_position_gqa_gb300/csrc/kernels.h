@@ -96,6 +96,8 @@ struct AttnArgs {
   // FP8 (E4M3) cache: K = code * k_scale, V = code * v_scale (decode only)
   bool kv_fp8 = false;
   float k_scale = 1.f, v_scale = 1.f;
+  // prefill only: factor on the output (v_scale when the pages were widened from FP8)
+  float out_scale = 1.f;
 };
 
 // Tensor maps built by the host for the attention kernels.
@@ -110,6 +112,12 @@ cudaError_t launch_sconv_dense(const SconvDenseArgs& a, cudaStream_t stream);
 cudaError_t launch_sconv_rollback(const SconvRollbackArgs& a, cudaStream_t stream);
 cudaError_t launch_prefill(const AttnArgs& a, const AttnMaps& maps, cudaStream_t stream);
 cudaError_t launch_decode(const AttnArgs& a, const AttnMaps& maps, cudaStream_t stream);
+// Prefill over an FP8 cache: pages a step's queries can see, widened to a bf16 pool.
+size_t prefill_fp8_range_pages(int max_q_len, int max_seq_len, int window);
+size_t prefill_fp8_workspace_bytes(int B, int Hkv, int max_blocks, int max_q_len,
+                                   int max_seq_len, int window);
+cudaError_t launch_widen_pages(const AttnArgs& a, void* k16, void* v16, int32_t* table16,
+                               int range_pages, cudaStream_t stream);
 
 // Decode split rule shared by the workspace query and the launch.
 struct DecodeSplit {

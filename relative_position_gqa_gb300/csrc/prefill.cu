@@ -106,6 +106,7 @@ struct Params {
   int B, T, Hq, Hkv, G, pairs_per_group, head_pairs, q_tiles, max_q_len;
   long long num_blocks;
   float scale;
+  float out_scale;  // output factor (v_scale of a widened FP8 cache, else 1)
 };
 
 __device__ __forceinline__ uint64_t desc_kmajor(const uint8_t (*atoms)[16384], int ks) {
@@ -555,7 +556,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_q,
         s.abort_flag = 1;
       } else {
         tc_fence_after();
-        const float inv_l = 1.f / l;
+        const float inv_l = p.out_scale / l;
         const int t = t_glob0 + r;
         const bool store = r < rows;
 #pragma unroll
@@ -626,6 +627,7 @@ cudaError_t launch_prefill(const AttnArgs& a, const AttnMaps& maps, cudaStream_t
   p.max_q_len = a.max_q_len;
   p.num_blocks = a.num_blocks;
   p.scale = a.scale;
+  p.out_scale = a.out_scale;
   const long long grid = (long long)p.q_tiles * p.B * p.head_pairs;
   if (grid == 0) return cudaSuccess;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;

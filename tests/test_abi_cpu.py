@@ -154,3 +154,24 @@ def test_step_host_checks(lib, name, over):
 def test_decode_step_host_checks(lib):
     assert _step(lib, "inkling_decode_step_host", mq=10) == 1   # more than 9 tokens
     assert _step(lib, "inkling_decode_step_host", ns=-1) == 1
+
+
+def test_prefill_fp8_host_checks(lib):
+    ws = lib.inkling_rel_attn_prefill_fp8_workspace_size
+    one = ws(1, 2, 4, 100, 500, 0)
+    assert one >= 2 * 4 * 2 * 128 * 128 * 2          # four visible pages of K and V, 2 heads
+    assert ws(1, 2, 4, 100, 500, 100) < one          # a window bounds the visible pages
+    f = lib.inkling_rel_attn_prefill_fp8
+    ok = dict(q=FAKE, k=FAKE, v=FAKE, ks=0.5, vs=0.5, bt=FAKE, maxb=4, cu=FAKE, sl=FAKE,
+              bias=FAKE, R=64, scale=0.1, window=0, out=FAKE, odt=0, lse=None, B=1, T=10, Hq=4,
+              Hkv=2, nb=4, mq=10, msl=500, ws=None, wsb=0, st=None, stream=None)
+
+    def call(**over):
+        a = dict(ok)
+        a.update(over)
+        return f(*a.values())
+    assert call(ks=0.0) == 1
+    assert call(vs=float("inf")) == 1
+    assert call(Hq=5) == 1
+    assert call() == 7                                # no workspace
+    assert call(ws=FAKE, wsb=16) == 7

@@ -136,3 +136,71 @@ def test_decode_fp8_rejects_bad_scale(ink):
         ink.rel_attn_decode_fp8(c.q, c.k_cache, c.v_cache, c.block_table, c.cu_q_lens,
                                 c.seq_lens, c.bias, k_scale=0.0, v_scale=1.0, scale=spec.scale,
                                 window=0, max_q_len=9, max_seq_len=spec.max_seq_len, out=out)
+
+
+PREFILL_CASES = {
+    "ragged": W.small(q_lens=(150, 37, 0, 300), seq_lens=(150, 200, 40, 300), hq=4, hkv=2, r=64),
+    "window_100": W.small(q_lens=(400, 129), seq_lens=(600, 129), hq=4, hkv=1, r=256, window=100),
+    "chunked_gqa4": W.small(q_lens=(200, 9, 130), seq_lens=(457, 300, 130), hq=8, hkv=2, r=100),
+}
+
+
+def _prefill_both(ink, spec, seed, ks, vs, nan_tail=False, out_dtype=torch.float32):
+    c = _fp8_case(spec, seed, ks, vs)
+    if nan_tail:
+        for b, L in enumerate(spec.seq_lens):
+            if L % 128:
+                blk = int(c.block_table[b, (L - 1) // 128])
+                c.k_cache[blk, :, L % 128:, :] = 0x7F
+                c.v_cache[blk, :, L % 128:, :] = 0x7F
+    g, _, _, _ = _sconv_both(ink, c, ks, vs)
+    out = torch.empty(spec.total_q, spec.hq, 128, dtype=out_dtype, device="cuda")
+    lse = torch.empty(spec.total_q, spec.hq, dtype=torch.float32, device="cuda")
+    st = _status()
+    ink.rel_attn_prefill_fp8(g.q, g.k_cache, g.v_cache, g.block_table, g.cu_q_lens, g.seq_lens,
+                             g.bias, k_scale=ks, v_scale=vs, scale=spec.scale,
+                             window=spec.window, max_q_len=spec.max_q_len,
+                             max_seq_len=spec.max_seq_len, out=out, lse=lse, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0, ink.status_string(int(st.item()))
+    ref, ref_lse = oracle.rel_attn_fp8(c.q, g.k_cache.cpu(), g.v_cache.cpu(), ks, vs,
+                                       c.block_table, c.cu_q_lens, c.seq_lens, c.bias,
+                                       scale=spec.scale, window=spec.window)
+    return out, lse, ref, ref_lse
+
+
+@pytest.mark.parametrize("name", sorted(PREFILL_CASES))
+@pytest.mark.parametrize("ks,vs", [(K_SCALE, V_SCALE), (0.1, 0.07)])
+def test_prefill_fp8_matches_oracle(ink, name, ks, vs):
+    """Prefill over E4M3 caches (pages widened to bf16 exactly, k_scale in the logit scale,
+    v_scale on the output) against the oracle's attention over the same codes."""
+    out, lse, ref, ref_lse = _prefill_both(ink, PREFILL_CASES[name], 87, ks, vs)
+    got = out.double().cpu().numpy()
+    assert np.isfinite(got).all()
+    err = np.abs(got - ref)
+    assert err.max() <= MAX_ABS, f"max |err| {err.max():.3e}"
+    assert err.mean() <= MEAN_ABS, f"mean |err| {err.mean():.3e}"
+    assert np.abs(lse.double().cpu().numpy() - ref_lse).max() <= LSE_ABS
+
+
+def test_prefill_fp8_ignores_stale_nan_slots(ink):
+    out, _, ref, _ = _prefill_both(ink, PREFILL_CASES["ragged"], 88, K_SCALE, V_SCALE,
+                                   nan_tail=True)
+    got = out.double().cpu().numpy()
+    assert np.isfinite(got).all()
+    assert np.abs(got - ref).max() <= MAX_ABS
+
+
+def test_prefill_fp8_workspace_too_small(ink):
+    spec = PREFILL_CASES["ragged"]
+    c = _fp8_case(spec, seed=89).to("cuda")
+    out = torch.empty(spec.total_q, spec.hq, 128, dtype=torch.float32, device="cuda")
+    need = ink.prefill_fp8_workspace_size(spec.batch, spec.hkv, c.block_table.shape[1],
+                                          spec.max_q_len, spec.max_seq_len, spec.window)
+    ws = torch.empty(need - 16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(ink.InklingError) as e:
+        ink.rel_attn_prefill_fp8(c.q, c.k_cache, c.v_cache, c.block_table, c.cu_q_lens,
+                                 c.seq_lens, c.bias, k_scale=K_SCALE, v_scale=V_SCALE,
+                                 scale=spec.scale, window=0, max_q_len=spec.max_q_len,
+                                 max_seq_len=spec.max_seq_len, out=out, workspace=ws)
+    assert e.value.code == 7
