@@ -173,8 +173,8 @@ class ClockSampler:
 # taken on: when that source has changed since, the figure no longer applies and the line
 # reports null.
 TRAFFIC = {
-    (2, None): ("prefill.cu", "f9c989910fdf43d9300961c5faa69cd49f25df2849c5f71b2e0df68d618f8bca",
-                613.3e6),
+    (2, None): ("prefill.cu", "d31d6f8e751e8228fc8da767e6fc115591a23f4a4c322f748ccb23ef12e50c27",
+                611.4e6),
     (5, "n1"): ("decode.cu", "cc12c06b99a34b1014eef848ca26221944e8bdd7ff3ac96e9a0f814361e0669d",
                 4301.1e6),
 }
