@@ -345,6 +345,19 @@ INKLING_API int inkling_decode_step_host(
     int32_t *dev_status, inkling_stream_t stream, inkling_stream_t h2d_stream,
     inkling_stream_t d2h_stream);
 
+/*
+ * inkling_selftest_bounded_wait — checks, on the device, the bounded waits that every
+ * pipeline kernel uses (their failure detection).  `ctas` CTAs each wait, with the
+ * kernels' own wait, on a barrier that nothing arrives on.  mode 0: every wait must give
+ * up after its cycle budget (about 2 s); dev_status becomes INKLING_ERR_TIMEOUT and
+ * *dev_gave_up counts the waits that gave up.  mode 1: CTA 0 first writes
+ * INKLING_ERR_BAD_INPUT to dev_status, and the other waits must see it and give up within
+ * about a millisecond.  dev_status and dev_gave_up are device int32s the caller zeroes.
+ * Nothing faults or hangs; the context stays usable afterwards.
+ */
+INKLING_API int inkling_selftest_bounded_wait(int32_t mode, int32_t ctas, int32_t *dev_status,
+                                              int32_t *dev_gave_up, inkling_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -345,3 +345,13 @@ def decode_step_host(q_host, k_raw_host, v_raw_host, out_host, staging, cu_q_len
                   q_dev.shape[0], q_dev.shape[1], hkv, k_cache.shape[0], int(max_q_len),
                   int(max_seq_len), int(num_splits), workspace, ws_bytes, int(chunks),
                   dev_status, _stream(stream), h2d_stream.cuda_stream, d2h_stream.cuda_stream)
+
+
+def selftest_bounded_wait(mode: int, ctas: int, dev_status: torch.Tensor,
+                          gave_up: torch.Tensor, stream=None) -> None:
+    """inkling_selftest_bounded_wait: CTAs wait on a barrier nothing arrives on; mode 0
+    must time out (about 2 s), mode 1 must stop early on another CTA's error."""
+    dev = _check_cuda(dev_status, gave_up)
+    with torch.cuda.device(dev):
+        _lib.call("inkling_selftest_bounded_wait", int(mode), int(ctas), dev_status, gave_up,
+                  _stream(stream))

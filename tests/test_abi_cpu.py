@@ -175,3 +175,10 @@ def test_prefill_fp8_host_checks(lib):
     assert call(Hq=5) == 1
     assert call() == 7                                # no workspace
     assert call(ws=FAKE, wsb=16) == 7
+
+
+def test_selftest_host_checks(lib):
+    f = lib.inkling_selftest_bounded_wait
+    assert f(2, 1, FAKE, FAKE, None) == 1
+    assert f(0, 0, FAKE, FAKE, None) == 1
+    assert f(0, 1, None, FAKE, None) == 1
