@@ -352,16 +352,17 @@ def run_ours(args, ws, rank, local):
     d2h = host_out.numel() * host_out.element_size()
     cu_host = g.cu_q_lens.cpu()
     up, down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-    # prefill: one group per sequence, up to four.  decode: one group (its copies are a few
+    # prefill: eight groups (a long sequence is cut into pieces of whole query tiles, so
+    # the 64K prefill overlaps its copies too).  decode: one group (its copies are a few
     # MB, and cutting the batch gives each group its own tail of ragged lengths: two groups
     # measured 1.66 ms on the full MTP decode against 1.41 ms for one)
-    e2e_chunks = 1 if decode else min(4, spec.batch)
+    e2e_chunks = 1 if decode else 8
     if fp8:
         e2e_path = (f"copies + sconv_kv_fp8 + rel_attn_{'decode' if decode else 'prefill'}_fp8, "
                     "serial")
     else:
         e2e_path = (f"inkling_{'decode' if decode else 'prefill'}_step_host, "
-                    f"{e2e_chunks} groups of sequences")
+                    f"{e2e_chunks} groups" + ("" if decode else " (sequences cut into query-tile pieces)"))
 
     def host_step():
         step_args = (host_in[0], host_in[1], host_in[2], host_out, (*dev_in, out), cu_host,

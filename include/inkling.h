@@ -319,7 +319,12 @@ INKLING_API int inkling_rel_attn_decode_noalloc(
  * once everything is enqueued, and out_host is complete when `stream` reaches that point.
  * Host-side argument errors are returned before anything is enqueued; an error from one
  * group's launch stops the enqueueing and is returned (earlier groups stay enqueued).
- * Device-side errors land in dev_status as for the separate calls.  The decode form takes
+ * Device-side errors land in dev_status as for the separate calls.  The prefill form may
+ * also cut a sequence with more than its group's share of tokens into pieces of whole
+ * 128-token query tiles, each computed as a chunked prefill of that sequence (outputs
+ * bit-identical to the uncut call); it does so only when given dev_scratch, device
+ * memory for 4 * chunks int32 lengths (NULL: groups of whole sequences only).  The decode
+ * form takes
  * a workspace sized for all B sequences (inkling_rel_attn_decode_workspace_size); the
  * groups reuse it one after another on `stream`, all with the split count the whole batch
  * would get (num_splits = 0) or the one given.
@@ -331,8 +336,9 @@ INKLING_API int inkling_prefill_step_host(
     const int64_t *slot_mapping, void *k_cache, void *v_cache, const int32_t *block_table,
     int32_t max_blocks, const int32_t *seq_lens, const float *bias, int32_t R, float scale,
     int32_t window, int32_t out_dtype, float *lse, int32_t B, int32_t T, int32_t Hq,
-    int32_t Hkv, int64_t num_blocks, int32_t max_q_len, int32_t chunks, int32_t *dev_status,
-    inkling_stream_t stream, inkling_stream_t h2d_stream, inkling_stream_t d2h_stream);
+    int32_t Hkv, int64_t num_blocks, int32_t max_q_len, int32_t chunks, int32_t *dev_scratch,
+    int32_t *dev_status, inkling_stream_t stream, inkling_stream_t h2d_stream,
+    inkling_stream_t d2h_stream);
 INKLING_API int inkling_decode_step_host(
     const void *q_host, const void *k_raw_host, const void *v_raw_host, void *out_host,
     void *q_dev, void *k_raw_dev, void *v_raw_dev, void *out_dev, const int32_t *cu_q_lens_host,

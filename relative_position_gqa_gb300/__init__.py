@@ -296,25 +296,32 @@ def _step_args(q_host, k_raw_host, v_raw_host, out_host, staging, cu_q_lens_host
 def prefill_step_host(q_host, k_raw_host, v_raw_host, out_host, staging, cu_q_lens_host, w_k,
                       w_v, sconv_state, cu_q_lens, slot_mapping, k_cache, v_cache, block_table,
                       seq_lens, bias, *, scale: float, window: int, max_q_len: int,
-                      h2d_stream, d2h_stream, chunks: int = 4, lse=None, dev_status=None,
+                      h2d_stream, d2h_stream, chunks: int = 4, split_sequences: bool = True,
+                      scratch: Optional[torch.Tensor] = None, lse=None, dev_status=None,
                       stream=None) -> None:
     """inkling_prefill_step_host: sconv_kv + rel_attn_prefill for a step whose Q, raw K/V
     and output live in page-locked host memory.  `staging` = (q_dev, k_raw_dev, v_raw_dev,
     out_dev), device buffers of the host buffers' shapes; the copies of one group of
-    sequences run on h2d_stream / d2h_stream while another group is computed."""
+    sequences run on h2d_stream / d2h_stream while another group is computed.  With
+    split_sequences, a long sequence may be cut into pieces of whole query tiles (its
+    lengths go to `scratch`, 4 * chunks int32 on the device, allocated when omitted)."""
     dev, out_dtype, cu_host = _step_args(q_host, k_raw_host, v_raw_host, out_host, staging,
                                          cu_q_lens_host, w_k, w_v, sconv_state, cu_q_lens,
                                          slot_mapping, k_cache, v_cache, block_table, seq_lens,
                                          bias, lse, dev_status)
     q_dev, k_dev, v_dev, out_dev = staging
     with torch.cuda.device(dev):
+        if split_sequences and scratch is None:
+            scratch = torch.empty(4 * max(int(chunks), 1), dtype=torch.int32, device=dev)
+        if not split_sequences:
+            scratch = None
         _lib.call("inkling_prefill_step_host", q_host, k_raw_host, v_raw_host, out_host, q_dev,
                   k_dev, v_dev, out_dev, cu_host, w_k, w_v, sconv_state, cu_q_lens,
                   slot_mapping, k_cache, v_cache, block_table, block_table.shape[1], seq_lens,
                   bias, bias.shape[1], float(scale), int(window), out_dtype, lse,
                   cu_q_lens.shape[0] - 1, q_dev.shape[0], q_dev.shape[1], k_cache.shape[1],
-                  k_cache.shape[0], int(max_q_len), int(chunks), dev_status, _stream(stream),
-                  h2d_stream.cuda_stream, d2h_stream.cuda_stream)
+                  k_cache.shape[0], int(max_q_len), int(chunks), scratch, dev_status,
+                  _stream(stream), h2d_stream.cuda_stream, d2h_stream.cuda_stream)
 
 
 def decode_step_host(q_host, k_raw_host, v_raw_host, out_host, staging, cu_q_lens_host, w_k,

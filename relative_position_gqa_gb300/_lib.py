@@ -36,7 +36,7 @@ SIGNATURES = {
                                         I32, I32, I32, I64, I32, I32, I32, P, P],
     "inkling_prefill_step_host": [P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, I32, P, P,
                                   I32, F32, I32, I32, P, I32, I32, I32, I32, I64, I32, I32, P,
-                                  P, P, P],
+                                  P, P, P, P],
     "inkling_decode_step_host": [P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, I32, P, P,
                                  I32, F32, I32, I32, P, I32, I32, I32, I32, I64, I32, I32, I32,
                                  P, SZ, I32, P, P, P, P],

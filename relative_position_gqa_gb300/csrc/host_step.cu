@@ -18,6 +18,7 @@ struct Group {
   int b0, b1;      // sequences [b0, b1)
   int64_t t0, t1;  // their new tokens [t0, t1)
   int max_n;       // longest n_b in the group
+  bool piece;      // a run of one sequence's new tokens (b1 == b0 + 1), not all of them
 };
 
 // Groups of whole sequences with about T / chunks new tokens each: a group closes once the
@@ -32,12 +33,60 @@ std::vector<Group> make_groups(const int32_t* cu, int B, int chunks) {
     const int k = (int)g.size() + 1;  // this group's index + 1
     const bool last = b + 1 == B;
     if (last || (k < chunks && (int64_t)cu[b + 1] * chunks >= T * k)) {
-      g.push_back(Group{b0, b + 1, cu[b0], cu[b + 1], max_n});
+      g.push_back(Group{b0, b + 1, cu[b0], cu[b + 1], max_n, false});
       b0 = b + 1;
       max_n = 0;
     }
   }
   return g;
+}
+
+// Prefill groups that may also cut a sequence: a sequence with more new tokens than a
+// group's share becomes pieces of whole 128-token query tiles (so that every query tile,
+// and with it the order of its sums, is the one the uncut call computes).  At most
+// `chunks` pieces in all (their lengths need one scratch slot each); past that budget a
+// long sequence stays whole.
+std::vector<Group> make_prefill_groups(const int32_t* cu, int B, int chunks) {
+  const int64_t T = cu[B];
+  const int64_t share = ((T + chunks - 1) / chunks + 127) / 128 * 128;
+  std::vector<Group> g;
+  int b0 = -1, max_n = 0, pieces = 0;
+  auto flush = [&](int b_end) {
+    if (b0 >= 0) g.push_back(Group{b0, b_end, cu[b0], cu[b_end], max_n, false});
+    b0 = -1;
+    max_n = 0;
+  };
+  for (int b = 0; b < B; ++b) {
+    const int n = cu[b + 1] - cu[b];
+    const int need = (int)((n + share - 1) / share);
+    if (n > share && pieces + need <= chunks) {
+      pieces += need;
+      flush(b);
+      for (int64_t r = 0; r < n; r += share) {
+        const int64_t e = r + share < n ? r + share : n;
+        g.push_back(Group{b, b + 1, cu[b] + r, cu[b] + e, (int)(e - r), true});
+      }
+      continue;
+    }
+    if (b0 < 0) b0 = b;
+    if (n > max_n) max_n = n;
+    if ((int64_t)(cu[b + 1] - cu[b0]) >= share) flush(b + 1);
+  }
+  flush(B);
+  return g;
+}
+
+// The lengths of a piece of sequence b, as the calls read them: cu = {0, rel1 - rel0} and
+// the sequence's length at the piece's last token.
+__global__ void piece_lens_kernel(const int32_t* cu_q_lens, const int32_t* seq_lens, int b,
+                                  int rel0, int rel1, int32_t* out) {
+  if (threadIdx.x == 0) {
+    const int n = cu_q_lens[b + 1] - cu_q_lens[b];
+    out[0] = 0;
+    out[1] = rel1 - rel0;
+    out[2] = seq_lens[b] - n + rel1;
+    out[3] = 0;
+  }
 }
 
 struct Events {
@@ -159,8 +208,9 @@ int inkling_prefill_step_host(
     const int64_t* slot_mapping, void* k_cache, void* v_cache, const int32_t* block_table,
     int32_t max_blocks, const int32_t* seq_lens, const float* bias, int32_t R, float scale,
     int32_t window, int32_t out_dtype, float* lse, int32_t B, int32_t T, int32_t Hq,
-    int32_t Hkv, int64_t num_blocks, int32_t max_q_len, int32_t chunks, int32_t* dev_status,
-    inkling_stream_t stream, inkling_stream_t h2d_stream, inkling_stream_t d2h_stream) {
+    int32_t Hkv, int64_t num_blocks, int32_t max_q_len, int32_t chunks, int32_t* dev_scratch,
+    int32_t* dev_status, inkling_stream_t stream, inkling_stream_t h2d_stream,
+    inkling_stream_t d2h_stream) {
   HostRows h;
   std::vector<Group> groups;
   int rc = prepare(q_host, k_raw_host, v_raw_host, out_host, q_dev, k_raw_dev, v_raw_dev,
@@ -170,8 +220,35 @@ int inkling_prefill_step_host(
   if (!w_k || !w_v || !sconv_state || !cu_q_lens || !slot_mapping || !block_table || !seq_lens)
     return INKLING_ERR_INVALID_ARG;
   if (B == 0 || T == 0) return INKLING_OK;
+  // with scratch for their lengths, long sequences may be cut into pieces
+  if (dev_scratch != nullptr) groups = make_prefill_groups(cu_q_lens_host, B, chunks);
   const size_t state_seq = (size_t)2 * 3 * Hkv * 128 * 2;  // bytes of one sequence's state
+  const size_t kv_row = (size_t)Hkv * 128 * 2;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int piece = 0;
   auto launch = [&](const Group& g) {
+    if (g.piece) {
+      // one run of sequence b's tokens: pointers start at its first row, and the lengths
+      // come from a scratch slot (cu = {0, rows}, the sequence's length at its last row)
+      int32_t* lens = dev_scratch + 4 * piece++;  // piece < chunks by construction
+      const int b = g.b0;
+      const int rel0 = (int)(g.t0 - cu_q_lens_host[b]), rel1 = (int)(g.t1 - cu_q_lens_host[b]);
+      const int rows = rel1 - rel0;
+      piece_lens_kernel<<<1, 32, 0, st>>>(cu_q_lens, seq_lens, b, rel0, rel1, lens);
+      if (cudaGetLastError() != cudaSuccess) return (int)INKLING_ERR_CUDA;
+      int r = inkling_sconv_kv(static_cast<uint8_t*>(k_raw_dev) + g.t0 * kv_row,
+                               static_cast<uint8_t*>(v_raw_dev) + g.t0 * kv_row, w_k, w_v,
+                               static_cast<uint8_t*>(sconv_state) + b * state_seq, lens,
+                               slot_mapping + g.t0, k_cache, v_cache, 1, rows, Hkv, num_blocks,
+                               rows, dev_status, stream);
+      if (r != INKLING_OK) return r;
+      return inkling_rel_attn_prefill(static_cast<uint8_t*>(q_dev) + g.t0 * h.q_row, k_cache,
+                                      v_cache, block_table + (size_t)b * max_blocks, max_blocks,
+                                      lens, lens + 2, bias, R, scale, window,
+                                      static_cast<uint8_t*>(out_dev) + g.t0 * h.out_row,
+                                      out_dtype, lse ? lse + g.t0 * Hq : nullptr, 1, rows, Hq,
+                                      Hkv, num_blocks, rows, dev_status, stream);
+    }
     const int nb = g.b1 - g.b0;
     int r = inkling_sconv_kv(k_raw_dev, v_raw_dev, w_k, w_v,
                              static_cast<uint8_t*>(sconv_state) + g.b0 * state_seq,

@@ -133,8 +133,10 @@ def _step(lib, name, **over):
              slot=FAKE, kc=FAKE, vc=FAKE, bt=FAKE, maxb=4, sl=FAKE, bias=FAKE, R=64, scale=0.1,
              window=0, odt=0, lse=None, B=2, T=10, Hq=4, Hkv=2, nb=4, mq=5)
     if name == "inkling_decode_step_host":
-        a.update(msl=500, ns=0, ws=None, wsb=0)
-    a.update(chunks=2, ds=None, s=None, up=0x20000, down=0x30000)
+        a.update(msl=500, ns=0, ws=None, wsb=0, chunks=2)
+    else:
+        a.update(chunks=2, scratch=None)
+    a.update(ds=None, s=None, up=0x20000, down=0x30000)
     a.update(over)
     rc = getattr(lib, name)(*a.values())
     del cu
