@@ -356,7 +356,7 @@ def run_ours(args, ws, rank, local):
     # the 64K prefill overlaps its copies too).  decode: one group (its copies are a few
     # MB, and cutting the batch gives each group its own tail of ragged lengths: two groups
     # measured 1.66 ms on the full MTP decode against 1.41 ms for one)
-    e2e_chunks = 1 if decode else 8
+    e2e_chunks = args.e2e_chunks if args.e2e_chunks > 0 else (1 if decode else 8)
     if fp8:
         e2e_path = (f"copies + sconv_kv_fp8 + rel_attn_{'decode' if decode else 'prefill'}_fp8, "
                     "serial")
@@ -660,6 +660,8 @@ def main():
     ap.add_argument("--ref-seconds", type=float, default=6.0,
                     help="oracle seconds per reference step / for the cpu_baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-chunks", type=int, default=0,
+                    help="groups for the end-to-end host-buffer step (0: 8 for prefill, 1 for decode)")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per launch of the dominant kernel from an ncu capture")
     args = ap.parse_args()
