@@ -204,3 +204,42 @@ def test_prefill_fp8_workspace_too_small(ink):
                                  scale=spec.scale, window=0, max_q_len=spec.max_q_len,
                                  max_seq_len=spec.max_seq_len, out=out, workspace=ws)
     assert e.value.code == 7
+
+
+@pytest.mark.parametrize("seed", range(300, 306))
+def test_fp8_random_shapes(ink, seed):
+    """Seeded random batches for the FP8 cache: the conv into E4M3 pages, then the decode
+    (even seeds) or the prefill (odd seeds) against the oracle over the same codes."""
+    import random
+    rnd = random.Random(seed)
+    decode = seed % 2 == 0
+    hkv = rnd.choice([1, 2])
+    g = rnd.choice([1, 4, 8])
+    B = rnd.randint(1, 4)
+    q_lens = [rnd.randint(1, 9) if decode else rnd.choice([1, 60, 130, 257]) for _ in range(B)]
+    seq_lens = [n + rnd.choice([0, 3, 128, 400]) for n in q_lens]
+    spec = W.small(name=f"fp8rand{seed}", q_lens=q_lens, seq_lens=seq_lens, hq=hkv * g, hkv=hkv,
+                   r=rnd.choice([5, 200, 1024]), window=rnd.choice([0, 50]))
+    ks, vs = rnd.choice([(K_SCALE, V_SCALE), (0.1, 0.07)])
+    if decode:
+        c = _fp8_case(spec, seed, ks, vs)
+        g_, _, _, _ = _sconv_both(ink, c, ks, vs)
+        out = torch.empty(spec.total_q, spec.hq, 128, dtype=torch.float32, device="cuda")
+        st = _status()
+        ink.rel_attn_decode_fp8(g_.q, g_.k_cache, g_.v_cache, g_.block_table, g_.cu_q_lens,
+                                g_.seq_lens, g_.bias, k_scale=ks, v_scale=vs, scale=spec.scale,
+                                window=spec.window, max_q_len=spec.max_q_len,
+                                max_seq_len=spec.max_seq_len, out=out, num_splits=seed % 3,
+                                dev_status=st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0, ink.status_string(int(st.item()))
+        ref, _ = oracle.rel_attn_fp8(c.q, g_.k_cache.cpu(), g_.v_cache.cpu(), ks, vs,
+                                     c.block_table, c.cu_q_lens, c.seq_lens, c.bias,
+                                     scale=spec.scale, window=spec.window)
+    else:
+        out, _, ref, _ = _prefill_both(ink, spec, seed, ks, vs)
+    got = out.double().cpu().numpy()
+    assert np.isfinite(got).all()
+    err = np.abs(got - ref)
+    assert err.max() <= MAX_ABS, f"max |err| {err.max():.3e}"
+    assert err.mean() <= MEAN_ABS, f"mean |err| {err.mean():.3e}"
