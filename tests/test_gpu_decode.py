@@ -128,3 +128,20 @@ def test_decode_rejects_more_than_nine_tokens(ink):
                             g.bias, scale=spec.scale, window=0, max_q_len=10, max_seq_len=100,
                             out=out)
     assert e.value.code == 1
+
+
+@pytest.mark.parametrize("num_splits", [1, 3])
+def test_decode_bad_block_reported(ink, num_splits):
+    """A page id past the cache in a sequence's visible range comes back as
+    INKLING_ERR_BAD_BLOCK, with no access made through it."""
+    spec = CASES["mixed_n"]
+    g = W.make_case(spec, seed=31, device="cuda")
+    st = _status()
+    gpu_sconv(ink, g, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    L = spec.seq_lens[3]
+    g.block_table[3, (L - 1) // 128 - 2] = g.num_blocks  # inside sequence 3's range
+    gpu_attn(ink, g, st, decode=True, num_splits=num_splits)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 5  # INKLING_ERR_BAD_BLOCK

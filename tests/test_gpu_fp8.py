@@ -243,3 +243,19 @@ def test_fp8_random_shapes(ink, seed):
     err = np.abs(got - ref)
     assert err.max() <= MAX_ABS, f"max |err| {err.max():.3e}"
     assert err.mean() <= MEAN_ABS, f"mean |err| {err.mean():.3e}"
+
+
+def test_prefill_fp8_bad_block_reported(ink):
+    """A page id past the cache stops the widening of that page and is reported; the
+    prefill then reads only pages of the pool."""
+    spec = PREFILL_CASES["ragged"]
+    c = _fp8_case(spec, seed=90).to("cuda")
+    c.block_table[0, 0] = c.k_cache.shape[0] + 3
+    out = torch.empty(spec.total_q, spec.hq, 128, dtype=torch.float32, device="cuda")
+    st = _status()
+    ink.rel_attn_prefill_fp8(c.q, c.k_cache, c.v_cache, c.block_table, c.cu_q_lens, c.seq_lens,
+                             c.bias, k_scale=K_SCALE, v_scale=V_SCALE, scale=spec.scale,
+                             window=0, max_q_len=spec.max_q_len, max_seq_len=spec.max_seq_len,
+                             out=out, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 5  # INKLING_ERR_BAD_BLOCK
