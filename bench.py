@@ -43,6 +43,14 @@ METRIC = "prefill attn TFLOP/s and decode KV-read GB/s on 1 GB300; % of roofline
 L2_FLUSH_BYTES = 512 << 20
 
 
+def max_over_ranks(values, ws: int, device) -> list:
+    """Per-rank timings -> their maximum over all ranks (every rank gets the result)."""
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    if ws > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return t.tolist()
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -398,11 +406,8 @@ def run_ours(args, ws, rank, local):
         raise RuntimeError(f"device status {ink.status_string(int(status.item()))}")
     e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_ev) / len(e2e_ev)
 
-    # max over ranks
-    t = torch.tensor([step_ms, attn_ms, e2e_ms, sconv_ms], dtype=torch.float64, device=dev)
-    if ws > 1:
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-    step_ms, attn_ms, e2e_ms, sconv_ms = t.tolist()
+    step_ms, attn_ms, e2e_ms, sconv_ms = max_over_ranks([step_ms, attn_ms, e2e_ms, sconv_ms],
+                                                        ws, dev)
 
     peaks, peak_src = measured_peaks()
     if decode:
@@ -509,10 +514,7 @@ def run_dense(args, ws, rank, local):
             e2e_ev.append((a, b))
     torch.cuda.synchronize()
     e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_ev) / len(e2e_ev)
-    t = torch.tensor([step_ms, e2e_ms], dtype=torch.float64, device=dev)
-    if ws > 1:
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-    step_ms, e2e_ms = t.tolist()
+    step_ms, e2e_ms = max_over_ranks([step_ms, e2e_ms], ws, dev)
     peaks, peak_src = measured_peaks()
     work = dense_bytes(DENSE_Q_LENS, DENSE_C)
     achieved = work / (step_ms * 1e-3) / 1e9

@@ -1,0 +1,53 @@
+"""The N > 1 path of bench.py on the CPU with the gloo backend (world size 2): the timing
+reduction takes the maximum over ranks, and under torchrun only rank 0 prints the
+reference arm's single JSON line while the other rank exits cleanly.  The attention path
+itself runs as independent replicas (no collective on its data path)."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, ws, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=ws)
+    sys.path.insert(0, ROOT)
+    import bench
+    got = bench.max_over_ranks([1.0 + rank, 10.0 - rank, 3.0 * rank], ws, "cpu")
+    out[rank] = got
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_gloo():
+    ws = 2
+    mgr = mp.Manager()
+    out = mgr.dict()
+    mp.start_processes(_worker, args=(ws, _free_port(), out), nprocs=ws, start_method="spawn")
+    assert out[0] == out[1] == [2.0, 10.0, 3.0]
+
+
+def test_reference_arm_under_torchrun_two_ranks():
+    port = _free_port()
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), "bench.py", "--gpus", "2",
+           "--impl", "reference", "--steps", "1", "--warmup", "3", "--ref-seconds", "0.3"]
+    r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
