@@ -185,6 +185,8 @@ TRAFFIC = {
                 611.4e6),
     (5, "n1"): ("decode.cu", "cc12c06b99a34b1014eef848ca26221944e8bdd7ff3ac96e9a0f814361e0669d",
                 4301.1e6),
+    (5, "n9_256k"): ("decode.cu", "cc12c06b99a34b1014eef848ca26221944e8bdd7ff3ac96e9a0f814361e0669d",
+                     1080.2e6),
 }
 
 
@@ -656,7 +658,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5, 6])
-    ap.add_argument("--variant", default=None, help="mtp_decode: swa|full; decode_1m: n1|n9")
+    ap.add_argument("--variant", default=None, help="mtp_decode: swa|full; decode_1m: n1|n9 (n1_256k|n9_256k: quarter length)")
     ap.add_argument("--kv", choices=["bf16", "fp8"], default="bf16",
                     help="KV cache type for the decode workloads")
     ap.add_argument("--ref-seconds", type=float, default=6.0,

@@ -97,9 +97,13 @@ def config(n: int, *, variant: Optional[str] = None) -> Spec:
                     hkv=4, r=8192, window=window, bias_std=0.5, q_lens=[9] * 64,
                     seq_lens=lens, history_random=True, state_random=True)
     if n == 5:
-        nq = 1 if variant in (None, "n1") else 9
-        return Spec(name=f"decode_1m_n{nq}", batch=1, hq=64, hkv=8, r=8192, window=0,
-                    bias_std=0.5, q_lens=[nq], seq_lens=[1 << 20], history_random=True,
+        # n1 / n9: the 1M-token sequence; n1_256k / n9_256k: a quarter of it (1 GB of K/V),
+        # small enough for multi-pass profiler captures of the same kernel
+        nq = 1 if variant in (None, "n1", "n1_256k") else 9
+        L = (1 << 18) if variant in ("n1_256k", "n9_256k") else (1 << 20)
+        tag = "256k" if L == (1 << 18) else "1m"
+        return Spec(name=f"decode_{tag}_n{nq}", batch=1, hq=64, hkv=8, r=8192, window=0,
+                    bias_std=0.5, q_lens=[nq], seq_lens=[L], history_random=True,
                     state_random=True)
     raise ValueError(f"no workload {n}")
 
