@@ -41,6 +41,7 @@ import workloads as W  # noqa: E402
 
 METRIC = "prefill attn TFLOP/s and decode KV-read GB/s on 1 GB300; % of roofline"
 L2_FLUSH_BYTES = 512 << 20
+REF_TOTAL_S = 120.0  # oracle seconds for a whole --impl reference run
 L2_NOTE = ("flushed between timed steps: 512 MB written, then read back (the read retires the "
            "write's dirty lines before the timed region, so the kernel is not charged for their "
            "write-back)")
@@ -633,9 +634,12 @@ def run_reference(args, ws, rank):
     per_step = []
     desc = None
     sspec, case = oracle_case(spec, seed=args.workload)
+    # each step a bounded sample: about two minutes of oracle time for the whole run,
+    # at most --ref-seconds a step
+    per_step_s = max(0.2, min(args.ref_seconds, REF_TOTAL_S / (args.warmup + args.steps)))
     for i in range(args.warmup + args.steps):
         pairs, t_attn, t_sconv, nrows, cores, sspec = oracle_sample(
-            sspec, case, budget_s=args.ref_seconds, seed=args.workload + i)
+            sspec, case, budget_s=per_step_s, seed=args.workload + i)
         if i >= args.warmup:
             per_step.append((pairs, t_attn, nrows))
         desc = (f"fp64 C oracle on {cores} host threads: {nrows} random query rows x "
