@@ -251,10 +251,13 @@ def run_ours(args, ws, rank, local):
     flush_sink = torch.empty(1, dtype=torch.float32, device=dev)
     ws_bytes = 0
     workspace = None
+    plan = None
     if decode:
         ws_bytes = ink.decode_workspace_size(spec.batch, spec.hq, spec.hkv, spec.max_q_len,
                                              spec.max_seq_len, spec.window)
         workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+        plan = ink.decode_plan(spec.batch, spec.hq, spec.hkv, spec.max_q_len, spec.max_seq_len,
+                               spec.window)
     elif fp8:  # the widened bf16 pages of the FP8 prefill
         ws_bytes = ink.prefill_fp8_workspace_size(spec.batch, spec.hkv, g.block_table.shape[1],
                                                   spec.max_q_len, spec.max_seq_len, spec.window)
@@ -459,10 +462,11 @@ def run_ours(args, ws, rank, local):
                    "global_batch": spec.batch * ws,
                    "seq_len": spec.max_seq_len, "parallelism": f"replicas x{ws}",
                    "l2": L2_NOTE,
-                   "attn_ms": round(attn_ms, 4), "sconv_ms": round(sconv_ms, 4)},
+                   "attn_ms": round(attn_ms, 4), "sconv_ms": round(sconv_ms, 4),
+                   **({"decode_plan": plan} if decode else {})},
         "e2e": {"value": round(e2e_value, 3), "unit": unit, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4), "path": e2e_path},
-        "gpu_launches": args.steps * (2 + (1 if (decode and ws_bytes > 0) or (fp8 and not decode)
+        "gpu_launches": args.steps * (2 + (1 if (decode and plan["merge"]) or (fp8 and not decode)
                                            else 0)),
         "roofline": roof,
         "clocks": clocks.summary(),

@@ -229,6 +229,21 @@ INKLING_API size_t inkling_rel_attn_decode_workspace_size(int32_t B, int32_t Hq,
                                               int32_t window, int32_t num_splits);
 
 /*
+ * inkling_rel_attn_decode_plan — how inkling_rel_attn_decode and
+ * inkling_rel_attn_decode_fp8 split the keys for these limits on the current device (the
+ * rule of the decode calls and of the workspace query).  plan: caller's array of 4 int32:
+ *   [0] splits per (sequence, KV head): the page ranges processed by separate CTAs;
+ *   [1] CTAs of the decode launch (splits x Hkv x B, saturating at INT32_MAX);
+ *   [2] pages per split;
+ *   [3] 1 when a merge kernel follows the decode kernel (more than one split), else 0.
+ * Returns INKLING_ERR_INVALID_ARG for bad limits (or a NULL plan), INKLING_ERR_CUDA when
+ * num_splits = 0 and no device is current.
+ */
+INKLING_API int inkling_rel_attn_decode_plan(int32_t B, int32_t Hq, int32_t Hkv, int32_t max_q_len,
+                                 int32_t max_seq_len, int32_t window, int32_t num_splits,
+                                 int32_t *plan);
+
+/*
  * inkling_rel_attn_decode — the same attention for decode steps of up to
  * INKLING_MAX_DECODE_Q (9) new tokens per sequence (MTP verify, blog "Model Architecture /
  * MTP"), with the keys of each sequence split into `num_splits` page ranges processed in

@@ -154,13 +154,22 @@ def decode_workspace_size(B: int, hq: int, hkv: int, max_q_len: int, max_seq_len
         return _lib.workspace_size(B, hq, hkv, max_q_len, max_seq_len, window, num_splits)
 
 
+def decode_plan(B: int, hq: int, hkv: int, max_q_len: int, max_seq_len: int, window: int,
+                num_splits: int = 0, device=None) -> dict:
+    """inkling_rel_attn_decode_plan: how the decode calls split the keys."""
+    with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
+        v = _lib.decode_plan(B, hq, hkv, max_q_len, max_seq_len, window, num_splits)
+    return {"num_splits": v[0], "ctas": v[1], "pages_per_split": v[2], "merge": bool(v[3])}
+
+
 def rel_attn_decode(q, k_cache, v_cache, block_table, cu_q_lens, seq_lens, bias, *,
                     scale: float, window: int, max_q_len: int, max_seq_len: int,
                     out: torch.Tensor, lse: Optional[torch.Tensor] = None, num_splits: int = 0,
                     workspace: Optional[torch.Tensor] = None, dev_status=None,
                     stream=None) -> None:
     """inkling_rel_attn_decode into `out`.  `workspace` is a caller-owned device buffer of
-    at least decode_workspace_size(...) bytes (allocated here when omitted)."""
+    at least decode_workspace_size(...) bytes (allocated here when omitted).  num_splits:
+    0 automatic, > 0 equal splits per (sequence, KV head) (decode_plan tells which)."""
     dev, out_dtype = _attn_common(q, k_cache, v_cache, block_table, cu_q_lens, seq_lens, bias,
                                   out, lse, dev_status)
     T, hq = q.shape[0], q.shape[1]

@@ -27,6 +27,7 @@ SIGNATURES = {
     "inkling_rel_attn_prefill_fp8": [P, P, P, F32, F32, P, I32, P, P, P, I32, F32, I32, P, I32,
                                      P, I32, I32, I32, I32, I64, I32, I32, P, SZ, P, P],
     "inkling_rel_attn_decode_workspace_size": [I32, I32, I32, I32, I32, I32, I32],
+    "inkling_rel_attn_decode_plan": [I32, I32, I32, I32, I32, I32, I32, P],
     "inkling_rel_attn_decode": [P, P, P, P, I32, P, P, P, I32, F32, I32, P, I32, P, I32, I32,
                                 I32, I32, I64, I32, I32, I32, P, SZ, P, P],
     "inkling_rel_attn_decode_fp8": [P, P, P, F32, F32, P, I32, P, P, P, I32, F32, I32, P, I32, P,
@@ -98,3 +99,11 @@ def call(name, *args):
 
 def workspace_size(*args) -> int:
     return int(load().inkling_rel_attn_decode_workspace_size(*[int(a) for a in args]))
+
+
+def decode_plan(*args) -> list:
+    plan = (ctypes.c_int32 * 4)()
+    rc = load().inkling_rel_attn_decode_plan(*[int(a) for a in args], plan)
+    if rc != 0:
+        raise InklingError("inkling_rel_attn_decode_plan", rc)
+    return list(plan)

@@ -293,6 +293,24 @@ size_t inkling_rel_attn_decode_workspace_size(int32_t B, int32_t Hq, int32_t Hkv
   return ink::decode_workspace_bytes(B, Hq, Hkv, max_q_len, sp.num_splits);
 }
 
+int inkling_rel_attn_decode_plan(int32_t B, int32_t Hq, int32_t Hkv, int32_t max_q_len,
+                                 int32_t max_seq_len, int32_t window, int32_t num_splits,
+                                 int32_t* plan) {
+  if (plan == nullptr || B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || max_q_len <= 0 ||
+      max_q_len > INKLING_MAX_DECODE_Q || max_seq_len <= 0 || window < 0 || num_splits < 0)
+    return INKLING_ERR_INVALID_ARG;
+  const int sms = num_splits > 0 ? 1 : num_sms_current();
+  if (sms <= 0) return INKLING_ERR_CUDA;
+  const ink::DecodeSplit sp =
+      ink::decode_split(B, Hkv, max_q_len, max_seq_len, window, num_splits, sms);
+  const long long grid = (long long)sp.num_splits * Hkv * B;
+  plan[0] = sp.num_splits;
+  plan[1] = (int32_t)(grid < 0x7fffffffLL ? grid : 0x7fffffffLL);
+  plan[2] = sp.pages_per_split;
+  plan[3] = sp.num_splits > 1 ? 1 : 0;
+  return INKLING_OK;
+}
+
 static int decode_entry(bool kv_fp8, float k_scale, float v_scale,
                         const void* q, const void* k_cache, const void* v_cache,
                             const int32_t* block_table, int32_t max_blocks,

@@ -93,6 +93,22 @@ def test_workspace_size_rule(lib):
     assert ws(1, 8, 1, 9, 100000, 0, 8) > two
 
 
+def test_decode_plan_rule(lib):
+    """The plan query follows the split rule: 8 pages in 3 splits are ranges of 3 pages
+    (3 + 3 + 2), 6 CTAs for 2 sequences; one split needs no merge."""
+    from relative_position_gqa_gb300 import _lib
+    assert _lib.decode_plan(2, 8, 1, 9, 1000, 0, 3) == [3, 6, 3, 1]
+    assert _lib.decode_plan(2, 8, 1, 9, 1000, 0, 1) == [1, 2, 8, 0]
+    # a 300-token window bounds the visible range to (300 + 8 + 127) // 128 + 1 = 4 pages
+    assert _lib.decode_plan(64, 32, 4, 9, 131072, 300, 2) == [2, 512, 2, 1]
+    for bad in (dict(mq=10), dict(ns=-1), dict(B=0)):
+        a = dict(B=2, Hq=8, Hkv=1, mq=9, msl=1000, w=0, ns=3)
+        a.update(bad)
+        with pytest.raises(_lib.InklingError) as e:
+            _lib.decode_plan(*a.values())
+        assert e.value.code == 1
+
+
 def test_dense_sconv_host_checks(lib):
     f = lib.inkling_sconv
     ok = dict(x=FAKE, w=FAKE, st=FAKE, cu=FAKE, y=FAKE + 4096, B=1, T=4, C=64, mq=4, ds=None, s=None)
