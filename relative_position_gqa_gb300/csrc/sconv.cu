@@ -216,7 +216,7 @@ __global__ void __launch_bounds__(kSconvThreads) sconv_step_kernel(const SconvDe
   const float inv_scale = which == 0 ? p.inv_scale[0] : p.inv_scale[1];
   uint16_t* st = p.state + ((size_t)b * p.streams + which) * 3 * C + c0;
 
-  // round 1: lengths, taps, the three rows before the step
+  // first batch of loads: lengths, taps, the three rows before the step
   const int t_begin = p.cu_q_lens[b];
   const int t_end = p.cu_q_lens[b + 1];
   float tap[kVec][4];
@@ -233,7 +233,7 @@ __global__ void __launch_bounds__(kSconvThreads) sconv_step_kernel(const SconvDe
     if (threadIdx.x == 0) report(p.status, kErrBadInput);
     return;
   }
-  // round 2: every raw row of the step and its slot
+  // second batch: every raw row of the step and its slot
   uint4 raw[kStepRows];
   long long slot[kStepRows];
 #pragma unroll
