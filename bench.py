@@ -679,7 +679,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5, 6])
-    ap.add_argument("--variant", default=None, help="mtp_decode: swa|full; decode_1m: n1|n9 (n1_256k|n9_256k: quarter length)")
+    ap.add_argument("--variant", default=None, help="mtp_decode: swa|full (swa_8k: contexts <= 8192); decode_1m: n1|n9 (n1_256k|n9_256k: quarter length)")
     ap.add_argument("--kv", choices=["bf16", "fp8"], default="bf16",
                     help="KV cache type for the decode workloads")
     ap.add_argument("--ref-seconds", type=float, default=6.0,

@@ -516,8 +516,11 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
     const int hf = warp >> 2, c0 = hf * 64;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const bool valid = r < rows;
-    const int t = valid ? r / p.G : 0;
-    const int g = valid ? r % p.G : 0;
+    // A padding row takes the head of its lane and the last token's position: its bias
+    // reads then fall on the words of valid rows (shared, not conflicting), so a warp's
+    // 32 lanes hit distinct banks.  Its Q is zero and nothing of it is stored.
+    const int t = min(r / p.G, n - 1);
+    const int g = r % p.G;
     const int h = kvh * p.G + g;
 
     // packed Q rows into TMEM columns [0, 64): this thread's half of the d range

@@ -81,7 +81,8 @@ def _prefill(name, B, S, hq, hkv, r, window, bias_std, q_prescale=1.0, scale=Non
 
 def config(n: int, *, variant: Optional[str] = None) -> Spec:
     """The five workloads.  `variant` picks the sliding/full half of the MTP decode
-    workload ("swa" | "full") and the 1- or 9-token form of the 1M decode ("n1" | "n9")."""
+    workload ("swa" | "full" | "swa_8k") and the 1- or 9-token form of the 1M decode
+    ("n1" | "n9" | "n1_256k" | "n9_256k")."""
     if n == 1:
         return _prefill("tiny_prefill", 1, 256, 4, 1, 512, 0, 1.0)
     if n == 2:
@@ -90,10 +91,15 @@ def config(n: int, *, variant: Optional[str] = None) -> Spec:
         return _prefill("full_prefill_64k", 1, 65536, 64, 8, 8192, 0, 0.5,
                         q_prescale=1.0 / math.sqrt(HEAD_DIM), scale=1.0)
     if n == 4:
+        # swa_8k: the sliding-window half with contexts in [4096, 8192] (the same 33-34
+        # visible pages per sequence, under 1 GB of cache), small enough for multi-pass
+        # profiler captures of the same kernel launch
         g = torch.Generator().manual_seed(4)
-        lens = torch.randint(4096, 131072 + 1, (64,), generator=g).tolist()
+        hi = 8192 if variant == "swa_8k" else 131072
+        lens = torch.randint(4096, hi + 1, (64,), generator=g).tolist()
         window = 0 if variant == "full" else 4096
-        return Spec(name=f"mtp_decode_{'full' if window == 0 else 'swa'}", batch=64, hq=32,
+        tag = "full" if window == 0 else ("swa_8k" if variant == "swa_8k" else "swa")
+        return Spec(name=f"mtp_decode_{tag}", batch=64, hq=32,
                     hkv=4, r=8192, window=window, bias_std=0.5, q_lens=[9] * 64,
                     seq_lens=lens, history_random=True, state_random=True)
     if n == 5:
