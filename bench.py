@@ -195,10 +195,10 @@ class ClockSampler:
 TRAFFIC = {
     (2, None): ("prefill.cu", "d31d6f8e751e8228fc8da767e6fc115591a23f4a4c322f748ccb23ef12e50c27",
                 611.4e6),
-    (5, "n1"): ("decode.cu", "cc12c06b99a34b1014eef848ca26221944e8bdd7ff3ac96e9a0f814361e0669d",
-                4301.1e6),
-    (5, "n9_256k"): ("decode.cu", "cc12c06b99a34b1014eef848ca26221944e8bdd7ff3ac96e9a0f814361e0669d",
-                     1080.2e6),
+    (4, "swa"): ("decode.cu", "3bb5685c103cbde3bbc25bc91b9ece3a2d33f2a806f6d062c78aeb3b50a4dbed", 564.8e6),
+    (4, "swa_8k"): ("decode.cu", "3bb5685c103cbde3bbc25bc91b9ece3a2d33f2a806f6d062c78aeb3b50a4dbed", 564.1e6),
+    (5, "n1"): ("decode.cu", "3bb5685c103cbde3bbc25bc91b9ece3a2d33f2a806f6d062c78aeb3b50a4dbed", 4301.0e6),
+    (5, "n9_256k"): ("decode.cu", "3bb5685c103cbde3bbc25bc91b9ece3a2d33f2a806f6d062c78aeb3b50a4dbed", 1079.8e6),
 }
 
 
@@ -207,6 +207,8 @@ def kernel_traffic(workload: int, variant=None, fp8: bool = False):
         return None
     if workload == 5 and variant is None:
         variant = "n1"
+    if workload == 4 and variant is None:
+        variant = "swa"
     entry = TRAFFIC.get((workload, variant))
     if entry is None:
         return None
