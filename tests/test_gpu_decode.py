@@ -145,3 +145,24 @@ def test_decode_bad_block_reported(ink, num_splits):
     gpu_attn(ink, g, st, decode=True, num_splits=num_splits)
     torch.cuda.synchronize()
     assert int(st.item()) == 5  # INKLING_ERR_BAD_BLOCK
+
+
+@pytest.mark.parametrize("name,num_splits", [("mixed_n", 0), ("mixed_n", 3), ("window_300", 0),
+                                             ("g16_n8", 2)])
+def test_decode_plan_matches_launch(ink, name, num_splits):
+    """decode_plan's merge flag agrees with the workspace the call needs, and its split
+    count with the split rule: ceil(pages / pages_per_split) splits cover the visible range."""
+    spec = CASES[name]
+    plan = ink.decode_plan(spec.batch, spec.hq, spec.hkv, spec.max_q_len, spec.max_seq_len,
+                           spec.window, num_splits)
+    need = ink.decode_workspace_size(spec.batch, spec.hq, spec.hkv, spec.max_q_len,
+                                     spec.max_seq_len, spec.window, num_splits)
+    assert plan["merge"] == (need > 0) == (plan["num_splits"] > 1)
+    assert plan["ctas"] == plan["num_splits"] * spec.hkv * spec.batch
+    if num_splits > 0:
+        assert plan["num_splits"] <= num_splits
+    pages = -(-spec.max_seq_len // 128)
+    if spec.window > 0:
+        pages = min(pages, (spec.window + spec.max_q_len - 1 + 127) // 128 + 1)
+    assert plan["num_splits"] * plan["pages_per_split"] >= pages
+    assert (plan["num_splits"] - 1) * plan["pages_per_split"] < pages

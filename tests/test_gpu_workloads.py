@@ -71,9 +71,9 @@ def test_full_prefill_64k_sampled(ink):
     _check(ink, 3, [0], rows, decode=False)
 
 
-@pytest.mark.parametrize("variant", ["swa", "full"])
+@pytest.mark.parametrize("variant", ["swa", "full", "swa_8k"])
 def test_mtp_decode_sampled(ink, variant):
-    lens = W.config(4).seq_lens
+    lens = W.config(4, variant=variant).seq_lens
     seqs = sorted({min(range(64), key=lambda b: lens[b]), max(range(64), key=lambda b: lens[b]), 17})
     _check(ink, 4, seqs, lambda i, n: range(n), decode=True, variant=variant)
 
