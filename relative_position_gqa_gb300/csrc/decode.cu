@@ -76,7 +76,7 @@ struct __align__(1024) Smem {
   uint64_t q_ready, s_full[2], p_full[2], pv_done, o_full, drain;
   // the two column halves of a row trade partial maxima (per page parity), and at the
   // end their sums (in the slot of the parity after the last page's)
-  uint64_t x_full[2], l_full;
+  uint64_t x_full[4][2], l_full;  // x_full[q]: warps q and q + 4 (the two halves of rows 32q..)
   float xm[2][2][128];
   // FP8 cache only: the converters' hand-offs (see convert_rows)
   uint64_t k8_empty[4], v8_empty[4], kh_full[2], kh_empty[2], vh_full[2], vh_empty[2];
@@ -228,8 +228,10 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
       mbar_init(&s.b_empty[i], 2 * nact);
     }
     mbar_init(&s.q_ready, 2 * nact);
-    mbar_init(&s.x_full[0], 2 * nact);
-    mbar_init(&s.x_full[1], 2 * nact);
+    for (int q = 0; q < 4; ++q) {
+      mbar_init(&s.x_full[q][0], 64);
+      mbar_init(&s.x_full[q][1], 64);
+    }
     mbar_init(&s.l_full, 2 * nact);
     mbar_init(&s.s_full[0], 1);
     mbar_init(&s.s_full[1], 1);
@@ -510,7 +512,8 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
     // ------------------------------------------------------------ softmax group ---
     // Thread (r, hf): packed row r = TMEM lane, columns 64 hf .. 64 hf + 63 of S, P, O.
     // The two halves of a row trade their partial maxima through shared memory (an
-    // mbarrier per page parity), so both use the same running max; each keeps its own
+    // mbarrier per warp pair and page parity: the pairs do not wait for one another), so
+    // both use the same running max; each keeps its own
     // partial sum, and the sums meet once at the end.
     const int r = (warp & 3) * 32 + lane;
     const int hf = warp >> 2, c0 = hf * 64;
@@ -623,8 +626,11 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
       // the other half's maximum of this page
       const float pm = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
       s.xm[i & 1][hf][r] = pm;
-      mbar_arrive(&s.x_full[i & 1]);
-      if (!mbar_wait(&s.x_full[i & 1], (i >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
+      mbar_arrive(&s.x_full[warp & 3][i & 1]);
+      if (!mbar_wait(&s.x_full[warp & 3][i & 1], (i >> 1) & 1, abort_flag, p.status)) {
+        ok = false;
+        break;
+      }
       const float m_new = fmax3(m, pm, s.xm[i & 1][hf ^ 1][r]);
       const bool need = m_new > m + kRescaleThreshold || (m == -INFINITY && m_new > -INFINITY);
       const float alpha = need ? ex2((m - m_new) * kLog2e) : 1.f;
