@@ -195,10 +195,10 @@ class ClockSampler:
 TRAFFIC = {
     (2, None): ("prefill.cu", "d31d6f8e751e8228fc8da767e6fc115591a23f4a4c322f748ccb23ef12e50c27",
                 611.4e6),
-    (4, "swa"): ("decode.cu", "3bb5685c103cbde3bbc25bc91b9ece3a2d33f2a806f6d062c78aeb3b50a4dbed", 564.8e6),
-    (4, "swa_8k"): ("decode.cu", "3bb5685c103cbde3bbc25bc91b9ece3a2d33f2a806f6d062c78aeb3b50a4dbed", 564.1e6),
-    (5, "n1"): ("decode.cu", "3bb5685c103cbde3bbc25bc91b9ece3a2d33f2a806f6d062c78aeb3b50a4dbed", 4301.0e6),
-    (5, "n9_256k"): ("decode.cu", "3bb5685c103cbde3bbc25bc91b9ece3a2d33f2a806f6d062c78aeb3b50a4dbed", 1079.8e6),
+    (4, "swa"): ("decode.cu", "d319709b06d5eca9b36ba83a40df24b32970b7a8e19fc792c299dd40f54c9bb3", 564.9e6),
+    (4, "swa_8k"): ("decode.cu", "d319709b06d5eca9b36ba83a40df24b32970b7a8e19fc792c299dd40f54c9bb3", 563.8e6),
+    (5, "n1"): ("decode.cu", "d319709b06d5eca9b36ba83a40df24b32970b7a8e19fc792c299dd40f54c9bb3", 4301.0e6),
+    (5, "n9_256k"): ("decode.cu", "d319709b06d5eca9b36ba83a40df24b32970b7a8e19fc792c299dd40f54c9bb3", 1079.9e6),
 }
 
 
