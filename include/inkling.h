@@ -298,11 +298,17 @@ INKLING_API int inkling_rel_attn_decode_fp8(const void *q, const void *k_cache, 
  * every GPU that loads the library holds it until the process exits.  A request whose
  * partials would not fit (inkling_rel_attn_decode_workspace_size(...) with the same
  * arguments above the capacity) returns INKLING_ERR_WORKSPACE and launches nothing.
+ * Argument checks and their order are those of inkling_rel_attn_decode: the capacity
+ * is compared last, so a call with a bad argument reports that argument's error.
  * The first call on a device looks up the array's device address (cudaGetSymbolAddress,
- * with that device current); make that first call before any stream capture.  No device
- * memory is allocated or freed.  All calls share the one array and it keeps the last
- * call's contents (the kernels need none of it zeroed): calls whose work can overlap on
- * the GPU (other streams, other threads) race on it and must be serialised by the caller.
+ * with that device current); make that first call before any stream capture.  The address
+ * is kept per device and CUDA context (by the context's process-unique id), so the first
+ * call after the device's context has been replaced (cudaDeviceReset, or the primary
+ * context released and made again) looks it up again and is again a first call.  No
+ * device memory is allocated or freed.  All calls share the one array and it keeps the
+ * last call's contents (the kernels need none of it zeroed): calls whose work can overlap
+ * on the GPU (other streams, other threads) race on it and must be serialised by the
+ * caller.
  */
 INKLING_API size_t inkling_rel_attn_decode_noalloc_capacity(void);
 INKLING_API int inkling_rel_attn_decode_noalloc(
