@@ -76,6 +76,27 @@ def snapshot(case: W.Case, seqs: Optional[Sequence[int]] = None) -> Snapshot:
     return Snapshot(case=sub, seqs=seqs, tok_index=tok, page_index=page_idx)
 
 
+def permute_pages(case: W.Case, seed: int) -> W.Case:
+    """The same logical K/V on other physical pages: page j of `case` moves to page
+    perm[j], and the block table and slot mapping follow it.  Storage only: every
+    sequence sees the same keys and values in the same logical order."""
+    dev = case.k_cache.device
+    nb = case.num_blocks
+    perm = torch.randperm(nb, generator=torch.Generator().manual_seed(seed)).to(dev)
+    k = torch.empty_like(case.k_cache)
+    v = torch.empty_like(case.v_cache)
+    k[perm] = case.k_cache
+    v[perm] = case.v_cache
+    bt = case.block_table
+    table = torch.where(bt >= 0, perm[bt.clamp_min(0).long()].to(torch.int32), bt)
+    sm = case.slot_mapping
+    slots = torch.where(sm >= 0, perm[(sm.clamp_min(0) // 128)] * 128 + sm.clamp_min(0) % 128, sm)
+    return dataclasses.replace(case, k_cache=k, v_cache=v, block_table=table.contiguous(),
+                               slot_mapping=slots.contiguous(), q=case.q.clone(),
+                               k_raw=case.k_raw.clone(), v_raw=case.v_raw.clone(),
+                               state=case.state.clone())
+
+
 def run_oracle(snap: Snapshot, rows: Optional[Sequence[int]] = None):
     """Oracle sconv into the snapshot's caches, then attention rows (snapshot indices)."""
     c = snap.case

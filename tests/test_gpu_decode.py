@@ -6,7 +6,7 @@ import pytest
 import torch
 
 import workloads as W
-from harness import compare_out, gpu_attn, gpu_sconv, run_oracle, snapshot
+from harness import compare_out, gpu_attn, gpu_sconv, permute_pages, run_oracle, snapshot
 
 pytestmark = pytest.mark.gpu
 
@@ -166,3 +166,37 @@ def test_decode_plan_matches_launch(ink, name, num_splits):
         pages = min(pages, (spec.window + spec.max_q_len - 1 + 127) // 128 + 1)
     assert plan["num_splits"] * plan["pages_per_split"] >= pages
     assert (plan["num_splits"] - 1) * plan["pages_per_split"] < pages
+
+
+# long enough that the automatic rule splits (num_splits 0), with ragged page tails
+ORDER_SPEC = {
+    0: W.small(q_lens=(9, 1, 9, 5), seq_lens=(6000, 300, 4500, 129), hq=8, hkv=2, r=2000),
+    1000: W.small(q_lens=(9, 1, 9, 5), seq_lens=(6000, 300, 4500, 129), hq=8, hkv=2, r=2000,
+                  window=1000),
+}
+
+
+@pytest.mark.parametrize("window", sorted(ORDER_SPEC))
+@pytest.mark.parametrize("num_splits", [1, 3, 0])
+def test_decode_page_order_free_and_deterministic(ink, num_splits, window):
+    """The same logical K/V on shuffled physical pages gives bit-identical outputs and
+    LSE, and so does running the same call again (a race in the split or merge path
+    would show up as a difference)."""
+    spec = ORDER_SPEC[window]
+    plan = ink.decode_plan(spec.batch, spec.hq, spec.hkv, spec.max_q_len, spec.max_seq_len,
+                           window, num_splits)
+    if num_splits != 1 and window == 0:
+        assert plan["num_splits"] > 1
+    base = W.make_case(spec, seed=67, device="cuda", identity_table=True)
+    st = _status()
+    results = []
+    for g in (base, permute_pages(base, seed=5), permute_pages(base, seed=6)):
+        gpu_sconv(ink, g, st)
+        for _ in range(2):
+            results.append(gpu_attn(ink, g, st, decode=True, num_splits=num_splits))
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0, ink.status_string(int(st.item()))
+    out0, lse0 = results[0]
+    assert torch.isfinite(out0).all()
+    for out, lse in results[1:]:
+        assert torch.equal(out, out0) and torch.equal(lse, lse0)

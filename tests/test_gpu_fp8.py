@@ -259,3 +259,34 @@ def test_prefill_fp8_bad_block_reported(ink):
                              out=out, dev_status=st)
     torch.cuda.synchronize()
     assert int(st.item()) == 5  # INKLING_ERR_BAD_BLOCK
+
+
+@pytest.mark.parametrize("num_splits", [1, 3, 0])
+def test_decode_fp8_page_order_free_and_deterministic(ink, num_splits):
+    """FP8 cache: shuffled physical pages and a second run give bit-identical outputs."""
+    from harness import permute_pages
+    spec = W.small(q_lens=(9, 1, 9, 5), seq_lens=(6000, 300, 4500, 129), hq=8, hkv=2, r=2000)
+    base = W.make_case(spec, seed=87, device="cuda", identity_table=True)
+    base.k_cache = W.fp8_history(base.k_cache, K_SCALE)
+    base.v_cache = W.fp8_history(base.v_cache, V_SCALE)
+    st = _status()
+    results = []
+    for g in (base, permute_pages(base, seed=5)):
+        ink.sconv_kv_fp8(g.k_raw, g.v_raw, g.w_k, g.w_v, g.state, g.cu_q_lens, g.slot_mapping,
+                         g.k_cache, g.v_cache, k_scale=K_SCALE, v_scale=V_SCALE,
+                         max_q_len=spec.max_q_len, dev_status=st)
+        for _ in range(2):
+            out = torch.full((spec.total_q, spec.hq, 128), float("nan"), device="cuda")
+            lse = torch.full((spec.total_q, spec.hq), float("nan"), device="cuda")
+            ink.rel_attn_decode_fp8(g.q, g.k_cache, g.v_cache, g.block_table, g.cu_q_lens,
+                                    g.seq_lens, g.bias, k_scale=K_SCALE, v_scale=V_SCALE,
+                                    scale=spec.scale, window=0, max_q_len=spec.max_q_len,
+                                    max_seq_len=spec.max_seq_len, out=out, lse=lse,
+                                    num_splits=num_splits, dev_status=st)
+            results.append((out, lse))
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0, ink.status_string(int(st.item()))
+    out0, lse0 = results[0]
+    assert torch.isfinite(out0).all()
+    for out, lse in results[1:]:
+        assert torch.equal(out, out0) and torch.equal(lse, lse0)
