@@ -1,22 +1,24 @@
 """Benchmark of the Inkling attention block on GB300.
 
-Default workload (one step = the whole hot path over one batch):
-  sliding-window prefill, B=4 sequences x 8192 new tokens, 32 query / 4 KV heads, head
-  dim 128, window 4096, relative-bias table [32 x 8192]:
-    inkling_sconv_kv      (K and V sconv into the paged bf16 cache, 512 channels)
-    inkling_rel_attn_prefill  (bf16 output)
-Metric: attention TFLOP/s counting only allowed (query, key) pairs, 4*D flops per pair
-per head (QK^T and PV).  Other workloads (--workload 1..5) print the same line shape;
-the decode ones report KV-read GB/s (algorithmic K/V bytes inside the causal/window range).
---kv fp8 runs the FP8 KV cache path (inkling_sconv_kv_fp8, then inkling_rel_attn_decode_fp8
-or inkling_rel_attn_prefill_fp8); decode GB/s count the E4M3 bytes, half of the bf16
-cache's; prefill TFLOP/s count the same flops as the bf16 cache.
---workload 4 also times the sconv-state rollback after the verify step on its own
-(config.rollback_us, not part of the step).  --workload 6 is the conv on a dense stream
-(inkling_sconv on the sliding-window prefill's attention output, 32768 tokens x 4096
-channels), reported in GB/s of algorithmic bytes (raw rows read + outputs written).
+One step = the whole hot path over one batch: inkling_sconv_kv (K and V sconv into the
+paged cache) then the attention (inkling_rel_attn_prefill or inkling_rel_attn_decode).
 
-python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload 2]
+Default line (python bench.py): the 64K full-causal prefill, B=1 x 65536 new tokens, 64
+query / 8 KV heads, head dim 128, relative-bias table [64 x 8192], exactly --steps timed
+steps.  The same JSON line then carries `workloads`: every workload measured in the same
+run with its own roofline, end-to-end figure and clock record:
+  1 tiny prefill, 2 sliding-window prefill, 3 64K prefill        (TFLOP/s)
+  4 MTP decode, window 4096 / full / the two as one layer pair   (KV-read GB/s)
+  5 1M-token decode, 1 and 9 tokens                              (KV-read GB/s)
+  and the FP8 (E4M3) KV cache forms of 2, 4 and 5.
+Prefill metric: attention TFLOP/s counting only allowed (query, key) pairs, 4*D flops per
+pair per head (QK^T and PV).  Decode metric: K/V bytes inside the causal/window range
+over the step time; with --kv fp8 / the _fp8 entries, the E4M3 bytes (half).
+--workload N [--variant V] [--kv fp8] times one workload alone (no sweep unless --sweep).
+--workload 6 is the conv on a dense stream (inkling_sconv on the sliding-window prefill's
+attention output, 32768 tokens x 4096 channels), in GB/s of algorithmic bytes.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload 3]
 Under torchrun (N > 1) every rank runs an independent replica (the path has no exchange
 step); value = work of all ranks / max time over ranks.
 """
@@ -233,24 +235,37 @@ def measured_peaks():
 
 
 # ------------------------------------------------------------------ our arm ---------
-def run_ours(args, ws, rank, local):
-    import relative_position_gqa_gb300 as ink
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    ink._lib.load()  # raises if the CUDA library is missing: no fallback
-    spec = workload_spec(args.workload, args.variant)
-    decode = is_decode(args.workload)
-    fp8 = args.kv == "fp8"
-    g = W.make_case(spec, seed=args.workload + 1000 * rank, device=dev)
-    K_SCALE, V_SCALE = 0.0625, 0.0625
+K_SCALE, V_SCALE = 0.0625, 0.0625  # FP8 cache scales of the benchmark
+MIN_TIMED_S = 0.25  # a timed loop lasts at least this long (several clock samples)
+
+
+class Bench:
+    """Device state shared by every workload of one run (the L2 flush buffers)."""
+
+    def __init__(self, dev):
+        self.dev = dev
+        self.flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        self.flush_sink = torch.empty(1, dtype=torch.float32, device=dev)
+
+
+def measure_attn(ink, bench: Bench, n: int, variant, fp8: bool, steps: int, warmup: int,
+                 ws: int, e2e_chunks: int = 0, exact: bool = False) -> dict:
+    """One workload: the step (conv + attention, no event between the launches), the
+    attention alone, the conv alone, and the step end to end over page-locked host
+    buffers.  Returns the timings (max over ranks), work and clock record.  Each timed
+    loop runs `steps` steps (exact) or, for short steps, enough that it lasts
+    MIN_TIMED_S."""
+    dev = bench.dev
+    spec = workload_spec(n, variant)
+    decode = is_decode(n)
+    rank = int(os.environ.get("RANK", "0"))
+    g = W.make_case(spec, seed=n + 1000 * rank, device=dev)
     if fp8:
         g.k_cache = W.fp8_history(g.k_cache, K_SCALE)
         g.v_cache = W.fp8_history(g.v_cache, V_SCALE)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     out = torch.empty(spec.total_q, spec.hq, 128, dtype=torch.bfloat16, device=dev)
     state0 = g.state.clone()
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-    flush_sink = torch.empty(1, dtype=torch.float32, device=dev)
     ws_bytes = 0
     workspace = None
     plan = None
@@ -300,37 +315,52 @@ def run_ours(args, ws, rank, local):
 
     def reset():
         g.state.copy_(state0)
-        flush_l2(flush, flush_sink)
+        flush_l2(bench.flush, bench.flush_sink)
 
-    # ---- device-resident timing: per step, events around the step and around attention
-    for _ in range(args.warmup):
-        reset()
-        sconv(g.k_raw, g.v_raw)
-        attn(g.q, out)
-    torch.cuda.synchronize()
-    if int(status.item()) != 0:
-        raise RuntimeError(f"device status {ink.status_string(int(status.item()))}")
-    # The step is timed with no event between its two launches, so that the attention
-    # kernel's programmatic dependent launch overlaps the conv's tail as it would in a
-    # model; the attention and the conv are then timed alone, each in a loop of its own.
-    def timed(fn):
+    def check():
+        torch.cuda.synchronize()
+        if int(status.item()) != 0:
+            raise RuntimeError(f"{spec.name}: device status {ink.status_string(int(status.item()))}")
+
+    def timed(fn, k):
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(args.steps)]
-        for i in range(args.steps):
+               for _ in range(k)]
+        for i in range(k):
             reset()
             evs[i][0].record(stream)
             fn()
             evs[i][1].record(stream)
         return evs
 
+    def mean_ms(evs):
+        return sum(a.elapsed_time(b) for a, b in evs) / len(evs)
+
+    # ---- warm-up, then the step count: at least `steps`, and enough that the timed loop
+    # lasts MIN_TIMED_S, so that the clock sampler sees several samples
+    for _ in range(warmup):
+        reset()
+        sconv(g.k_raw, g.v_raw)
+        attn(g.q, out)
+    check()
+    probe = timed(lambda: (sconv(g.k_raw, g.v_raw), attn(g.q, out)), 3)
+    check()
+    est_ms = mean_ms(probe)
+    k = steps
+    if not exact:
+        k = max(steps, min(5000, int(math.ceil(MIN_TIMED_S * 1e3 / max(est_ms + 0.1, 1e-3)))))
+        k = int(max_over_ranks([k], ws, dev)[0])
+
+    # ---- device-resident timing.  The step is timed with no event between its two
+    # launches, so that the attention kernel's programmatic dependent launch overlaps the
+    # conv's tail as it would in a model; the attention and the conv are then timed alone.
     if ws > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    with ClockSampler(local) as clocks:
-        ev_step = timed(lambda: (sconv(g.k_raw, g.v_raw), attn(g.q, out)))
+    with ClockSampler(dev.index if dev.index is not None else 0) as clocks:
+        ev_step = timed(lambda: (sconv(g.k_raw, g.v_raw), attn(g.q, out)), k)
         torch.cuda.synchronize()
-    ev_attn, ev_sconv = [], []
-    for i in range(args.steps):
+    ev_attn = []
+    for i in range(k):
         reset()
         sconv(g.k_raw, g.v_raw)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -338,35 +368,29 @@ def run_ours(args, ws, rank, local):
         attn(g.q, out)
         b.record(stream)
         ev_attn.append((a, b))
-    ev_sconv = timed(lambda: sconv(g.k_raw, g.v_raw))
-    torch.cuda.synchronize()
+    ev_sconv = timed(lambda: sconv(g.k_raw, g.v_raw), k)
+    check()
     if ws > 1:
         torch.distributed.barrier()
-    if int(status.item()) != 0:
-        raise RuntimeError(f"device status {ink.status_string(int(status.item()))}")
-    step_ms = sum(a.elapsed_time(b) for a, b in ev_step) / args.steps
-    attn_ms = sum(a.elapsed_time(b) for a, b in ev_attn) / args.steps
-    sconv_ms = sum(a.elapsed_time(b) for a, b in ev_sconv) / args.steps
+    step_ms, attn_ms, sconv_ms = mean_ms(ev_step), mean_ms(ev_attn), mean_ms(ev_sconv)
 
     rollback_us = None
-    if args.workload == 4:
+    if n == 4 and not fp8:
         # after a verify step, keep a seeded random prefix of each sequence's 9 tokens
         gen = torch.Generator().manual_seed(4)
         accepted = torch.randint(0, 10, (spec.batch,), generator=gen, dtype=torch.int32).to(dev)
-        rb = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(args.steps)]
-        for i in range(args.warmup + args.steps):
+        rb = []
+        for i in range(warmup + steps):
             reset()
-            if i >= args.warmup:
-                rb[i - args.warmup][0].record(stream)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
             ink.sconv_state_rollback(state0, g.k_raw, g.v_raw, g.cu_q_lens, accepted, g.state,
                                      dev_status=status)
-            if i >= args.warmup:
-                rb[i - args.warmup][1].record(stream)
-        torch.cuda.synchronize()
-        if int(status.item()) != 0:
-            raise RuntimeError(f"device status {ink.status_string(int(status.item()))}")
-        rollback_us = round(1e3 * sum(a.elapsed_time(b) for a, b in rb) / args.steps, 2)
+            b.record(stream)
+            if i >= warmup:
+                rb.append((a, b))
+        check()
+        rollback_us = round(1e3 * mean_ms(rb), 2)
 
     # ---- end to end through the public API with host buffers: the step entry points
     # (inkling_prefill_step_host / inkling_decode_step_host) take page-locked Q, raw K/V
@@ -384,13 +408,13 @@ def run_ours(args, ws, rank, local):
     # the 64K prefill overlaps its copies too).  decode: one group (its copies are a few
     # MB, and cutting the batch gives each group its own tail of ragged lengths: two groups
     # measured 1.66 ms on the full MTP decode against 1.41 ms for one)
-    e2e_chunks = args.e2e_chunks if args.e2e_chunks > 0 else (1 if decode else 8)
+    chunks = e2e_chunks if e2e_chunks > 0 else (1 if decode else 8)
     if fp8:
         e2e_path = (f"copies + sconv_kv_fp8 + rel_attn_{'decode' if decode else 'prefill'}_fp8, "
                     "serial")
     else:
-        e2e_path = (f"inkling_{'decode' if decode else 'prefill'}_step_host, "
-                    f"{e2e_chunks} groups" + ("" if decode else " (sequences cut into query-tile pieces)"))
+        e2e_path = (f"inkling_{'decode' if decode else 'prefill'}_step_host, {chunks} groups"
+                    + ("" if decode else " (sequences cut into query-tile pieces)"))
 
     def host_step():
         step_args = (host_in[0], host_in[1], host_in[2], host_out, (*dev_in, out), cu_host,
@@ -406,75 +430,171 @@ def run_ours(args, ws, rank, local):
             ink.decode_step_host(*step_args, scale=spec.scale, window=spec.window,
                                  max_q_len=spec.max_q_len, max_seq_len=spec.max_seq_len,
                                  workspace=workspace, h2d_stream=up, d2h_stream=down,
-                                 chunks=e2e_chunks, dev_status=status)
+                                 chunks=chunks, dev_status=status)
         else:
             ink.prefill_step_host(*step_args, scale=spec.scale, window=spec.window,
                                   max_q_len=spec.max_q_len, h2d_stream=up, d2h_stream=down,
-                                  chunks=e2e_chunks, dev_status=status)
+                                  chunks=chunks, dev_status=status)
 
-    e2e_ev = []
-    for i in range(args.warmup + args.steps):
+    for _ in range(warmup):
         reset()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
         host_step()
-        b.record(stream)
-        if i >= args.warmup:
-            e2e_ev.append((a, b))
-    torch.cuda.synchronize()
-    if int(status.item()) != 0:
-        raise RuntimeError(f"device status {ink.status_string(int(status.item()))}")
-    e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_ev) / len(e2e_ev)
-
+    check()
+    ev_e2e = timed(host_step, k)
+    check()
+    e2e_ms = mean_ms(ev_e2e)
     step_ms, attn_ms, e2e_ms, sconv_ms = max_over_ranks([step_ms, attn_ms, e2e_ms, sconv_ms],
                                                         ws, dev)
 
     peaks, peak_src = measured_peaks()
     if decode:
         work = decode_kv_bytes(spec) / (2 if fp8 else 1)
-        unit = "GB/s"
-        value = ws * work / (step_ms * 1e-3) / 1e9
-        e2e_value = ws * work / (e2e_ms * 1e-3) / 1e9
-        achieved = work / (attn_ms * 1e-3) / 1e9
+        unit, scale_u = "GB/s", 1e9
         peak = float(peaks["hbm_gbs"])
-        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "traffic": None,
-                "peak_source": f"{peak_src} hbm_gbs",
+        roof = {"bound": "hbm", "unit": "GB/s", "peak_source": f"{peak_src} hbm_gbs",
                 "kernel": "decode_kernel<true> (FP8 cache)" if fp8 else "decode_kernel (+combine)"}
     else:
         work = attn_flops(spec)
-        unit = "TFLOP/s"
-        value = ws * work / (step_ms * 1e-3) / 1e12
-        e2e_value = ws * work / (e2e_ms * 1e-3) / 1e12
-        achieved = work / (attn_ms * 1e-3) / 1e12
+        unit, scale_u = "TFLOP/s", 1e12
         peak = float(peaks["bf16_tflops"])
-        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
-                "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
+        roof = {"bound": "tensor", "unit": "TFLOP/s",
                 "peak_source": f"{peak_src} bf16_tflops (burst; kernel timed per launch)",
                 "kernel": "widen_pages_kernel + prefill_kernel" if fp8 else "prefill_kernel"}
-    roof["traffic"] = args.traffic if args.traffic is not None else kernel_traffic(args.workload, args.variant, fp8)
-    line = {
-        "metric": METRIC, "value": round(value, 3), "unit": unit, "n_gpus": ws,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": ("bf16 (KV cache e4m3, f16 MMA)" if decode else "bf16 (KV cache e4m3 widened to bf16)")
-                 if fp8 else "bf16",
-        "data": "synthetic (seeded N(0,1) Q/K/V, N(0,0.5) sconv taps, N(0,sd) bias)",
-        "config": {"workload": workload_name(spec) + (" kv=e4m3" if fp8 else ""),
-                   "global_batch": spec.batch * ws,
-                   "seq_len": spec.max_seq_len, "parallelism": f"replicas x{ws}",
-                   "l2": L2_NOTE,
-                   "attn_ms": round(attn_ms, 4), "sconv_ms": round(sconv_ms, 4),
-                   **({"decode_plan": plan} if decode else {})},
-        "e2e": {"value": round(e2e_value, 3), "unit": unit, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4), "path": e2e_path},
-        "gpu_launches": args.steps * (2 + (1 if (decode and plan["merge"]) or (fp8 and not decode)
-                                           else 0)),
+    achieved = work / (attn_ms * 1e-3) / scale_u
+    roof.update({"achieved": round(achieved, 1), "peak": peak, "frac": round(achieved / peak, 4),
+                 "traffic": kernel_traffic(n, variant, fp8)})
+    launches_per_step = 2 + (1 if (decode and plan["merge"]) or (fp8 and not decode) else 0)
+    entry = {
+        "workload": workload_name(spec) + (" kv=e4m3" if fp8 else ""),
+        "value": round(ws * work / (step_ms * 1e-3) / scale_u, 3), "unit": unit,
+        "ms_per_step": round(step_ms, 4), "steps": k, "attn_ms": round(attn_ms, 4),
+        "sconv_ms": round(sconv_ms, 4),
+        "e2e": {"value": round(ws * work / (e2e_ms * 1e-3) / scale_u, 3), "unit": unit,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_ms, 4), "path": e2e_path},
         "roofline": roof,
         "clocks": clocks.summary(),
+        "gpu_launches": k * launches_per_step,
+        "dtype": ("bf16 (KV cache e4m3, f16 MMA)" if decode else
+                  "bf16 (KV cache e4m3 widened to bf16)") if fp8 else "bf16",
+        "_work": work, "_attn_ms": attn_ms, "_e2e_ms": e2e_ms, "_spec": spec,
     }
+    if decode:
+        entry["decode_plan"] = plan
     if rollback_us is not None:
-        line["config"]["rollback_us"] = rollback_us
+        entry["rollback_us"] = rollback_us
+    del g, out, workspace, host_in, dev_in, host_out
+    torch.cuda.empty_cache()
+    return entry
+
+
+def combined_decode(swa: dict, full: dict) -> dict:
+    """One sliding-window and one full MTP decode layer as one figure: both calls' K/V
+    bytes over both calls' time (the two layer kinds alternate in the model)."""
+    work = swa["_work"] + full["_work"]
+    step_ms = swa["ms_per_step"] + full["ms_per_step"]
+    attn_ms = swa["_attn_ms"] + full["_attn_ms"]
+    e2e_ms = swa["_e2e_ms"] + full["_e2e_ms"]
+    peak = swa["roofline"]["peak"]
+    achieved = work / (attn_ms * 1e-3) / 1e9
+    return {
+        "workload": "mtp_decode: one window-4096 layer + one full layer (K/V bytes of both "
+                    "calls over both calls' time)",
+        "value": round(work / (step_ms * 1e-3) / 1e9, 3), "unit": "GB/s",
+        "ms_per_step": round(step_ms, 4), "attn_ms": round(attn_ms, 4),
+        "e2e": {"value": round(work / (e2e_ms * 1e-3) / 1e9, 3), "unit": "GB/s",
+                "h2d_bytes_per_step": swa["e2e"]["h2d_bytes_per_step"] + full["e2e"]["h2d_bytes_per_step"],
+                "d2h_bytes_per_step": swa["e2e"]["d2h_bytes_per_step"] + full["e2e"]["d2h_bytes_per_step"],
+                "ms_per_step": round(e2e_ms, 4)},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": None,
+                     "peak_source": swa["roofline"]["peak_source"],
+                     "kernel": swa["roofline"]["kernel"]},
+        "clocks": {"from": ["4_mtp_decode_swa", "4_mtp_decode_full"]},
+    }
+
+
+def public(entry: dict) -> dict:
+    return {k: v for k, v in entry.items() if not k.startswith("_")}
+
+
+# every workload of the sweep: (key, workload, variant, FP8 cache)
+SWEEP = [
+    ("1_tiny_prefill", 1, None, False),
+    ("2_swa_prefill", 2, None, False),
+    ("3_full_prefill_64k", 3, None, False),
+    ("4_mtp_decode_swa", 4, "swa", False),
+    ("4_mtp_decode_full", 4, "full", False),
+    ("5_decode_1m_n1", 5, "n1", False),
+    ("5_decode_1m_n9", 5, "n9", False),
+    ("2_swa_prefill_fp8", 2, None, True),
+    ("4_mtp_decode_swa_fp8", 4, "swa", True),
+    ("4_mtp_decode_full_fp8", 4, "full", True),
+    ("5_decode_1m_n1_fp8", 5, "n1", True),
+    ("5_decode_1m_n9_fp8", 5, "n9", True),
+]
+
+
+def sweep_key(n: int, variant, fp8: bool):
+    """The sweep's key for a workload (variant None is the sliding-window MTP decode and
+    the one-token 1M decode, as in workloads.config)."""
+    v = variant if variant is not None else {4: "swa", 5: "n1"}.get(n)
+    for key, n2, v2, f2 in SWEEP:
+        if n2 == n and v2 == v and f2 == fp8:
+            return key
+    return None
+
+
+def line_config(spec: W.Spec, ws: int, fp8: bool) -> dict:
+    return {"workload": workload_name(spec) + (" kv=e4m3" if fp8 else ""),
+            "global_batch": spec.batch * ws, "seq_len": spec.max_seq_len,
+            "parallelism": f"replicas x{ws}", "l2": L2_NOTE}
+
+
+def run_ours(args, ws, rank, local):
+    import relative_position_gqa_gb300 as ink
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    ink._lib.load()  # raises if the CUDA library is missing: no fallback
+    bench = Bench(dev)
+    fp8 = args.kv == "fp8"
+    # the headline: exactly --steps timed steps
+    main = measure_attn(ink, bench, args.workload, args.variant, fp8, args.steps, args.warmup,
+                        ws, args.e2e_chunks, exact=True)
+    if args.traffic is not None:
+        main["roofline"]["traffic"] = args.traffic
+    spec = main["_spec"]
+    line = {
+        "metric": METRIC, "value": main["value"], "unit": main["unit"], "n_gpus": ws,
+        "steps": main["steps"], "warmup": args.warmup, "ms_per_step": main["ms_per_step"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": main["dtype"],
+        "data": "synthetic (seeded N(0,1) Q/K/V, N(0,0.5) sconv taps, N(0,sd) bias)",
+        "config": line_config(spec, ws, fp8),
+        "detail": {"attn_ms": main["attn_ms"], "sconv_ms": main["sconv_ms"],
+                   **({"decode_plan": main["decode_plan"]} if "decode_plan" in main else {}),
+                   **({"rollback_us": main["rollback_us"]} if "rollback_us" in main else {})},
+        "e2e": main["e2e"],
+        "gpu_launches": main["gpu_launches"],
+        "roofline": main["roofline"],
+        "clocks": main["clocks"],
+    }
+    if args.sweep:
+        # every configuration in the same run: prefill TFLOP/s and decode KV-read GB/s,
+        # each with its roofline, end-to-end figure and clock record
+        results = {}
+        main_key = sweep_key(args.workload, args.variant, fp8)
+        for key, n, variant, f8 in SWEEP:
+            if key == main_key:
+                results[key] = main
+                continue
+            results[key] = measure_attn(ink, bench, n, variant, f8, args.steps, args.warmup, ws)
+        results["4_mtp_decode_combined"] = combined_decode(results["4_mtp_decode_swa"],
+                                                           results["4_mtp_decode_full"])
+        results["4_mtp_decode_combined_fp8"] = combined_decode(
+            results["4_mtp_decode_swa_fp8"], results["4_mtp_decode_full_fp8"])
+        line["workloads"] = {k: public(v) for k, v in results.items()}
+        line["gpu_launches_all"] = sum(v.get("gpu_launches", 0) for v in results.values())
     return line
 
 
@@ -667,7 +787,7 @@ def run_reference(args, ws, rank):
         "impl": "reference", "metric": METRIC, "value": value, "unit": unit, "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": workload_name(spec)},
+        "data": "synthetic", "config": line_config(spec, ws, False),
         "cpu_baseline": {"value": value, "unit": unit, "cores": cores, "kind": "oracle",
                          "sample": desc},
         "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -677,10 +797,15 @@ def run_reference(args, ws, rank):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5, 6])
+    ap.add_argument("--workload", type=int, default=None, choices=[1, 2, 3, 4, 5, 6],
+                    help="default: 3 (the 64K full prefill), with every other workload "
+                         "measured in the same run (--sweep)")
+    ap.add_argument("--sweep", action=argparse.BooleanOptionalAction, default=None,
+                    help="measure every workload after the headline one (default: on when "
+                         "--workload is not given)")
     ap.add_argument("--variant", default=None, help="mtp_decode: swa|full (swa_8k: contexts <= 8192); decode_1m: n1|n9 (n1_256k|n9_256k: quarter length)")
     ap.add_argument("--kv", choices=["bf16", "fp8"], default="bf16",
                     help="KV cache type for the decode workloads")
@@ -693,6 +818,10 @@ def main():
                     help="DRAM bytes per launch of the dominant kernel from an ncu capture")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    if args.sweep is None:
+        args.sweep = args.workload is None and args.kv == "bf16" and args.variant is None
+    if args.workload is None:
+        args.workload = 3
 
     ws, rank, local = dist_env()
     if ws > 1:
