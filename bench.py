@@ -374,6 +374,24 @@ def measure_attn(ink, bench: Bench, n: int, variant, fp8: bool, steps: int, warm
         torch.distributed.barrier()
     step_ms, attn_ms, sconv_ms = mean_ms(ev_step), mean_ms(ev_attn), mean_ms(ev_sconv)
 
+    fused_ms = None
+    if decode and not fp8:
+        # the same step as one call: the conv of the new tokens fused into the decode
+        # kernel's prologue (inkling_rel_attn_decode_sconv)
+        def fused():
+            ink.rel_attn_decode_sconv(g.q, g.k_raw, g.v_raw, g.w_k, g.w_v, g.state, g.k_cache,
+                                      g.v_cache, g.block_table, g.cu_q_lens, g.seq_lens, g.bias,
+                                      scale=spec.scale, window=spec.window,
+                                      max_q_len=spec.max_q_len, max_seq_len=spec.max_seq_len,
+                                      out=out, workspace=workspace, dev_status=status)
+        for _ in range(warmup):
+            reset()
+            fused()
+        check()
+        ev_fused = timed(fused, k)
+        check()
+        fused_ms = mean_ms(ev_fused)
+
     rollback_us = None
     if n == 4 and not fp8:
         # after a verify step, keep a seeded random prefix of each sequence's 9 tokens
@@ -445,6 +463,8 @@ def measure_attn(ink, bench: Bench, n: int, variant, fp8: bool, steps: int, warm
     e2e_ms = mean_ms(ev_e2e)
     step_ms, attn_ms, e2e_ms, sconv_ms = max_over_ranks([step_ms, attn_ms, e2e_ms, sconv_ms],
                                                         ws, dev)
+    if fused_ms is not None:
+        fused_ms = max_over_ranks([fused_ms], ws, dev)[0]
 
     peaks, peak_src = measured_peaks()
     if decode:
@@ -481,6 +501,11 @@ def measure_attn(ink, bench: Bench, n: int, variant, fp8: bool, steps: int, warm
     }
     if decode:
         entry["decode_plan"] = plan
+    if fused_ms is not None:
+        entry["fused_step"] = {"value": round(ws * work / (fused_ms * 1e-3) / scale_u, 3),
+                               "unit": unit, "ms_per_step": round(fused_ms, 4),
+                               "path": "inkling_rel_attn_decode_sconv (conv in the decode "
+                                       "kernel's prologue)"}
     if rollback_us is not None:
         entry["rollback_us"] = rollback_us
     del g, out, workspace, host_in, dev_in, host_out
@@ -572,6 +597,7 @@ def run_ours(args, ws, rank, local):
         "data": "synthetic (seeded N(0,1) Q/K/V, N(0,0.5) sconv taps, N(0,sd) bias)",
         "config": line_config(spec, ws, fp8),
         "detail": {"attn_ms": main["attn_ms"], "sconv_ms": main["sconv_ms"],
+                   **({"fused_step": main["fused_step"]} if "fused_step" in main else {}),
                    **({"decode_plan": main["decode_plan"]} if "decode_plan" in main else {}),
                    **({"rollback_us": main["rollback_us"]} if "rollback_us" in main else {})},
         "e2e": main["e2e"],

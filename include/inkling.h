@@ -268,6 +268,39 @@ INKLING_API int inkling_rel_attn_decode(const void *q, const void *k_cache, cons
                             inkling_stream_t stream);
 
 /*
+ * inkling_rel_attn_decode_sconv — one decode step with the sconv of its new tokens fused
+ * into the decode kernel's prologue (blog "vLLM Integration & Optimization", closing
+ * paragraph: kernel fusion and PDL; "Managing the sconv cache": the last W-1 = 3 raw rows
+ * per sequence).  The same results as inkling_sconv_kv followed by inkling_rel_attn_decode
+ * on the same stream, with one launch (two when the keys are split) instead of two (three):
+ * the cache rows and the state are bit-identical to the separate conv's, and the
+ * attention output to the separate decode's.
+ *
+ * k_raw, v_raw [T][Hkv*128] bf16: the new tokens' raw (pre-conv) K and V rows, packed as
+ *   q (sequence b's rows at cu_q_lens[b] ..);
+ * w_k, w_v [Hkv*128][4] fp32 taps (w[c][3] multiplies the current token);
+ * sconv_state [B][2][3][Hkv*128] bf16, in/out, as for inkling_sconv_kv;
+ * k_cache, v_cache: the bf16 paged caches, written at the new rows' slots and read by the
+ *   attention.  Sequence b's new row t (position L_b - n_b + t) goes to page
+ *   block_table[b][pos / 128], slot pos % 128: the slots a decode step's slot mapping
+ *   names (no slot_mapping argument; the block table alone decides where a row lives).
+ * Every other argument, the workspace, num_splits and the errors are those of
+ * inkling_rel_attn_decode; k_raw, v_raw, w_k, w_v and sconv_state must be non-NULL and
+ * 16-byte aligned (INKLING_ERR_INVALID_ARG).  Each (split, KV head, sequence) CTA
+ * convolves the new rows that fall in its own pages before it loads them; the state of a
+ * sequence whose keys are split is written by the merge kernel, after every CTA that
+ * reads the old state has finished.  bf16 caches only.
+ */
+INKLING_API int inkling_rel_attn_decode_sconv(
+    const void *q, const void *k_raw, const void *v_raw, const float *w_k, const float *w_v,
+    void *sconv_state, void *k_cache, void *v_cache, const int32_t *block_table,
+    int32_t max_blocks, const int32_t *cu_q_lens, const int32_t *seq_lens, const float *bias,
+    int32_t R, float scale, int32_t window, void *out, int32_t out_dtype, float *lse,
+    int32_t B, int32_t T, int32_t Hq, int32_t Hkv, int64_t num_blocks, int32_t max_q_len,
+    int32_t max_seq_len, int32_t num_splits, void *workspace, size_t workspace_bytes,
+    int32_t *dev_status, inkling_stream_t stream);
+
+/*
  * inkling_rel_attn_decode_fp8 — inkling_rel_attn_decode over an FP8 KV cache written by
  * inkling_sconv_kv_fp8: K = e4m3(code) * k_scale, V = e4m3(code) * v_scale.  The pages
  * are read as bytes (half the HBM traffic of the bf16 cache) and widened to f16 in shared

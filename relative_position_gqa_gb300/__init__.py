@@ -188,6 +188,37 @@ def rel_attn_decode(q, k_cache, v_cache, block_table, cu_q_lens, seq_lens, bias,
                   dev_status, _stream(stream))
 
 
+def rel_attn_decode_sconv(q, k_raw, v_raw, w_k, w_v, sconv_state, k_cache, v_cache,
+                          block_table, cu_q_lens, seq_lens, bias, *, scale: float, window: int,
+                          max_q_len: int, max_seq_len: int, out: torch.Tensor,
+                          lse: Optional[torch.Tensor] = None, num_splits: int = 0,
+                          workspace: Optional[torch.Tensor] = None, dev_status=None,
+                          stream=None) -> None:
+    """inkling_rel_attn_decode_sconv: one decode step with the conv of its new tokens fused
+    into the decode kernel (the new K/V rows go into the caches at the slots the block
+    table gives their positions; the state is updated in place).  The same results as
+    sconv_kv followed by rel_attn_decode."""
+    dev, out_dtype = _attn_common(q, k_cache, v_cache, block_table, cu_q_lens, seq_lens, bias,
+                                  out, lse, dev_status)
+    _check_cuda(k_raw, v_raw, w_k, w_v, sconv_state)
+    assert k_raw.dtype == v_raw.dtype == sconv_state.dtype == torch.bfloat16
+    assert w_k.dtype == w_v.dtype == torch.float32
+    T, hq = q.shape[0], q.shape[1]
+    B = cu_q_lens.shape[0] - 1
+    hkv = k_cache.shape[1]
+    with torch.cuda.device(dev):
+        need = _lib.workspace_size(B, hq, hkv, int(max_q_len), int(max_seq_len), int(window),
+                                   int(num_splits))
+        if workspace is None and need > 0:
+            workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+        ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+        _lib.call("inkling_rel_attn_decode_sconv", q, k_raw, v_raw, w_k, w_v, sconv_state,
+                  k_cache, v_cache, block_table, block_table.shape[1], cu_q_lens, seq_lens, bias,
+                  bias.shape[1], float(scale), int(window), out, out_dtype, lse, B, T, hq, hkv,
+                  k_cache.shape[0], int(max_q_len), int(max_seq_len), int(num_splits), workspace,
+                  ws_bytes, dev_status, _stream(stream))
+
+
 def rel_attn_decode_fp8(q, k_cache, v_cache, block_table, cu_q_lens, seq_lens, bias, *,
                         k_scale: float, v_scale: float, scale: float, window: int,
                         max_q_len: int, max_seq_len: int, out: torch.Tensor,

@@ -30,6 +30,8 @@ SIGNATURES = {
     "inkling_rel_attn_decode_plan": [I32, I32, I32, I32, I32, I32, I32, P],
     "inkling_rel_attn_decode": [P, P, P, P, I32, P, P, P, I32, F32, I32, P, I32, P, I32, I32,
                                 I32, I32, I64, I32, I32, I32, P, SZ, P, P],
+    "inkling_rel_attn_decode_sconv": [P, P, P, P, P, P, P, P, P, I32, P, P, P, I32, F32, I32, P,
+                                      I32, P, I32, I32, I32, I32, I64, I32, I32, I32, P, SZ, P, P],
     "inkling_rel_attn_decode_fp8": [P, P, P, F32, F32, P, I32, P, P, P, I32, F32, I32, P, I32, P,
                                     I32, I32, I32, I32, I64, I32, I32, I32, P, SZ, P, P],
     "inkling_rel_attn_decode_noalloc_capacity": [],

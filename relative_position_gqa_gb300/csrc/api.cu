@@ -320,8 +320,15 @@ static int decode_entry(bool kv_fp8, float k_scale, float v_scale,
                             int32_t Hq, int32_t Hkv, int64_t num_blocks, int32_t max_q_len,
                             int32_t max_seq_len, int32_t num_splits, void* workspace,
                             size_t workspace_bytes, int32_t* dev_status,
-                            inkling_stream_t stream) {
+                            inkling_stream_t stream, const AttnArgs* conv = nullptr) {
   AttnArgs a{};
+  if (conv != nullptr) {  // the step's conv fused into the decode (bf16 cache only)
+    a.conv_k_raw = conv->conv_k_raw;
+    a.conv_v_raw = conv->conv_v_raw;
+    a.conv_w_k = conv->conv_w_k;
+    a.conv_w_v = conv->conv_w_v;
+    a.conv_state = conv->conv_state;
+  }
   a.q = q; a.k_cache = k_cache; a.v_cache = v_cache; a.block_table = block_table;
   a.max_blocks = max_blocks; a.cu_q_lens = cu_q_lens; a.seq_lens = seq_lens; a.bias = bias;
   a.R = R; a.scale = scale; a.window = window; a.out = out; a.out_dtype = out_dtype; a.lse = lse;
@@ -370,6 +377,32 @@ int inkling_rel_attn_decode(const void* q, const void* k_cache, const void* v_ca
                       seq_lens, bias, R, scale, window, out, out_dtype, lse, B, T, Hq, Hkv,
                       num_blocks, max_q_len, max_seq_len, num_splits, workspace,
                       workspace_bytes, dev_status, stream);
+}
+
+int inkling_rel_attn_decode_sconv(const void* q, const void* k_raw, const void* v_raw,
+                                  const float* w_k, const float* w_v, void* sconv_state,
+                                  void* k_cache, void* v_cache, const int32_t* block_table,
+                                  int32_t max_blocks, const int32_t* cu_q_lens,
+                                  const int32_t* seq_lens, const float* bias, int32_t R,
+                                  float scale, int32_t window, void* out, int32_t out_dtype,
+                                  float* lse, int32_t B, int32_t T, int32_t Hq, int32_t Hkv,
+                                  int64_t num_blocks, int32_t max_q_len, int32_t max_seq_len,
+                                  int32_t num_splits, void* workspace, size_t workspace_bytes,
+                                  int32_t* dev_status, inkling_stream_t stream) {
+  if (!k_raw || !v_raw || !w_k || !w_v || !sconv_state) return INKLING_ERR_INVALID_ARG;
+  if (!aligned16(k_raw) || !aligned16(v_raw) || !aligned16(w_k) || !aligned16(w_v) ||
+      !aligned16(sconv_state))
+    return INKLING_ERR_INVALID_ARG;
+  AttnArgs conv{};
+  conv.conv_k_raw = k_raw;
+  conv.conv_v_raw = v_raw;
+  conv.conv_w_k = w_k;
+  conv.conv_w_v = w_v;
+  conv.conv_state = sconv_state;
+  return decode_entry(false, 1.f, 1.f, q, k_cache, v_cache, block_table, max_blocks, cu_q_lens,
+                      seq_lens, bias, R, scale, window, out, out_dtype, lse, B, T, Hq, Hkv,
+                      num_blocks, max_q_len, max_seq_len, num_splits, workspace,
+                      workspace_bytes, dev_status, stream, &conv);
 }
 
 int inkling_rel_attn_decode_fp8(const void* q, const void* k_cache, const void* v_cache,

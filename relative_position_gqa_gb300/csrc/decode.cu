@@ -16,6 +16,9 @@
 //               consumed, so a fast warp may finish page i+1 while a slow one is still on
 //               page i, and one barrier for both pages would complete too early.
 //   warps 0-3   thread r owns packed row r: bias, mask, online softmax, P, epilogue.
+//   warp 11     (the fused-conv call only) the sconv of the step's new K/V rows that fall
+//               in the CTA's pages, for its KV head's 128 channels, written into the
+//               cache before the producer loads those pages.
 // TMEM columns: Q [0,64), S0 [128,256), S1 [256,384), O [384,512).
 // A sequence whose key range fits one split writes its output directly; otherwise every
 // split writes (m, l, unnormalised O) to the workspace and combine_kernel merges them:
@@ -42,7 +45,7 @@ constexpr int kThreads = 384;
 constexpr int kLaunchRegs = 168, kSoftmaxRegs = 216, kOtherRegs = 64;
 static_assert(256 * kSoftmaxRegs + 128 * kOtherRegs <= kThreads * kLaunchRegs,
               "register split exceeds the launch allocation");
-constexpr int kWarpTma = 8, kWarpMma = 9, kWarpBias = 10, kWarpConv = 12;
+constexpr int kWarpTma = 8, kWarpMma = 9, kWarpBias = 10, kWarpConvRows = 11, kWarpConv = 12;
 // FP8 cache: two more warpgroups, warps 12-15 widen the E4M3 K pages and 16-19 the V
 // pages (32 rows each).  Widening a page with two warps took 0.8 us and, with one f16
 // page per tensor, set the page period (a clock64 trace: widen V(j) -> PV(j) -> widen
@@ -73,7 +76,7 @@ struct __align__(1024) Smem {
   float bias[kStages][kMaxG * kBiasStride];  // raw table values, staged per page by the bias warp
   // k_full / v_full: kStages bf16 stages or kStagesF8 (4) E4M3 stages
   uint64_t k_full[4], v_full[4], kv_empty[kStages], b_full[kStages], b_empty[kStages];
-  uint64_t q_ready, s_full[2], p_full[2], pv_done, o_full, drain;
+  uint64_t q_ready, s_full[2], p_full[2], pv_done, o_full, drain, conv_done;
   // the two column halves of a row trade partial maxima (per page parity), and at the
   // end their sums (in the slot of the parity after the last page's)
   uint64_t x_full[4][2], l_full;  // x_full[q]: warps q and q + 4 (the two halves of rows 32q..)
@@ -104,6 +107,11 @@ struct Params {
   int B, T, Hq, Hkv, G, max_q_len, rmax, num_splits, pages_per_split;
   long long num_blocks;
   float scale;
+  // the step's conv fused into the prologue (conv_x[0] == nullptr: conv done separately)
+  const uint16_t* conv_x[2];  // raw K, V rows of the new tokens [T][Hkv*128]
+  const float* conv_w[2];     // taps [Hkv*128][4]
+  uint16_t* conv_state;       // [B][2][3][Hkv*128], in/out
+  uint16_t* cache_w[2];       // the bf16 caches, written at the new rows' slots
 };
 
 // Key pages a sequence's decode rows can see: [kt_lo, kt_hi].
@@ -200,6 +208,12 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
   const int pg0 = kt_lo + split * p.pages_per_split;
   const int np = min(p.pages_per_split, kt_hi + 1 - pg0);
   const int rows = n * p.G;
+  // fused conv: the new rows t whose position L - n + t lies in this CTA's pages
+  const bool conv = !kFp8 && p.conv_x[0] != nullptr;
+  const int conv_t_lo = max(0, pg0 * 128 - (L - n));
+  const int conv_t_hi = min(n, (pg0 + np) * 128 - (L - n));
+  const bool conv_here = conv && conv_t_lo < conv_t_hi;
+  const int conv_page0 = (L - n + conv_t_lo) >> 7;  // the first page holding a new row
   // softmax warps that own packed rows; the others sit out (their TMEM lanes hold rows
   // nobody reads, and the MMA rows are independent of each other)
   const int nact = ((rows + 31) / 32) * 32;
@@ -240,6 +254,7 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
     mbar_init(&s.pv_done, 1);
     mbar_init(&s.o_full, 1);
     mbar_init(&s.drain, 1);
+    mbar_init(&s.conv_done, 1);
     if (kFp8) {
       for (int i = 0; i < kStagesF8; ++i) {
         if (i >= kStages) {  // the stages past the bf16 ring's
@@ -310,6 +325,13 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
           s.abort_flag = 1;
           break;
         }
+        // the pages holding new rows are read once the fused conv has written them
+        if (conv_here && pg0 + i == conv_page0 &&
+            !mbar_wait(&s.conv_done, 0, abort_flag, p.status)) {
+          report(p.status, kErrTimeout);
+          s.abort_flag = 1;
+          break;
+        }
         mbar_arrive_expect_tx(&s.k_full[st], 32768u);
         tma_load_3d_hint(s.k[st][0], &map_k, &s.k_full[st], 0, 0, page, pol);
         tma_load_3d_hint(s.k[st][1], &map_k, &s.k_full[st], 64, 0, page, pol);
@@ -357,6 +379,64 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
     if (!ok) {
       report(p.status, kErrTimeout);
       s.abort_flag = 1;
+    }
+  } else if (!kFp8 && warp == kWarpConvRows) {
+    // ------------------------------------------------------------ fused conv ---
+    // Lane l: channels 4l .. 4l+3 of this KV head, K then V, over the new rows up to the
+    // CTA's last one (earlier rows only feed the window of three).  The arithmetic and
+    // its order are those of the separate step conv, so the cache rows are bit-identical.
+    // The sequence's only CTA (one split) also writes the new state; with more splits the
+    // merge kernel does, once no CTA can still be reading the old one.
+    if (conv_here) {
+      const int C = p.Hkv * 128;
+      const int c = kvh * 128 + lane * 4;
+      auto bf = [](uint32_t w, int hi) { return __uint_as_float(hi ? (w & 0xffff0000u) : (w << 16)); };
+      for (int which = 0; which < 2; ++which) {
+        const uint16_t* x = p.conv_x[which];
+        const float* w = p.conv_w[which];
+        uint16_t* st = p.conv_state + ((size_t)b * 2 + which) * 3 * C + c;
+        float tap[4][4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float4 t4 = __ldg(reinterpret_cast<const float4*>(w + (size_t)(c + i) * 4));
+          tap[i][0] = t4.x; tap[i][1] = t4.y; tap[i][2] = t4.z; tap[i][3] = t4.w;
+        }
+        uint2 h0 = *reinterpret_cast<const uint2*>(st);
+        uint2 h1 = *reinterpret_cast<const uint2*>(st + C);
+        uint2 h2 = *reinterpret_cast<const uint2*>(st + 2 * C);
+        for (int t = 0; t < conv_t_hi; ++t) {
+          const uint2 cur = __ldg(reinterpret_cast<const uint2*>(x + (size_t)(t_seq0 + t) * C + c));
+          if (t >= conv_t_lo) {
+            float y[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const uint32_t w0 = i < 2 ? h0.x : h0.y, w1 = i < 2 ? h1.x : h1.y;
+              const uint32_t w2 = i < 2 ? h2.x : h2.y, w3 = i < 2 ? cur.x : cur.y;
+              float a = tap[i][0] * bf(w0, i & 1);
+              a = fmaf(tap[i][1], bf(w1, i & 1), a);
+              a = fmaf(tap[i][2], bf(w2, i & 1), a);
+              a = fmaf(tap[i][3], bf(w3, i & 1), a);
+              y[i] = a;
+            }
+            const int pos = L - n + t;
+            uint16_t* dst = p.cache_w[which] +
+                            (((size_t)table[pos >> 7] * p.Hkv + kvh) * 128 + (pos & 127)) * 128 + lane * 4;
+            *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]));
+          }
+          h0 = h1;
+          h1 = h2;
+          h2 = cur;
+        }
+        if (nsplit_b == 1) {  // conv_t_hi == n here: h0..h2 are the last three rows
+          *reinterpret_cast<uint2*>(st) = h0;
+          *reinterpret_cast<uint2*>(st + C) = h1;
+          *reinterpret_cast<uint2*>(st + 2 * C) = h2;
+        }
+      }
+      // the rows are read next by this CTA's TMA loads (the async proxy)
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.conv_done);
     }
   } else if (warp == kWarpBias) {
     // ------------------------------------------------------------ bias stager ---
@@ -763,6 +843,26 @@ combine_kernel(const Params p) {
   pdl_wait();
   const int t_seq0 = p.cu_q_lens[b];
   const int n = p.cu_q_lens[b + 1] - t_seq0;
+  if (p.conv_x[0] != nullptr && blockIdx.x == 0 && n > 0 && n <= p.max_q_len) {
+    // fused conv: the new state of a sequence split over several CTAs (they have all read
+    // the old one by now), the last three rows of [old state ; new rows], this KV head's
+    // 128 channels of K and V, one thread per channel
+    const int L = p.seq_lens[b];
+    int kt_lo, kt_hi;
+    page_range(L, n, p.window, kt_lo, kt_hi);
+    const int nsp = (kt_hi - kt_lo + 1 + p.pages_per_split - 1) / p.pages_per_split;
+    if (n <= L && L <= p.max_blocks * 128 && nsp > 1 && nsp <= p.num_splits) {
+      const int C = p.Hkv * 128;
+      const int which = threadIdx.x >> 7, c = kvh * 128 + (threadIdx.x & 127);
+      uint16_t* st = p.conv_state + ((size_t)b * 2 + which) * 3 * C + c;
+      uint16_t v[3];
+#pragma unroll
+      for (int k = 0; k < 3; ++k)
+        v[k] = n + k < 3 ? st[(size_t)(n + k) * C] : p.conv_x[which][(size_t)(t_seq0 + n + k - 3) * C + c];
+#pragma unroll
+      for (int k = 0; k < 3; ++k) st[(size_t)k * C] = v[k];
+    }
+  }
   if (n <= 0 || n > p.max_q_len || r >= n * p.G) return;
   const int L = p.seq_lens[b];
   if (n > L || L > p.max_blocks * 128) return;
@@ -890,6 +990,13 @@ cudaError_t launch_decode(const AttnArgs& a, const AttnMaps& maps, cudaStream_t 
   p.v_scale = a.kv_fp8 ? a.v_scale : 1.f;
   p.part_o = nullptr;
   p.part_ml = nullptr;
+  p.conv_x[0] = static_cast<const uint16_t*>(a.conv_k_raw);
+  p.conv_x[1] = static_cast<const uint16_t*>(a.conv_v_raw);
+  p.conv_w[0] = a.conv_w_k;
+  p.conv_w[1] = a.conv_w_v;
+  p.conv_state = static_cast<uint16_t*>(a.conv_state);
+  p.cache_w[0] = static_cast<uint16_t*>(const_cast<void*>(a.k_cache));
+  p.cache_w[1] = static_cast<uint16_t*>(const_cast<void*>(a.v_cache));
   if (a.num_splits > 1) {
     const size_t rows = (size_t)a.B * a.Hkv * a.num_splits * p.rmax;
     uintptr_t w = (reinterpret_cast<uintptr_t>(a.workspace) + 255) & ~uintptr_t(255);

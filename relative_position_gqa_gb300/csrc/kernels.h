@@ -98,6 +98,14 @@ struct AttnArgs {
   float k_scale = 1.f, v_scale = 1.f;
   // prefill only: factor on the output (v_scale when the pages were widened from FP8)
   float out_scale = 1.f;
+  // decode with the step's conv fused into its prologue (bf16 cache): the new tokens'
+  // raw K/V rows [T][Hkv*128], the taps [Hkv*128][4], the state [B][2][3][Hkv*128]
+  // (in/out); the new rows go into k_cache / v_cache at the slots the block table gives
+  const void* conv_k_raw = nullptr;
+  const void* conv_v_raw = nullptr;
+  const float* conv_w_k = nullptr;
+  const float* conv_w_v = nullptr;
+  void* conv_state = nullptr;
 };
 
 // Tensor maps built by the host for the attention kernels.

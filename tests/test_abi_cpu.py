@@ -76,6 +76,23 @@ def test_decode_host_checks(lib):
     assert _decode(lib, ws=None, wsb=0) == 7     # two splits need a workspace
 
 
+def _decode_sconv(lib, **over):
+    a = dict(q=FAKE, kr=FAKE, vr=FAKE, wk=FAKE, wv=FAKE, state=FAKE, k=FAKE, v=FAKE, bt=FAKE,
+             maxb=4, cu=FAKE, sl=FAKE, bias=FAKE, R=64, scale=0.1, window=0, out=FAKE, odt=0,
+             lse=None, B=1, T=10, Hq=8, Hkv=1, nb=4, mq=9, msl=500, ns=2, ws=None, wsb=0,
+             st=None, stream=None)
+    a.update(over)
+    return lib.inkling_rel_attn_decode_sconv(*a.values())
+
+
+def test_decode_sconv_host_checks(lib):
+    assert _decode_sconv(lib, kr=None) == 1          # the conv's inputs are required
+    assert _decode_sconv(lib, state=FAKE + 8) == 1   # and 16-byte aligned
+    assert _decode_sconv(lib, mq=10) == 1            # the decode's own checks follow
+    assert _decode_sconv(lib, Hq=32, Hkv=1) == 2
+    assert _decode_sconv(lib, ws=None, wsb=0) == 7
+
+
 def test_sconv_host_checks(lib):
     f = lib.inkling_sconv_kv
     assert f(None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 4, 1, 4, 4, None, None) == 1
