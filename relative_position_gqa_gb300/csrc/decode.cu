@@ -85,7 +85,6 @@ struct __align__(1024) Smem {
   uint64_t k8_empty[4], v8_empty[4], kh_full[2], kh_empty[2], vh_full[2], vh_empty[2];
   uint32_t tmem_base;
   int abort_flag;
-  int bad_block;
 };
 
 // 227 KB per CTA, with 1 KB of slack to align the dynamic buffer to 1024 bytes
@@ -119,6 +118,30 @@ __device__ __forceinline__ void page_range(int L, int n, int window, int& kt_lo,
   const int k_lo = window > 0 ? max(0, L - n - window + 1) : 0;
   kt_lo = k_lo >> 7;
   kt_hi = (L - 1) >> 7;
+}
+
+// Packed rows.  When G divides 32, every warp holds tokens of one parity: the even tokens
+// fill the first ceil(ceil(n/2) G / 32) warps and the odd tokens the next ones (with G = 8
+// and 9 tokens: 0 2 4 6 | 1 3 5 7 | 8), so that the bias pairs of a warp's threads share
+// one alignment (see the softmax).  Otherwise row r is token r / G, head r % G.  Rows
+// past a parity's tokens are padding: they take its last token and their lane's head.
+__host__ __device__ __forceinline__ int packed_warps(int n, int G) {
+  if (32 % G != 0) return (n * G + 31) / 32;
+  return ((n + 1) / 2 * G + 31) / 32 + (n / 2 * G + 31) / 32;
+}
+__device__ __forceinline__ bool packed_row(int r, int n, int G, int& t, int& g) {
+  if (32 % G != 0) {
+    t = min(r / G, n - 1);
+    g = r % G;
+    return r < n * G;
+  }
+  const int ne = (n + 1) / 2, we = (ne * G + 31) / 32;
+  const int w = r >> 5, par = w >= we ? 1 : 0;
+  const int k = ((w - par * we) * 32 + (r & 31)) / G;
+  const int cnt = par ? n / 2 : ne;
+  g = r % G;
+  t = 2 * min(k, cnt - 1) + par;
+  return k < cnt;
 }
 
 __device__ __forceinline__ uint64_t desc_k(const uint8_t (*atoms)[16384], int ks) {
@@ -207,7 +230,6 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
   }
   const int pg0 = kt_lo + split * p.pages_per_split;
   const int np = min(p.pages_per_split, kt_hi + 1 - pg0);
-  const int rows = n * p.G;
   // fused conv: the new rows t whose position L - n + t lies in this CTA's pages
   const bool conv = !kFp8 && p.conv_x[0] != nullptr;
   const int conv_t_lo = max(0, pg0 * 128 - (L - n));
@@ -216,24 +238,16 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
   const int conv_page0 = (L - n + conv_t_lo) >> 7;  // the first page holding a new row
   // softmax warps that own packed rows; the others sit out (their TMEM lanes hold rows
   // nobody reads, and the MMA rows are independent of each other)
-  const int nact = ((rows + 31) / 32) * 32;
+  const int nwarps = packed_warps(n, p.G);
+  const int nact = nwarps * 32;
   const int32_t* table = p.block_table + (size_t)b * p.max_blocks;
 
+  // Page ids are checked by whoever uses them first, before the use: the producer before
+  // each page's loads (ids read three pages ahead), the fused conv before its writes.  A
+  // bad id is reported (first error wins) and raises the abort flag, which stops the other
+  // roles; no access is made through it.
   if (threadIdx.x == 0) {
     s.abort_flag = 0;
-    s.bad_block = 0;
-  }
-  __syncthreads();
-  for (int i = threadIdx.x; i < np; i += (kFp8 ? kThreadsF8 : kThreads)) {
-    const int32_t blk = table[pg0 + i];
-    if (blk < 0 || (long long)blk >= p.num_blocks) s.bad_block = 1;
-  }
-  __syncthreads();
-  if (s.bad_block) {
-    if (threadIdx.x == 0) report(p.status, kErrBadBlock);
-    return;
-  }
-  if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&s.k_full[i], 1);
       mbar_init(&s.v_full[i], 1);
@@ -293,9 +307,21 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
       tma_prefetch_desc(&map_k);
       tma_prefetch_desc(&map_v);
       int issued = 0;
+      auto page_id = [&](int i) -> int32_t { return i < np ? table[pg0 + i] : 0; };
+      int32_t id1 = page_id(0), id2 = page_id(1), id3 = page_id(2);
       for (int i = 0; i < np; ++i) {
         const int st = i % NS;
-        const int page = table[pg0 + i] * p.Hkv + kvh;
+        const int32_t blk = id1;
+        id1 = id2;
+        id2 = id3;
+        id3 = page_id(i + 3);
+        if (blk < 0 || (long long)blk >= p.num_blocks) {
+          report(p.status, kErrBadBlock);
+          __threadfence();  // the report lands before any role that sees the flag reports
+          s.abort_flag = 1;
+          break;
+        }
+        const int page = blk * p.Hkv + kvh;
         if (kFp8) {
           // one 16 KB E4M3 box per K and V page; a stage is free once converted
           const uint32_t eph = ((i / NS) - 1) & 1;
@@ -419,9 +445,14 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
               y[i] = a;
             }
             const int pos = L - n + t;
-            uint16_t* dst = p.cache_w[which] +
-                            (((size_t)table[pos >> 7] * p.Hkv + kvh) * 128 + (pos & 127)) * 128 + lane * 4;
-            *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]));
+            const int32_t blk = table[pos >> 7];
+            if (blk < 0 || (long long)blk >= p.num_blocks) {
+              report(p.status, kErrBadBlock);  // no write; the producer stops at this page
+            } else {
+              uint16_t* dst = p.cache_w[which] +
+                              (((size_t)blk * p.Hkv + kvh) * 128 + (pos & 127)) * 128 + lane * 4;
+              *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]));
+            }
           }
           h0 = h1;
           h1 = h2;
@@ -588,7 +619,7 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
    }
   } else {
    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kFp8 ? kF8SoftmaxRegs : kSoftmaxRegs));
-   if ((warp & 3) * 32 < rows) {
+   if ((warp & 3) < nwarps) {
     // ------------------------------------------------------------ softmax group ---
     // Thread (r, hf): packed row r = TMEM lane, columns 64 hf .. 64 hf + 63 of S, P, O.
     // The two halves of a row trade their partial maxima through shared memory (an
@@ -598,12 +629,11 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
     const int r = (warp & 3) * 32 + lane;
     const int hf = warp >> 2, c0 = hf * 64;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const bool valid = r < rows;
-    // A padding row takes the head of its lane and the last token's position: its bias
-    // reads then fall on the words of valid rows (shared, not conflicting), so a warp's
-    // 32 lanes hit distinct banks.  Its Q is zero and nothing of it is stored.
-    const int t = min(r / p.G, n - 1);
-    const int g = r % p.G;
+    // A padding row takes the head of its lane and the last token of its warp's parity:
+    // its bias reads then fall on the words of valid rows (shared, not conflicting), so a
+    // warp's lanes hit distinct banks.  Its Q is zero and nothing of it is stored.
+    int t, g;
+    const bool valid = packed_row(r, n, p.G, t, g);
     const int h = kvh * p.G + g;
 
     // packed Q rows into TMEM columns [0, 64): this thread's half of the d range
@@ -667,6 +697,34 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
         for (int k = 0; k < 32; ++k)
           x[k] = __ffma2_rn(make_float2(__uint_as_float(sr[2 * k]), __uint_as_float(sr[2 * k + 1])),
                             sc2, bc2);
+      } else if (32 % p.G == 0) {
+        // pairs of columns by 8-byte loads.  The slot of column c0 is `base`; its parity
+        // is that of the token, so it is the same for the whole warp (packed_row).  base
+        // odd: the pair (c0 + 2k, c0 + 2k + 1) is the aligned word at base - 1 - 2k, higher
+        // column first.  base even: the aligned words at base - 2j hold (c0 + 2j,
+        // c0 + 2j - 1), so pair k takes the first half of word k and the second of word
+        // k + 1 (33 loads).  Slices 164 words (4 mod 32) apart put the 8 heads of a token
+        // on distinct bank pairs and token t + 2 two words over: a half-warp's 16 loads
+        // are conflict-free.
+        const int base = (pq - k0 - (dmin & ~3)) - c0;
+        const float* bb = bias_buf + g * kBiasStride + base;
+        if (base & 1) {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) {
+            const float2 w2 = *reinterpret_cast<const float2*>(bb - 1 - 2 * k);
+            x[k] = __ffma2_rn(make_float2(__uint_as_float(sr[2 * k]), __uint_as_float(sr[2 * k + 1])),
+                              sc2, make_float2(w2.y, w2.x));
+          }
+        } else {
+          float2 prev = *reinterpret_cast<const float2*>(bb);
+#pragma unroll
+          for (int k = 0; k < 32; ++k) {
+            const float2 nxt = *reinterpret_cast<const float2*>(bb - 2 - 2 * k);
+            x[k] = __ffma2_rn(make_float2(__uint_as_float(sr[2 * k]), __uint_as_float(sr[2 * k + 1])),
+                              sc2, make_float2(prev.x, nxt.y));
+            prev = nxt;
+          }
+        }
       } else {
         // slot of column c: distance pq - k0 - c minus the slice start a0
         const float* bp = bias_buf + g * kBiasStride + (pq - k0 - (dmin & ~3)) - c0;
@@ -863,7 +921,9 @@ combine_kernel(const Params p) {
       for (int k = 0; k < 3; ++k) st[(size_t)k * C] = v[k];
     }
   }
-  if (n <= 0 || n > p.max_q_len || r >= n * p.G) return;
+  if (n <= 0 || n > p.max_q_len || r >= p.rmax) return;
+  int t, g;
+  if (!packed_row(r, n, p.G, t, g)) return;
   const int L = p.seq_lens[b];
   if (n > L || L > p.max_blocks * 128) return;
   int kt_lo, kt_hi;
@@ -890,7 +950,7 @@ combine_kernel(const Params p) {
     lsum = fmaf(wgt, ml.y, lsum);
   }
   const float inv = 1.f / lsum;
-  const int t = r / p.G, h = kvh * p.G + r % p.G;
+  const int h = kvh * p.G + g;
   const size_t obase = ((size_t)(t_seq0 + t) * p.Hq + h) * 128 + lane * 4;
   if (p.out_dtype == 0) {
     uint2 w;
@@ -954,9 +1014,14 @@ DecodeSplit decode_split(int B, int Hkv, int max_q_len, int max_seq_len, int win
   return DecodeSplit{(int)ns, (int)pps};
 }
 
+// Rows of a packed tile for up to max_q_len tokens (whole warps when G divides 32).
+static int decode_rmax(int max_q_len, int G) {
+  return 32 % G == 0 ? 32 * decode::packed_warps(max_q_len, G) : max_q_len * G;
+}
+
 size_t decode_workspace_bytes(int B, int Hq, int Hkv, int max_q_len, int num_splits) {
   if (num_splits <= 1) return 0;
-  const size_t rmax = (size_t)max_q_len * (Hq / Hkv);
+  const size_t rmax = (size_t)decode_rmax(max_q_len, Hq / Hkv);
   const size_t rows = (size_t)B * Hkv * num_splits * rmax;
   return rows * 128 * sizeof(float) + rows * 2 * sizeof(float) + 256;
 }
@@ -982,7 +1047,7 @@ cudaError_t launch_decode(const AttnArgs& a, const AttnMaps& maps, cudaStream_t 
   p.Hkv = a.Hkv;
   p.G = a.Hq / a.Hkv;
   p.max_q_len = a.max_q_len;
-  p.rmax = a.max_q_len * p.G;
+  p.rmax = decode_rmax(a.max_q_len, p.G);
   p.num_splits = a.num_splits;
   p.pages_per_split = a.pages_per_split;
   p.num_blocks = a.num_blocks;
