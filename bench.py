@@ -1,7 +1,9 @@
 """Benchmark of the Inkling attention block on GB300.
 
-One step = the whole hot path over one batch: inkling_sconv_kv (K and V sconv into the
-paged cache) then the attention (inkling_rel_attn_prefill or inkling_rel_attn_decode).
+One step = the whole hot path over one batch: the sconv of the new K/V rows into the paged
+cache, then the attention.  Prefill: inkling_sconv_kv, then inkling_rel_attn_prefill.
+Decode over a bf16 cache: one call, inkling_rel_attn_decode_sconv (the conv in the decode
+kernel's prologue); the two separate calls are timed too (two_call_step).
 
 Default line (python bench.py): the 64K full-causal prefill, B=1 x 65536 new tokens, 64
 query / 8 KV heads, head dim 128, relative-bias table [64 x 8192], exactly --steps timed
@@ -196,11 +198,16 @@ class ClockSampler:
 # reports null.
 TRAFFIC = {
     (2, None): ("prefill.cu", "d31d6f8e751e8228fc8da767e6fc115591a23f4a4c322f748ccb23ef12e50c27",
-                611.4e6),
-    (4, "swa"): ("decode.cu", "d319709b06d5eca9b36ba83a40df24b32970b7a8e19fc792c299dd40f54c9bb3", 564.9e6),
-    (4, "swa_8k"): ("decode.cu", "d319709b06d5eca9b36ba83a40df24b32970b7a8e19fc792c299dd40f54c9bb3", 563.8e6),
-    (5, "n1"): ("decode.cu", "d319709b06d5eca9b36ba83a40df24b32970b7a8e19fc792c299dd40f54c9bb3", 4301.0e6),
-    (5, "n9_256k"): ("decode.cu", "d319709b06d5eca9b36ba83a40df24b32970b7a8e19fc792c299dd40f54c9bb3", 1079.9e6),
+                601.9e6),
+    # decode: captured on the small-context forms (swa_8k, n1_256k, n9_256k) and scaled to
+    # the full workloads by their algorithmic K/V bytes (the same for swa and swa_8k, 4x
+    # for the 1M-token decodes)
+    (4, "swa"): ("decode.cu", "49ece78672754038e6c41a82b631f587e7df51eaa452b9e5384762be8fa88dcb", 564.1e6),
+    (4, "swa_8k"): ("decode.cu", "49ece78672754038e6c41a82b631f587e7df51eaa452b9e5384762be8fa88dcb", 564.1e6),
+    (5, "n1"): ("decode.cu", "49ece78672754038e6c41a82b631f587e7df51eaa452b9e5384762be8fa88dcb", 4315.1e6),
+    (5, "n9"): ("decode.cu", "49ece78672754038e6c41a82b631f587e7df51eaa452b9e5384762be8fa88dcb", 4316.3e6),
+    (5, "n1_256k"): ("decode.cu", "49ece78672754038e6c41a82b631f587e7df51eaa452b9e5384762be8fa88dcb", 1078.8e6),
+    (5, "n9_256k"): ("decode.cu", "49ece78672754038e6c41a82b631f587e7df51eaa452b9e5384762be8fa88dcb", 1079.1e6),
 }
 
 
@@ -317,6 +324,23 @@ def measure_attn(ink, bench: Bench, n: int, variant, fp8: bool, steps: int, warm
         g.state.copy_(state0)
         flush_l2(bench.flush, bench.flush_sink)
 
+    # the decode step over a bf16 cache is one call: the conv of the new tokens fused into
+    # the decode kernel's prologue (inkling_rel_attn_decode_sconv); otherwise the two calls
+    fused_step = decode and not fp8
+
+    def fused():
+        ink.rel_attn_decode_sconv(g.q, g.k_raw, g.v_raw, g.w_k, g.w_v, g.state, g.k_cache,
+                                  g.v_cache, g.block_table, g.cu_q_lens, g.seq_lens, g.bias,
+                                  scale=spec.scale, window=spec.window, max_q_len=spec.max_q_len,
+                                  max_seq_len=spec.max_seq_len, out=out, workspace=workspace,
+                                  dev_status=status)
+
+    def two_calls():
+        sconv(g.k_raw, g.v_raw)
+        attn(g.q, out)
+
+    step_fn = fused if fused_step else two_calls
+
     def check():
         torch.cuda.synchronize()
         if int(status.item()) != 0:
@@ -339,10 +363,12 @@ def measure_attn(ink, bench: Bench, n: int, variant, fp8: bool, steps: int, warm
     # lasts MIN_TIMED_S, so that the clock sampler sees several samples
     for _ in range(warmup):
         reset()
-        sconv(g.k_raw, g.v_raw)
-        attn(g.q, out)
+        two_calls()
+        if fused_step:
+            reset()
+            fused()
     check()
-    probe = timed(lambda: (sconv(g.k_raw, g.v_raw), attn(g.q, out)), 3)
+    probe = timed(step_fn, 3)
     check()
     est_ms = mean_ms(probe)
     k = steps
@@ -357,7 +383,7 @@ def measure_attn(ink, bench: Bench, n: int, variant, fp8: bool, steps: int, warm
         torch.distributed.barrier()
     torch.cuda.synchronize()
     with ClockSampler(dev.index if dev.index is not None else 0) as clocks:
-        ev_step = timed(lambda: (sconv(g.k_raw, g.v_raw), attn(g.q, out)), k)
+        ev_step = timed(step_fn, k)
         torch.cuda.synchronize()
     ev_attn = []
     for i in range(k):
@@ -374,23 +400,12 @@ def measure_attn(ink, bench: Bench, n: int, variant, fp8: bool, steps: int, warm
         torch.distributed.barrier()
     step_ms, attn_ms, sconv_ms = mean_ms(ev_step), mean_ms(ev_attn), mean_ms(ev_sconv)
 
-    fused_ms = None
-    if decode and not fp8:
-        # the same step as one call: the conv of the new tokens fused into the decode
-        # kernel's prologue (inkling_rel_attn_decode_sconv)
-        def fused():
-            ink.rel_attn_decode_sconv(g.q, g.k_raw, g.v_raw, g.w_k, g.w_v, g.state, g.k_cache,
-                                      g.v_cache, g.block_table, g.cu_q_lens, g.seq_lens, g.bias,
-                                      scale=spec.scale, window=spec.window,
-                                      max_q_len=spec.max_q_len, max_seq_len=spec.max_seq_len,
-                                      out=out, workspace=workspace, dev_status=status)
-        for _ in range(warmup):
-            reset()
-            fused()
+    two_call_ms = None
+    if fused_step:
+        # the same step as the two separate calls (inkling_sconv_kv, then the decode)
+        ev_two = timed(two_calls, k)
         check()
-        ev_fused = timed(fused, k)
-        check()
-        fused_ms = mean_ms(ev_fused)
+        two_call_ms = mean_ms(ev_two)
 
     rollback_us = None
     if n == 4 and not fp8:
@@ -463,8 +478,8 @@ def measure_attn(ink, bench: Bench, n: int, variant, fp8: bool, steps: int, warm
     e2e_ms = mean_ms(ev_e2e)
     step_ms, attn_ms, e2e_ms, sconv_ms = max_over_ranks([step_ms, attn_ms, e2e_ms, sconv_ms],
                                                         ws, dev)
-    if fused_ms is not None:
-        fused_ms = max_over_ranks([fused_ms], ws, dev)[0]
+    if two_call_ms is not None:
+        two_call_ms = max_over_ranks([two_call_ms], ws, dev)[0]
 
     peaks, peak_src = measured_peaks()
     if decode:
@@ -483,7 +498,8 @@ def measure_attn(ink, bench: Bench, n: int, variant, fp8: bool, steps: int, warm
     achieved = work / (attn_ms * 1e-3) / scale_u
     roof.update({"achieved": round(achieved, 1), "peak": peak, "frac": round(achieved / peak, 4),
                  "traffic": kernel_traffic(n, variant, fp8)})
-    launches_per_step = 2 + (1 if (decode and plan["merge"]) or (fp8 and not decode) else 0)
+    launches_per_step = (1 if fused_step else 2) + (1 if (decode and plan["merge"]) or
+                                                      (fp8 and not decode) else 0)
     entry = {
         "workload": workload_name(spec) + (" kv=e4m3" if fp8 else ""),
         "value": round(ws * work / (step_ms * 1e-3) / scale_u, 3), "unit": unit,
@@ -501,11 +517,14 @@ def measure_attn(ink, bench: Bench, n: int, variant, fp8: bool, steps: int, warm
     }
     if decode:
         entry["decode_plan"] = plan
-    if fused_ms is not None:
-        entry["fused_step"] = {"value": round(ws * work / (fused_ms * 1e-3) / scale_u, 3),
-                               "unit": unit, "ms_per_step": round(fused_ms, 4),
-                               "path": "inkling_rel_attn_decode_sconv (conv in the decode "
-                                       "kernel's prologue)"}
+    entry["step_path"] = ("inkling_rel_attn_decode_sconv (the conv in the decode kernel's "
+                          "prologue)" if fused_step else
+                          f"inkling_sconv_kv{'_fp8' if fp8 else ''} + "
+                          f"inkling_rel_attn_{'decode' if decode else 'prefill'}{'_fp8' if fp8 else ''}")
+    if two_call_ms is not None:
+        entry["two_call_step"] = {"value": round(ws * work / (two_call_ms * 1e-3) / scale_u, 3),
+                                  "unit": unit, "ms_per_step": round(two_call_ms, 4),
+                                  "path": "inkling_sconv_kv + inkling_rel_attn_decode"}
     if rollback_us is not None:
         entry["rollback_us"] = rollback_us
     del g, out, workspace, host_in, dev_in, host_out
@@ -597,7 +616,8 @@ def run_ours(args, ws, rank, local):
         "data": "synthetic (seeded N(0,1) Q/K/V, N(0,0.5) sconv taps, N(0,sd) bias)",
         "config": line_config(spec, ws, fp8),
         "detail": {"attn_ms": main["attn_ms"], "sconv_ms": main["sconv_ms"],
-                   **({"fused_step": main["fused_step"]} if "fused_step" in main else {}),
+                   "step_path": main["step_path"],
+                   **({"two_call_step": main["two_call_step"]} if "two_call_step" in main else {}),
                    **({"decode_plan": main["decode_plan"]} if "decode_plan" in main else {}),
                    **({"rollback_us": main["rollback_us"]} if "rollback_us" in main else {})},
         "e2e": main["e2e"],
