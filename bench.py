@@ -202,12 +202,12 @@ TRAFFIC = {
     # decode: captured on the small-context forms (swa_8k, n1_256k, n9_256k) and scaled to
     # the full workloads by their algorithmic K/V bytes (the same for swa and swa_8k, 4x
     # for the 1M-token decodes)
-    (4, "swa"): ("decode.cu", "49ece78672754038e6c41a82b631f587e7df51eaa452b9e5384762be8fa88dcb", 564.1e6),
-    (4, "swa_8k"): ("decode.cu", "49ece78672754038e6c41a82b631f587e7df51eaa452b9e5384762be8fa88dcb", 564.1e6),
-    (5, "n1"): ("decode.cu", "49ece78672754038e6c41a82b631f587e7df51eaa452b9e5384762be8fa88dcb", 4315.1e6),
-    (5, "n9"): ("decode.cu", "49ece78672754038e6c41a82b631f587e7df51eaa452b9e5384762be8fa88dcb", 4316.3e6),
-    (5, "n1_256k"): ("decode.cu", "49ece78672754038e6c41a82b631f587e7df51eaa452b9e5384762be8fa88dcb", 1078.8e6),
-    (5, "n9_256k"): ("decode.cu", "49ece78672754038e6c41a82b631f587e7df51eaa452b9e5384762be8fa88dcb", 1079.1e6),
+    (4, "swa"): ("decode.cu", "6ab7497ba9b2b8bf9c632609eac7fb9ab51c0bb3518f1c799f24e7a3d44450a2", 564.1e6),
+    (4, "swa_8k"): ("decode.cu", "6ab7497ba9b2b8bf9c632609eac7fb9ab51c0bb3518f1c799f24e7a3d44450a2", 564.1e6),
+    (5, "n1"): ("decode.cu", "6ab7497ba9b2b8bf9c632609eac7fb9ab51c0bb3518f1c799f24e7a3d44450a2", 4315.1e6),
+    (5, "n9"): ("decode.cu", "6ab7497ba9b2b8bf9c632609eac7fb9ab51c0bb3518f1c799f24e7a3d44450a2", 4316.3e6),
+    (5, "n1_256k"): ("decode.cu", "6ab7497ba9b2b8bf9c632609eac7fb9ab51c0bb3518f1c799f24e7a3d44450a2", 1078.8e6),
+    (5, "n9_256k"): ("decode.cu", "6ab7497ba9b2b8bf9c632609eac7fb9ab51c0bb3518f1c799f24e7a3d44450a2", 1079.1e6),
 }
 
 

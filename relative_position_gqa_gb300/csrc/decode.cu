@@ -761,7 +761,11 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
       }
       mx0 = fmax3(mx0, x[30].x, x[30].y);
       mx1 = fmax3(mx1, x[31].x, x[31].y);
-      // the other half's maximum of this page
+      // the other half's maximum of this page.  Slot xm[i & 1][hf][r] is read only by the
+      // partner warp (hf ^ 1, the same lanes), and this thread writes it again at page i + 2
+      // only after both warps have passed page i + 1's exchange, which the partner enters
+      // after its read: ordering within the warp pair is enough, and the pairs need not
+      // wait for one another.
       const float pm = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
       s.xm[i & 1][hf][r] = pm;
       mbar_arrive(&s.x_full[warp & 3][i & 1]);
@@ -813,7 +817,8 @@ decode_kernel(const __grid_constant__ CUtensorMap map_k,
     const float l_mine = l2.x + l2.y;
     float l = l_mine;
     if (ok) {
-      // slot np % 2 was last used by page np - 2, whose reads page np - 1's exchange ordered
+      // slot np % 2 was last used by page np - 2, whose reads (by the partner warp only)
+      // page np - 1's exchange ordered
       s.xm[np & 1][hf][r] = l_mine;
       mbar_arrive(&s.l_full);
       ok = mbar_wait(&s.l_full, 0, abort_flag, p.status);
