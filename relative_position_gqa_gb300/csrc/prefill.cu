@@ -117,18 +117,58 @@ __device__ __forceinline__ uint64_t desc_v(const uint8_t (*atoms)[16384], int ks
   // 16 keys per MMA = 2048 bytes, the two d halves 16 KB apart.
   return sdesc_sw128(smem_u32(atoms[0]) + ks * 2048, 16384, 1024);
 }
-// The descriptor of k-step ks from that of k-step 0: only the start address moves, and
-// the address field counts 16-byte units (shared addresses stay far below its 2^18 B).
-__device__ __forceinline__ uint64_t step_kmajor(uint64_t d0, int ks) {
-  return d0 + (uint64_t)((ks >> 2) * 1024 + (ks & 3) * 2);
-}
-__device__ __forceinline__ uint64_t step_v(uint64_t d0, int ks) { return d0 + (uint64_t)(ks * 128); }
 // A value the compiler must treat as new at this point: keeps it from precomputing, and
-// holding in the issuer's few registers, all sixteen k-step descriptors of the Q tiles.
+// holding in the issuer's few registers, the k-step descriptors of the Q tiles.
 __device__ __forceinline__ uint64_t opaque(uint64_t x) {
   asm volatile("" : "+l"(x));
   return x;
 }
+
+// The MMA issue blocks.  Each issues the eight 16-wide k-steps of one product from the
+// lane that elect.sync picks, with every lane of the warp executing it (converged), in one
+// asm block that adds the k-step offsets itself.  Issued this way the warp keeps up one
+// MMA every ~40 cycles while the softmax warps on the same sub-partitions take most issue
+// slots; single-MMA statements under a lane-0 branch fell to one every 130-260 cycles
+// under the same load (measured with FFMA and softmax-like loops in the other warps).
+//
+// A k-step's descriptor is that of k-step 0 plus its start-address offset: the address
+// field counts 16-byte units, and shared addresses plus the offsets stay below its 2^18 B,
+// so the add never carries into the next field.
+//
+// S[d] = Q K^T: both operands K-major, two 64-column atoms 16 KB apart; k-step ks starts
+// (ks & 3) * 32 bytes into atom ks >> 2 (+2 and +1024 units).
+#define INK_QK_STEP(off)                                      \
+  "add.s64 ra, %1, " #off ";\n\tadd.s64 rb, %2, " #off ";\n\t" \
+  "@pe tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %3, pt;\n\t"
+__device__ __forceinline__ void qk_x8(uint32_t d, uint64_t a, uint64_t b) {
+  asm volatile(
+      "{\n\t.reg .pred pe, pf, pt;\n\t.reg .b64 ra, rb;\n\t"
+      "setp.ne.b32 pf, %4, %4;\n\tsetp.eq.b32 pt, %4, %4;\n\t"
+      "elect.sync _|pe, 0xffffffff;\n\t"
+      "@pe tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, pf;\n\t"
+      INK_QK_STEP(2) INK_QK_STEP(4) INK_QK_STEP(6) INK_QK_STEP(1024) INK_QK_STEP(1026)
+      INK_QK_STEP(1028) INK_QK_STEP(1030) "}" ::"r"(d),
+      "l"(a), "l"(b), "n"(kIdescQK), "r"(0)
+      : "memory");
+}
+// O[d] (+)= P V: P from TMEM columns p (8 columns, 16 keys, a k-step), V an MN-major B
+// operand whose k-steps are 2048 bytes apart (+128); the first k-step accumulates iff acc.
+#define INK_PV_STEP(po, bo)                                     \
+  "add.s32 rp, %1, " #po ";\n\tadd.s64 rb, %2, " #bo ";\n\t"    \
+  "@pe tcgen05.mma.cta_group::1.kind::f16 [%0], [rp], rb, %3, pt;\n\t"
+__device__ __forceinline__ void pv_x8(uint32_t d, uint32_t p, uint64_t b, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred pe, pa, pt;\n\t.reg .b64 rb;\n\t.reg .b32 rp;\n\t"
+      "setp.ne.b32 pa, %4, 0;\n\tsetp.eq.b32 pt, %4, %4;\n\t"
+      "elect.sync _|pe, 0xffffffff;\n\t"
+      "@pe tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, pa;\n\t"
+      INK_PV_STEP(8, 128) INK_PV_STEP(16, 256) INK_PV_STEP(24, 384) INK_PV_STEP(32, 512)
+      INK_PV_STEP(40, 640) INK_PV_STEP(48, 768) INK_PV_STEP(56, 896) "}" ::"r"(d),
+      "r"(p), "l"(b), "n"(kIdescPV), "r"(acc)
+      : "memory");
+}
+#undef INK_QK_STEP
+#undef INK_PV_STEP
 
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap map_q,
@@ -340,86 +380,73 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_q,
     asm volatile("cp.async.wait_all;" ::: "memory");
   } else if (warp == 9) {
     // ------------------------------------------------------------- MMA issuer ---
+    // The whole warp runs this loop converged (the issue blocks and their commits elect
+    // one lane); each wait's outcome is made warp-uniform before it is acted on.
     const uint64_t dq0 = desc_kmajor(s.q[0], 0), dq1 = desc_kmajor(s.q[1], 0);
-    // S[tmem_d] = Q K^T over the eight 16-wide k-steps of d = 128
     auto qk = [&](uint32_t tmem_d, uint64_t dq, const uint8_t (*k_atoms)[16384]) {
-      const uint64_t a = opaque(dq), b = desc_kmajor(k_atoms, 0);
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks)
-        umma_ss(tmem_d, step_kmajor(a, ks), step_kmajor(b, ks), kIdescQK, ks > 0);
+      qk_x8(tmem_d, opaque(dq), desc_kmajor(k_atoms, 0));
     };
-    // O[tmem_d] (+)= P V over eight 16-key k-steps, P read from TMEM columns tmem_p
     auto pv = [&](uint32_t tmem_d, uint32_t tmem_p, const uint8_t (*v_atoms)[16384], bool acc) {
-      const uint64_t b = desc_v(v_atoms, 0);
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks)
-        umma_ts(tmem_d, tmem_p + ks * 8, step_v(b, ks), kIdescPV, acc || ks > 0);
+      pv_x8(tmem_d, tmem_p, desc_v(v_atoms, 0), acc ? 1u : 0u);
     };
     bool ok = mbar_wait(&s.q_full, 0, abort_flag, p.status) && mbar_wait(&s.k_full[0], 0, abort_flag, p.status);
+    ok = __all_sync(0xffffffffu, ok);
     bool issued_any = false;
     if (ok) {
       // tile 0 holds the diagonal: keys past the end of the sequence are stale slots
       if ((kt_hi + 1) * kTile > L) zero_tail_rows(s.k[0], L - kt_hi * kTile, lane);
       tc_fence_after();
-      if (lane == 0) {
-        qk(tmem + 0, dq0, s.k[0]);
-        umma_commit(&s.s_full[0]);
-        if (has_b) {
-          qk(tmem + 128, dq1, s.k[0]);
-          umma_commit(&s.s_full[1]);
-        }
-        umma_commit(&s.k_empty[0]);  // tile 0's K has been read by both QK^T
+      qk(tmem + 0, dq0, s.k[0]);
+      umma_commit_elected(&s.s_full[0]);
+      if (has_b) {
+        qk(tmem + 128, dq1, s.k[0]);
+        umma_commit_elected(&s.s_full[1]);
       }
+      umma_commit_elected(&s.k_empty[0]);  // tile 0's K has been read by both QK^T
       issued_any = true;
-      __syncwarp();
     }
     for (int i = 0; ok && i < ntiles; ++i) {
       const int st = i % kStages;
       const uint32_t ph = (i / kStages) & 1;
       ok = mbar_wait(&s.p_full[0], i & 1, abort_flag, p.status) && mbar_wait(&s.v_full[st], ph, abort_flag, p.status);
+      ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       // keys past the end of the sequence: their P is 0, but junk V could be NaN
       if (i == 0 && (kt_hi + 1) * kTile > L) zero_tail_rows(s.v[st], L - kt_hi * kTile, lane);
       tc_fence_after();
-      if (lane == 0) pv(tmem + 256, tmem + 0, s.v[st], i > 0);
-      __syncwarp();
+      pv(tmem + 256, tmem + 0, s.v[st], i > 0);
       const bool more = i + 1 < ntiles;
       const int st1 = (i + 1) % kStages;
       if (more) {
         ok = mbar_wait(&s.k_full[st1], ((i + 1) / kStages) & 1, abort_flag, p.status);
+        ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
-        if (lane == 0) {
-          qk(tmem + 0, dq0, s.k[st1]);
-          umma_commit(&s.s_full[0]);
-        }
-        __syncwarp();
+        qk(tmem + 0, dq0, s.k[st1]);
+        umma_commit_elected(&s.s_full[0]);
       }
       if (has_b) {
         ok = mbar_wait(&s.p_full[1], i & 1, abort_flag, p.status);
+        ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
-        if (lane == 0) pv(tmem + 384, tmem + 128, s.v[st], i > 0);
-        __syncwarp();
+        pv(tmem + 384, tmem + 128, s.v[st], i > 0);
       }
-      if (lane == 0) {
-        umma_commit(&s.v_empty[st]);  // both PV of tile i are issued
-        if (has_b && more) {
-          qk(tmem + 128, dq1, s.k[st1]);
-          umma_commit(&s.s_full[1]);
-        }
-        if (more) umma_commit(&s.k_empty[st1]);  // both QK^T of tile i+1 are issued
+      umma_commit_elected(&s.v_empty[st]);  // both PV of tile i are issued
+      if (has_b && more) {
+        qk(tmem + 128, dq1, s.k[st1]);
+        umma_commit_elected(&s.s_full[1]);
       }
-      __syncwarp();
+      if (more) umma_commit_elected(&s.k_empty[st1]);  // both QK^T of tile i+1 are issued
     }
     if (ok) {
-      if (lane == 0) umma_commit(&s.o_full);
+      umma_commit_elected(&s.o_full);
     } else {
       report(p.status, kErrTimeout);
       s.abort_flag = 1;
       if (issued_any) {
         // wait for the tensor core to finish whatever was issued before freeing TMEM
-        if (lane == 0) umma_commit(&s.drain);
+        umma_commit_elected(&s.drain);
         __syncwarp();
         volatile int never = 0;
         mbar_wait(&s.drain, 0, &never);

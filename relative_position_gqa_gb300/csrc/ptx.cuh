@@ -194,6 +194,16 @@ __device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// The commit for MMAs issued by the lane that elect.sync picks in a converged warp (the
+// issue blocks of the attention kernels): the same full-mask election picks the same lane,
+// so the commit tracks those MMAs.  Called by every lane of the warp.
+__device__ __forceinline__ void umma_commit_elected(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
 // Arrive once on `bar` when every tcgen05 operation issued so far by this thread is done.
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile(
