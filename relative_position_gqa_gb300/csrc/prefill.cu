@@ -124,51 +124,6 @@ __device__ __forceinline__ uint64_t opaque(uint64_t x) {
   return x;
 }
 
-// The MMA issue blocks.  Each issues the eight 16-wide k-steps of one product from the
-// lane that elect.sync picks, with every lane of the warp executing it (converged), in one
-// asm block that adds the k-step offsets itself.  Issued this way the warp keeps up one
-// MMA every ~40 cycles while the softmax warps on the same sub-partitions take most issue
-// slots; single-MMA statements under a lane-0 branch fell to one every 130-260 cycles
-// under the same load (measured with FFMA and softmax-like loops in the other warps).
-//
-// A k-step's descriptor is that of k-step 0 plus its start-address offset: the address
-// field counts 16-byte units, and shared addresses plus the offsets stay below its 2^18 B,
-// so the add never carries into the next field.
-//
-// S[d] = Q K^T: both operands K-major, two 64-column atoms 16 KB apart; k-step ks starts
-// (ks & 3) * 32 bytes into atom ks >> 2 (+2 and +1024 units).
-#define INK_QK_STEP(off)                                      \
-  "add.s64 ra, %1, " #off ";\n\tadd.s64 rb, %2, " #off ";\n\t" \
-  "@pe tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %3, pt;\n\t"
-__device__ __forceinline__ void qk_x8(uint32_t d, uint64_t a, uint64_t b) {
-  asm volatile(
-      "{\n\t.reg .pred pe, pf, pt;\n\t.reg .b64 ra, rb;\n\t"
-      "setp.ne.b32 pf, %4, %4;\n\tsetp.eq.b32 pt, %4, %4;\n\t"
-      "elect.sync _|pe, 0xffffffff;\n\t"
-      "@pe tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, pf;\n\t"
-      INK_QK_STEP(2) INK_QK_STEP(4) INK_QK_STEP(6) INK_QK_STEP(1024) INK_QK_STEP(1026)
-      INK_QK_STEP(1028) INK_QK_STEP(1030) "}" ::"r"(d),
-      "l"(a), "l"(b), "n"(kIdescQK), "r"(0)
-      : "memory");
-}
-// O[d] (+)= P V: P from TMEM columns p (8 columns, 16 keys, a k-step), V an MN-major B
-// operand whose k-steps are 2048 bytes apart (+128); the first k-step accumulates iff acc.
-#define INK_PV_STEP(po, bo)                                     \
-  "add.s32 rp, %1, " #po ";\n\tadd.s64 rb, %2, " #bo ";\n\t"    \
-  "@pe tcgen05.mma.cta_group::1.kind::f16 [%0], [rp], rb, %3, pt;\n\t"
-__device__ __forceinline__ void pv_x8(uint32_t d, uint32_t p, uint64_t b, uint32_t acc) {
-  asm volatile(
-      "{\n\t.reg .pred pe, pa, pt;\n\t.reg .b64 rb;\n\t.reg .b32 rp;\n\t"
-      "setp.ne.b32 pa, %4, 0;\n\tsetp.eq.b32 pt, %4, %4;\n\t"
-      "elect.sync _|pe, 0xffffffff;\n\t"
-      "@pe tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, pa;\n\t"
-      INK_PV_STEP(8, 128) INK_PV_STEP(16, 256) INK_PV_STEP(24, 384) INK_PV_STEP(32, 512)
-      INK_PV_STEP(40, 640) INK_PV_STEP(48, 768) INK_PV_STEP(56, 896) "}" ::"r"(d),
-      "r"(p), "l"(b), "n"(kIdescPV), "r"(acc)
-      : "memory");
-}
-#undef INK_QK_STEP
-#undef INK_PV_STEP
 
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap map_q,
@@ -384,10 +339,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_q,
     // one lane); each wait's outcome is made warp-uniform before it is acted on.
     const uint64_t dq0 = desc_kmajor(s.q[0], 0), dq1 = desc_kmajor(s.q[1], 0);
     auto qk = [&](uint32_t tmem_d, uint64_t dq, const uint8_t (*k_atoms)[16384]) {
-      qk_x8(tmem_d, opaque(dq), desc_kmajor(k_atoms, 0));
+      mma8_ss_kmajor<kIdescQK>(tmem_d, opaque(dq), desc_kmajor(k_atoms, 0), 0);
     };
     auto pv = [&](uint32_t tmem_d, uint32_t tmem_p, const uint8_t (*v_atoms)[16384], bool acc) {
-      pv_x8(tmem_d, tmem_p, desc_v(v_atoms, 0), acc ? 1u : 0u);
+      mma8_ts_mnmajor<kIdescPV>(tmem_d, tmem_p, desc_v(v_atoms, 0), acc ? 1u : 0u);
     };
     bool ok = mbar_wait(&s.q_full, 0, abort_flag, p.status) && mbar_wait(&s.k_full[0], 0, abort_flag, p.status);
     ok = __all_sync(0xffffffffu, ok);

@@ -194,6 +194,67 @@ __device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// Eight-k-step MMA issue blocks: D[d] (+)= A B over the eight 16-wide k-steps of a
+// 128-deep product, issued from the lane that elect.sync picks, with every lane of the
+// warp executing the block (converged), in one asm statement that adds the k-step offsets
+// itself.  Issued this way a warp keeps up one MMA every ~40 cycles while other warps on
+// its sub-partition run FFMA/MUFU work; single-MMA statements under a lane-0 branch fell
+// to one every 130-260 cycles under the same load.  The first k-step accumulates iff
+// acc != 0, the others always.
+//
+// A k-step's descriptor is that of k-step 0 plus its start-address offset: the address
+// field counts 16-byte units, and shared addresses plus the offsets stay below its 2^18 B,
+// so the add never carries into the next field.  K-major operands are two 64-column
+// 128-byte-swizzled atoms 16 KB apart, k-step ks starting (ks & 3) * 32 bytes into atom
+// ks >> 2 (+2 and +1024 units); an MN-major B operand steps 16 rows = 2048 bytes (+128);
+// a TMEM A operand steps 8 columns (16 bf16/f16 values packed in pairs).
+#define INK_MMA_SS_STEP(off)                                  \
+  "add.s64 ra, %1, " #off ";\n\tadd.s64 rb, %2, " #off ";\n\t" \
+  "@pe tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %3, pt;\n\t"
+#define INK_MMA_TS_STEP(ao, bo)                                 \
+  "add.s32 rt, %1, " #ao ";\n\tadd.s64 rb, %2, " #bo ";\n\t"    \
+  "@pe tcgen05.mma.cta_group::1.kind::f16 [%0], [rt], rb, %3, pt;\n\t"
+#define INK_MMA_HEAD                                                   \
+  "setp.ne.b32 pa, %4, 0;\n\tsetp.eq.b32 pt, %4, %4;\n\t"             \
+  "elect.sync _|pe, 0xffffffff;\n\t"
+// A and B K-major in shared memory (S = Q K^T of the prefill).
+template <uint32_t kIdesc>
+__device__ __forceinline__ void mma8_ss_kmajor(uint32_t d, uint64_t a, uint64_t b, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred pe, pa, pt;\n\t.reg .b64 ra, rb;\n\t" INK_MMA_HEAD
+      "@pe tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, pa;\n\t"
+      INK_MMA_SS_STEP(2) INK_MMA_SS_STEP(4) INK_MMA_SS_STEP(6) INK_MMA_SS_STEP(1024)
+      INK_MMA_SS_STEP(1026) INK_MMA_SS_STEP(1028) INK_MMA_SS_STEP(1030) "}" ::"r"(d),
+      "l"(a), "l"(b), "n"(kIdesc), "r"(acc)
+      : "memory");
+}
+// A in TMEM, B K-major in shared memory (S = K Q^T of the decode: Q resident in TMEM).
+template <uint32_t kIdesc>
+__device__ __forceinline__ void mma8_ts_kmajor(uint32_t d, uint32_t a, uint64_t b, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred pe, pa, pt;\n\t.reg .b64 rb;\n\t.reg .b32 rt;\n\t" INK_MMA_HEAD
+      "@pe tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, pa;\n\t"
+      INK_MMA_TS_STEP(8, 2) INK_MMA_TS_STEP(16, 4) INK_MMA_TS_STEP(24, 6)
+      INK_MMA_TS_STEP(32, 1024) INK_MMA_TS_STEP(40, 1026) INK_MMA_TS_STEP(48, 1028)
+      INK_MMA_TS_STEP(56, 1030) "}" ::"r"(d),
+      "r"(a), "l"(b), "n"(kIdesc), "r"(acc)
+      : "memory");
+}
+// A in TMEM, B MN-major in shared memory (O += P V: P in TMEM, V rows = keys).
+template <uint32_t kIdesc>
+__device__ __forceinline__ void mma8_ts_mnmajor(uint32_t d, uint32_t a, uint64_t b, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred pe, pa, pt;\n\t.reg .b64 rb;\n\t.reg .b32 rt;\n\t" INK_MMA_HEAD
+      "@pe tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, pa;\n\t"
+      INK_MMA_TS_STEP(8, 128) INK_MMA_TS_STEP(16, 256) INK_MMA_TS_STEP(24, 384)
+      INK_MMA_TS_STEP(32, 512) INK_MMA_TS_STEP(40, 640) INK_MMA_TS_STEP(48, 768)
+      INK_MMA_TS_STEP(56, 896) "}" ::"r"(d),
+      "r"(a), "l"(b), "n"(kIdesc), "r"(acc)
+      : "memory");
+}
+#undef INK_MMA_SS_STEP
+#undef INK_MMA_TS_STEP
+#undef INK_MMA_HEAD
 // The commit for MMAs issued by the lane that elect.sync picks in a converged warp (the
 // issue blocks of the attention kernels): the same full-mask election picks the same lane,
 // so the commit tracks those MMAs.  Called by every lane of the warp.
