@@ -363,20 +363,23 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_q,
     for (int i = 0; ok && i < ntiles; ++i) {
       const int st = i % kStages;
       const uint32_t ph = (i / kStages) & 1;
-      ok = mbar_wait(&s.p_full[0], i & 1, abort_flag, p.status) && mbar_wait(&s.v_full[st], ph, abort_flag, p.status);
+      const bool more = i + 1 < ntiles;
+      const int st1 = (i + 1) % kStages;
+      // V(i) and K(i+1) have normally landed long before P_A(i) (their stages were freed
+      // a tile earlier): wait for them first, so that PV_A(i) and S_A(i+1) follow P_A(i)
+      // back to back.
+      ok = mbar_wait(&s.v_full[st], ph, abort_flag, p.status) &&
+           (!more || mbar_wait(&s.k_full[st1], ((i + 1) / kStages) & 1, abort_flag, p.status));
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       // keys past the end of the sequence: their P is 0, but junk V could be NaN
       if (i == 0 && (kt_hi + 1) * kTile > L) zero_tail_rows(s.v[st], L - kt_hi * kTile, lane);
+      ok = mbar_wait(&s.p_full[0], i & 1, abort_flag, p.status);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
       tc_fence_after();
       pv(tmem + 256, tmem + 0, s.v[st], i > 0);
-      const bool more = i + 1 < ntiles;
-      const int st1 = (i + 1) % kStages;
       if (more) {
-        ok = mbar_wait(&s.k_full[st1], ((i + 1) / kStages) & 1, abort_flag, p.status);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-        tc_fence_after();
         qk(tmem + 0, dq0, s.k[st1]);
         umma_commit_elected(&s.s_full[0]);
       }
