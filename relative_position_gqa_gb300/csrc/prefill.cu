@@ -135,12 +135,21 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_q,
   const int warp = warp_id(), lane = lane_id();
   pdl_wait();
 
-  // ---- work item: heavy (late) query tiles first, head pairs fastest ----
+  // ---- work item: one KV group after another, so that the CTAs resident at a time
+  // share the K/V of one or two groups (a group's whole history, 32 MB at 64K tokens,
+  // stays in L2 while they stream it) and each group's K/V is read from HBM about once;
+  // within a group, heavy (late) query tiles first, then sequences, then the group's
+  // head pairs ----
   const int idx = blockIdx.x;
-  const int hp = idx % p.head_pairs;
-  const int rest = idx / p.head_pairs;
-  const int b = rest % p.B;
-  const int qt = p.q_tiles - 1 - rest / p.B;
+  const int per_tile = p.B * p.pairs_per_group;  // items of one query tile and KV group
+  const int per_group = p.q_tiles * per_tile;
+  const int kvg = idx / per_group;
+  int rr = idx - kvg * per_group;
+  const int qt_rank = rr / per_tile;
+  rr -= qt_rank * per_tile;
+  const int b = rr / p.pairs_per_group;
+  const int hp = kvg * p.pairs_per_group + (rr - b * p.pairs_per_group);
+  const int qt = p.q_tiles - 1 - qt_rank;
   const int t_seq0 = p.cu_q_lens[b];
   const int n = p.cu_q_lens[b + 1] - t_seq0;
   if (qt * kTile >= n) return;  // whole CTA, before any barrier
