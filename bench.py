@@ -197,17 +197,19 @@ class ClockSampler:
 # taken on: when that source has changed since, the figure no longer applies and the line
 # reports null.
 TRAFFIC = {
-    (2, None): ("prefill.cu", "d31d6f8e751e8228fc8da767e6fc115591a23f4a4c322f748ccb23ef12e50c27",
-                601.9e6),
+    (2, None): ("prefill.cu", "a8b80591280b0d14262a5a37db5f80eb22dc265fd9eb67e7f0f4d441cfc76f99",
+                562.1e6),
+    (3, None): ("prefill.cu", "a8b80591280b0d14262a5a37db5f80eb22dc265fd9eb67e7f0f4d441cfc76f99",
+                2409.9e6),
     # decode: captured on the small-context forms (swa_8k, n1_256k, n9_256k) and scaled to
     # the full workloads by their algorithmic K/V bytes (the same for swa and swa_8k, 4x
     # for the 1M-token decodes)
-    (4, "swa"): ("decode.cu", "6ab7497ba9b2b8bf9c632609eac7fb9ab51c0bb3518f1c799f24e7a3d44450a2", 564.1e6),
-    (4, "swa_8k"): ("decode.cu", "6ab7497ba9b2b8bf9c632609eac7fb9ab51c0bb3518f1c799f24e7a3d44450a2", 564.1e6),
-    (5, "n1"): ("decode.cu", "6ab7497ba9b2b8bf9c632609eac7fb9ab51c0bb3518f1c799f24e7a3d44450a2", 4315.1e6),
-    (5, "n9"): ("decode.cu", "6ab7497ba9b2b8bf9c632609eac7fb9ab51c0bb3518f1c799f24e7a3d44450a2", 4316.3e6),
-    (5, "n1_256k"): ("decode.cu", "6ab7497ba9b2b8bf9c632609eac7fb9ab51c0bb3518f1c799f24e7a3d44450a2", 1078.8e6),
-    (5, "n9_256k"): ("decode.cu", "6ab7497ba9b2b8bf9c632609eac7fb9ab51c0bb3518f1c799f24e7a3d44450a2", 1079.1e6),
+    (4, "swa"): ("decode.cu", "04b49e1efa667743fab8fdcde3c794c6bb5a55114c1c8b72328e392bbe8eb0c2", 563.8e6),
+    (4, "swa_8k"): ("decode.cu", "04b49e1efa667743fab8fdcde3c794c6bb5a55114c1c8b72328e392bbe8eb0c2", 563.8e6),
+    (5, "n1"): ("decode.cu", "04b49e1efa667743fab8fdcde3c794c6bb5a55114c1c8b72328e392bbe8eb0c2", 4316.8e6),
+    (5, "n9"): ("decode.cu", "04b49e1efa667743fab8fdcde3c794c6bb5a55114c1c8b72328e392bbe8eb0c2", 4314.8e6),
+    (5, "n1_256k"): ("decode.cu", "04b49e1efa667743fab8fdcde3c794c6bb5a55114c1c8b72328e392bbe8eb0c2", 1079.2e6),
+    (5, "n9_256k"): ("decode.cu", "04b49e1efa667743fab8fdcde3c794c6bb5a55114c1c8b72328e392bbe8eb0c2", 1078.7e6),
 }
 
 
