@@ -17,7 +17,9 @@ names:
   - P to E4M3 as e4m3(P * 448) (P <= 1, so the codes span the format's range), PV with
     those codes, O = sum_j (p8_j / 448) V_j / l with l the fp32 sum of P (variant "l=P") or
     of the rounded P (variant "l=p8").
-Variants: Q in FP8 only (P kept bf16 as the shipped kernels do), P in FP8 only, both.
+Variants: Q in FP8 only (P kept bf16 as the shipped kernels do), P in FP8 only, both; and
+Q and/or P as the sum of two E4M3 terms at one scale, x ~ (e4m3(x/s) + e4m3(x/s - e4m3(x/s))) s,
+which two FP8 MMAs would accumulate into one fp32 result (K and V read as E4M3 directly).
 
 python tests/fp8_qp_error.py [--workload 2|3] [--rows N] [--seed S]
 """
@@ -46,17 +48,27 @@ def e4m3(x: np.ndarray) -> np.ndarray:
     return t.to(torch.float8_e4m3fn).to(torch.float64).numpy()
 
 
+def e4m3_split(x: np.ndarray, s: float) -> np.ndarray:
+    """x as the sum of two E4M3 terms at scale s: a leading code and the code of its residual."""
+    hi = e4m3(x / s)
+    return (hi + e4m3(x / s - hi)) * s
+
+
 def bf16(x: np.ndarray) -> np.ndarray:
     return torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16).to(torch.float64).numpy()
 
 
-def emulate_row(q, kcodes, vcodes, bias_row, R, p, window, scale, q_fp8, p_fp8, l_from_p8):
+def emulate_row(q, kcodes, vcodes, bias_row, R, p, window, scale, q_fp8, p_fp8, l_from_p8,
+                split=False):
     """One query row of one head: q [128] (bf16 values), kcodes/vcodes [L, 128] (E4M3
     values), keys 0..L-1 at positions 0..L-1, the query at position p."""
     lo = 0 if window <= 0 else max(0, p - window + 1)
     if q_fp8:
         s_q = np.abs(q).max() / 448.0
-        qq = e4m3(q / s_q) * s_q if s_q > 0 else q
+        if s_q <= 0:
+            qq = q
+        else:
+            qq = e4m3_split(q, s_q) if split else e4m3(q / s_q) * s_q
     else:
         qq = q
     m, l = -math.inf, 0.0
@@ -76,7 +88,7 @@ def emulate_row(q, kcodes, vcodes, bias_row, R, p, window, scale, q_fp8, p_fp8, 
         m = m_new
         pj = np.exp(x - m)
         if p_fp8:
-            pq = e4m3(pj * 448.0) / 448.0
+            pq = e4m3_split(pj, 1.0 / 448.0) if split else e4m3(pj * 448.0) / 448.0
         else:
             pq = bf16(pj)
         o += pq @ (vcodes[j0:j1] * VS)
@@ -115,7 +127,10 @@ def main():
     heads = rng.choice(spec.hq, size=min(args.heads, spec.hq), replace=False)
     variants = {"Q fp8, P bf16": (True, False, False), "Q bf16, P fp8 (l=P)": (False, True, False),
                 "Q bf16, P fp8 (l=p8)": (False, True, True), "Q fp8, P fp8 (l=p8)": (True, True, True),
-                "Q bf16, P bf16 (shipped)": (False, False, False)}
+                "Q bf16, P bf16 (shipped)": (False, False, False),
+                "Q 2xfp8, P bf16": (True, False, False, True),
+                "Q bf16, P 2xfp8 (l=P)": (False, True, False, True),
+                "Q 2xfp8, P 2xfp8 (l=P)": (True, True, False, True)}
     errs = {k: [] for k in variants}
     qf = c.q.to(torch.float64).numpy()
     bias = c.bias.to(torch.float64).numpy()
@@ -125,9 +140,8 @@ def main():
         vv = f8(vc[pages, kvh]).reshape(-1, 128).numpy()
         for i, t in enumerate(rows):
             p = spec.seq_lens[0] - n + t
-            for name, (qf8, pf8, lp8) in variants.items():
-                o = emulate_row(qf[t, h], kk, vv, bias[h], spec.r, p, spec.window, spec.scale,
-                                qf8, pf8, lp8)
+            for name, v in variants.items():
+                o = emulate_row(qf[t, h], kk, vv, bias[h], spec.r, p, spec.window, spec.scale, *v)
                 errs[name].append(np.abs(o - ref[i, h]))
     print(f"workload {args.workload} ({spec.name}): {len(rows)} rows x {len(heads)} heads, "
           f"E4M3 cache, bar max 1e-2 / mean 1e-3")
