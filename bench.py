@@ -197,19 +197,19 @@ class ClockSampler:
 # taken on: when that source has changed since, the figure no longer applies and the line
 # reports null.
 TRAFFIC = {
-    (2, None): ("prefill.cu", "a8b80591280b0d14262a5a37db5f80eb22dc265fd9eb67e7f0f4d441cfc76f99",
+    (2, None): ("prefill.cu", "2f8a9615a16ad800df7c4bba4534fb17996b6fc65041fd3cdc44a1ba2f7e8ce2",
                 562.1e6),
-    (3, None): ("prefill.cu", "a8b80591280b0d14262a5a37db5f80eb22dc265fd9eb67e7f0f4d441cfc76f99",
+    (3, None): ("prefill.cu", "2f8a9615a16ad800df7c4bba4534fb17996b6fc65041fd3cdc44a1ba2f7e8ce2",
                 2409.9e6),
     # decode: captured on the small-context forms (swa_8k, n1_256k, n9_256k) and scaled to
     # the full workloads by their algorithmic K/V bytes (the same for swa and swa_8k, 4x
     # for the 1M-token decodes)
-    (4, "swa"): ("decode.cu", "04b49e1efa667743fab8fdcde3c794c6bb5a55114c1c8b72328e392bbe8eb0c2", 563.8e6),
-    (4, "swa_8k"): ("decode.cu", "04b49e1efa667743fab8fdcde3c794c6bb5a55114c1c8b72328e392bbe8eb0c2", 563.8e6),
-    (5, "n1"): ("decode.cu", "04b49e1efa667743fab8fdcde3c794c6bb5a55114c1c8b72328e392bbe8eb0c2", 4316.8e6),
-    (5, "n9"): ("decode.cu", "04b49e1efa667743fab8fdcde3c794c6bb5a55114c1c8b72328e392bbe8eb0c2", 4314.8e6),
-    (5, "n1_256k"): ("decode.cu", "04b49e1efa667743fab8fdcde3c794c6bb5a55114c1c8b72328e392bbe8eb0c2", 1079.2e6),
-    (5, "n9_256k"): ("decode.cu", "04b49e1efa667743fab8fdcde3c794c6bb5a55114c1c8b72328e392bbe8eb0c2", 1078.7e6),
+    (4, "swa"): ("decode.cu", "5c022f1d15b6f440fa1d162d679b9393382f7e18ed02446048c3048227780e4a", 563.8e6),
+    (4, "swa_8k"): ("decode.cu", "5c022f1d15b6f440fa1d162d679b9393382f7e18ed02446048c3048227780e4a", 563.8e6),
+    (5, "n1"): ("decode.cu", "5c022f1d15b6f440fa1d162d679b9393382f7e18ed02446048c3048227780e4a", 4316.8e6),
+    (5, "n9"): ("decode.cu", "5c022f1d15b6f440fa1d162d679b9393382f7e18ed02446048c3048227780e4a", 4314.8e6),
+    (5, "n1_256k"): ("decode.cu", "5c022f1d15b6f440fa1d162d679b9393382f7e18ed02446048c3048227780e4a", 1079.2e6),
+    (5, "n9_256k"): ("decode.cu", "5c022f1d15b6f440fa1d162d679b9393382f7e18ed02446048c3048227780e4a", 1078.7e6),
 }
 
 

@@ -7,18 +7,23 @@
 // and G = 8), so each K/V page is read from HBM once per KV head.  The packed Q lives in
 // tensor memory (64 columns of bf16 pairs) and both contractions run on the tensor core:
 // S = Q K^T with Q from TMEM (TS form), O += P V with P from TMEM.
-//   warp 4      TMA producer: K/V pages of the split (three-stage ring of 64 KB).
-//   warp 6      bias stager: cp.async each page's bias slices (G heads) into a ring of
-//               its own, whose slots the softmax frees as soon as it has added the bias,
-//               so the slices of later pages load while the current one is processed.
-//   warp 5      MMA issuer; S is double-buffered so S(i+1) overlaps softmax(i).  Page i's
+//   warps 0-7   softmax: the pair w, w + 4 shares packed rows 32 (w % 4) .. + 31 (their
+//               TMEM lanes) and splits their 128 columns, trading partial maxima once
+//               per page; thread (r, half) does bias, mask, online softmax, P and the
+//               epilogue for its 64 columns of row r.
+//   warp 8      TMA producer: K/V pages of the split (three-stage ring of 64 KB).
+//   warp 9      MMA issuer; S is double-buffered so S(i+1) overlaps softmax(i).  Page i's
 //               "P ready" barrier is p_full[i & 1]: S(i+1) is issued before P(i) is
 //               consumed, so a fast warp may finish page i+1 while a slow one is still on
-//               page i, and one barrier for both pages would complete too early.
-//   warps 0-3   thread r owns packed row r: bias, mask, online softmax, P, epilogue.
+//               page i, and one barrier for both pages would complete too early.  Over a
+//               bf16 cache each product's eight k-steps are one elected asm block.
+//   warp 10     bias stager: cp.async each page's bias slices (G heads) into a ring of
+//               its own, whose slots the softmax frees as soon as it has added the bias,
+//               so the slices of later pages load while the current one is processed.
 //   warp 11     (the fused-conv call only) the sconv of the step's new K/V rows that fall
 //               in the CTA's pages, for its KV head's 128 channels, written into the
 //               cache before the producer loads those pages.
+//   warps 12-19 (FP8 cache only) converters: E4M3 pages widened to f16 for the MMAs.
 // TMEM columns: Q [0,64), S0 [128,256), S1 [256,384), O [384,512).
 // A sequence whose key range fits one split writes its output directly; otherwise every
 // split writes (m, l, unnormalised O) to the workspace and combine_kernel merges them:
@@ -36,7 +41,8 @@ namespace decode {
 
 constexpr int kStages = 3;
 // Warps 0-7 softmax (the pair w, w+4 shares TMEM lanes 32(w%4).. and splits the 128
-// columns of those rows), 8 TMA producer, 9 MMA issuer, 10 bias stager, 11 idle.
+// columns of those rows), 8 TMA producer, 9 MMA issuer, 10 bias stager, 11 the fused
+// conv (idle in the plain decode).
 // Register split (setmaxnreg): built for 168 registers a thread at launch (65536 / 384),
 // the two softmax warpgroups grow to 216 and the third gives back down to 64:
 // 256*216 + 128*64 = 63488 <= 384*168.  The host refuses the launch unless the built

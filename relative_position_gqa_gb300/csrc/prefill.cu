@@ -8,9 +8,10 @@
 //
 // Design (one CTA = 128 query tokens x two query heads of one KV group):
 //   warp 8      TMA producer: Q tiles once, then K and V pages (two-stage ring).
-//   warp 9      MMA issuer (one thread): S = Q K^T (SS form), O += P V (P read from
-//               tensor memory, TS form), commits to mbarriers.  Owns the TMEM allocation.
-//               Its k-step descriptors are stepped from one base per tile.
+//   warp 9      MMA issuer: S = Q K^T (SS form), O += P V (P read from tensor memory,
+//               TS form), each product's eight k-steps issued by the lane elect.sync
+//               picks from one asm block (mma8_*), commits to mbarriers.  Owns the TMEM
+//               allocation.  Waits for V(i) and K(i+1) before P_A(i).
 //   warps 10-11 bias stagers (one per head): stage the tile's slice of the bias table
 //               in shared memory, one stage ahead (one bulk copy expanded into four
 //               shifted copies, or 4-byte cp.async where entries need clamping).
@@ -20,7 +21,7 @@
 //               more than 2^8), writes P as bf16 over the S columns, and finally
 //               normalises O and stores it.
 // Tensor memory (512 columns): S_A [0,128) S_B [128,256) O_A [256,384) O_B [384,512);
-// P_X overlays the first 64 columns of S_X.  The MMA thread issues
+// P_X overlays the first 64 columns of S_X.  The issuer issues
 //   S_A0 S_B0 | PV_A0 S_A1 | PV_B0 S_B1 | PV_A1 S_A2 | ...
 // so each softmax group works while the tensor core serves the other (ping-pong).
 //
