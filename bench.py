@@ -439,11 +439,12 @@ def measure_attn(ink, bench: Bench, n: int, variant, fp8: bool, steps: int, warm
     d2h = host_out.numel() * host_out.element_size()
     cu_host = g.cu_q_lens.cpu()
     up, down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-    # prefill: eight groups (a long sequence is cut into pieces of whole query tiles, so
-    # the 64K prefill overlaps its copies too).  decode: one group (its copies are a few
+    # prefill: sixteen groups (a long sequence is cut into pieces of whole query tiles, so
+    # the 64K prefill overlaps its copies too; 4 / 8 / 16 groups measured 1412 / 1419 /
+    # 1428 TFLOP/s end to end on it, 647 / 689 / 691 on the window prefill).  decode: one group (its copies are a few
     # MB, and cutting the batch gives each group its own tail of ragged lengths: two groups
     # measured 1.66 ms on the full MTP decode against 1.41 ms for one)
-    chunks = e2e_chunks if e2e_chunks > 0 else (1 if decode else 8)
+    chunks = e2e_chunks if e2e_chunks > 0 else (1 if decode else 16)
     if fp8:
         e2e_path = (f"copies + sconv_kv_fp8 + rel_attn_{'decode' if decode else 'prefill'}_fp8, "
                     "serial")
@@ -861,7 +862,7 @@ def main():
                     help="oracle seconds per reference step / for the cpu_baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-chunks", type=int, default=0,
-                    help="groups for the end-to-end host-buffer step (0: 8 for prefill, 1 for decode)")
+                    help="groups for the end-to-end host-buffer step (0: 16 for prefill, 1 for decode)")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per launch of the dominant kernel from an ncu capture")
     args = ap.parse_args()

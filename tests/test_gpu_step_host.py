@@ -57,11 +57,12 @@ PREFILL = W.small(q_lens=(150, 37, 0, 300, 9), seq_lens=(150, 200, 40, 300, 600)
 DECODE = W.small(q_lens=(9, 9, 3, 1), seq_lens=(500, 700, 129, 1000), hq=8, hkv=1, r=64)
 
 
-@pytest.mark.parametrize("chunks", [1, 2, 3, 8])
+@pytest.mark.parametrize("chunks", [1, 2, 3, 8, 16])
 @pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
 def test_prefill_step_host_bit_identical(ink, chunks, out_dtype):
-    """With 3 or 8 groups the 150- and 300-token sequences are cut into pieces of whole
-    query tiles (chunked prefills of one sequence); the bits must not change."""
+    """With 3, 8 or 16 groups the 150- and 300-token sequences are cut into pieces of whole
+    query tiles (chunked prefills of one sequence; 16 asks for more pieces than the query
+    tiles allow); the bits must not change."""
     a = W.make_case(PREFILL, seed=5, device="cuda")
     b = W.make_case(PREFILL, seed=5, device="cuda")
     ref, ref_lse = _device_step(ink, a, decode=False, out_dtype=out_dtype)
