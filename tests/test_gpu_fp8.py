@@ -128,6 +128,25 @@ def test_decode_fp8_ignores_stale_nan_slots(ink):
     _decode_both(ink, CASES["mixed_n"], seed=84, num_splits=2, nan_tail=True)
 
 
+@pytest.mark.parametrize("num_splits", [1, 3])
+def test_decode_fp8_bad_block_reported(ink, num_splits):
+    """A page id past the cache in a sequence's visible range comes back as
+    INKLING_ERR_BAD_BLOCK: the converter warps check each id before they read the page."""
+    spec = CASES["mixed_n"]
+    c = _fp8_case(spec, seed=86)
+    g, _, _, _ = _sconv_both(ink, c)
+    L = spec.seq_lens[3]
+    g.block_table[3, (L - 1) // 128 - 2] = g.k_cache.shape[0]  # inside sequence 3's range
+    out = torch.empty(spec.total_q, spec.hq, 128, dtype=torch.float32, device="cuda")
+    st = _status()
+    ink.rel_attn_decode_fp8(g.q, g.k_cache, g.v_cache, g.block_table, g.cu_q_lens, g.seq_lens,
+                            g.bias, k_scale=K_SCALE, v_scale=V_SCALE, scale=spec.scale,
+                            window=0, max_q_len=spec.max_q_len, max_seq_len=spec.max_seq_len,
+                            out=out, num_splits=num_splits, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 5  # INKLING_ERR_BAD_BLOCK
+
+
 def test_decode_fp8_rejects_bad_scale(ink):
     spec = CASES["g1_n9"]
     c = _fp8_case(spec, seed=85).to("cuda")
