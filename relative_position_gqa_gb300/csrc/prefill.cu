@@ -23,7 +23,9 @@
 // Tensor memory (512 columns): S_A [0,128) S_B [128,256) O_A [256,384) O_B [384,512);
 // P_X overlays the first 64 columns of S_X.  The issuer issues
 //   S_A0 S_B0 | PV_A0 S_A1 | PV_B0 S_B1 | PV_A1 S_A2 | ...
-// so each softmax group works while the tensor core serves the other (ping-pong).
+// so each softmax group works while the tensor core serves the other (ping-pong).  Each
+// head's O is signalled right after its own last PV, so head A's epilogue runs while head
+// B finishes its last tile.
 //
 // The relative bias ("sheared" along the tile diagonals): within a 128x128 tile the
 // distance is delta + r - c with delta = p0 - k0, so row r needs a contiguous run of the
@@ -89,7 +91,7 @@ struct __align__(1024) Smem {
   // a K stage is free once the tile's last QK^T is done, a V stage once its last PV is
   // done: K for the next tile is fetched while the current tile's softmax and PV run
   uint64_t k_full[kStages], v_full[kStages], k_empty[kStages], v_empty[kStages];
-  uint64_t s_full[2], p_full[2], o_full, drain, b_full[kStages];
+  uint64_t s_full[2], p_full[2], o_full[2], drain, b_full[kStages];
   uint64_t raw_full[kStages][2];
   uint32_t tmem_base;
   int abort_flag;
@@ -189,7 +191,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_q,
       mbar_init(&s.s_full[i], 1);
       mbar_init(&s.p_full[i], 128);
     }
-    mbar_init(&s.o_full, 1);
+    mbar_init(&s.o_full[0], 1);
+    mbar_init(&s.o_full[1], 1);
     mbar_init(&s.drain, 1);
     fence_barrier_init();
   }
@@ -389,6 +392,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_q,
       if (!ok) break;
       tc_fence_after();
       pv(tmem + 256, tmem + 0, s.v[st], i > 0);
+      if (!more) umma_commit_elected(&s.o_full[0]);  // head A's O is final
       if (more) {
         qk(tmem + 0, dq0, s.k[st1]);
         umma_commit_elected(&s.s_full[0]);
@@ -399,6 +403,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_q,
         if (!ok) break;
         tc_fence_after();
         pv(tmem + 384, tmem + 128, s.v[st], i > 0);
+        if (!more) umma_commit_elected(&s.o_full[1]);
       }
       umma_commit_elected(&s.v_empty[st]);  // both PV of tile i are issued
       if (has_b && more) {
@@ -407,9 +412,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_q,
       }
       if (more) umma_commit_elected(&s.k_empty[st1]);  // both QK^T of tile i+1 are issued
     }
-    if (ok) {
-      umma_commit_elected(&s.o_full);
-    } else {
+    if (!ok) {
       report(p.status, kErrTimeout);
       s.abort_flag = 1;
       if (issued_any) {
@@ -545,7 +548,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_q,
         mbar_arrive(&s.p_full[grp]);
       }
       const float l = l2.x + l2.y;
-      if (ok) ok = mbar_wait(&s.o_full, 0, abort_flag, p.status);
+      if (ok) ok = mbar_wait(&s.o_full[grp], 0, abort_flag, p.status);
       if (!ok) {
         report(p.status, kErrTimeout);
         s.abort_flag = 1;
