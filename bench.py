@@ -197,10 +197,10 @@ class ClockSampler:
 # taken on: when that source has changed since, the figure no longer applies and the line
 # reports null.
 TRAFFIC = {
-    (2, None): ("prefill.cu", "2f8a9615a16ad800df7c4bba4534fb17996b6fc65041fd3cdc44a1ba2f7e8ce2",
-                562.1e6),
-    (3, None): ("prefill.cu", "2f8a9615a16ad800df7c4bba4534fb17996b6fc65041fd3cdc44a1ba2f7e8ce2",
-                2409.9e6),
+    (2, None): ("prefill.cu", "8dd95e6094469a10dd713dcb5f27c753c376a317c5928be4a0492058e1ad8105",
+                562.07e6),
+    (3, None): ("prefill.cu", "8dd95e6094469a10dd713dcb5f27c753c376a317c5928be4a0492058e1ad8105",
+                2405.9e6),
     # decode: captured on the small-context forms (swa_8k, n1_256k, n9_256k) and scaled to
     # the full workloads by their algorithmic K/V bytes (the same for swa and swa_8k, 4x
     # for the 1M-token decodes)
