@@ -428,10 +428,9 @@ def measure_attn(ink, bench: Bench, n: int, variant, fp8: bool, steps: int, warm
         rollback_us = round(1e3 * mean_ms(rb), 2)
 
     # ---- end to end through the public API with host buffers: the step entry points
-    # (inkling_prefill_step_host / inkling_decode_step_host) take page-locked Q, raw K/V
-    # and output buffers and overlap the copies of one group of sequences with the
-    # compute of another; the FP8 cache has no such entry, so there the copies and the
-    # two calls are issued one after another.
+    # (inkling_prefill_step_host / inkling_decode_step_host and their _fp8 forms) take
+    # page-locked Q, raw K/V and output buffers and overlap the copies of one group of
+    # sequences with the compute of another.
     host_in = [t.cpu().pin_memory() for t in (g.q, g.k_raw, g.v_raw)]
     dev_in = [torch.empty_like(t, device=dev) for t in host_in]
     host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
@@ -445,23 +444,22 @@ def measure_attn(ink, bench: Bench, n: int, variant, fp8: bool, steps: int, warm
     # MB, and cutting the batch gives each group its own tail of ragged lengths: two groups
     # measured 1.66 ms on the full MTP decode against 1.41 ms for one)
     chunks = e2e_chunks if e2e_chunks > 0 else (1 if decode else 16)
-    if fp8:
-        e2e_path = (f"copies + sconv_kv_fp8 + rel_attn_{'decode' if decode else 'prefill'}_fp8, "
-                    "serial")
-    else:
-        e2e_path = (f"inkling_{'decode' if decode else 'prefill'}_step_host, {chunks} groups"
-                    + ("" if decode else " (sequences cut into query-tile pieces)"))
+    e2e_path = (f"inkling_{'decode' if decode else 'prefill'}_step_host{'_fp8' if fp8 else ''}, "
+                f"{chunks} groups" + ("" if decode else " (sequences cut into query-tile pieces)"))
 
     def host_step():
         step_args = (host_in[0], host_in[1], host_in[2], host_out, (*dev_in, out), cu_host,
                      g.w_k, g.w_v, g.state, g.cu_q_lens, g.slot_mapping, g.k_cache, g.v_cache,
                      g.block_table, g.seq_lens, g.bias)
         if fp8:
-            for d, h in zip(dev_in, host_in):
-                d.copy_(h, non_blocking=True)
-            sconv(dev_in[1], dev_in[2])
-            attn(dev_in[0], out)
-            host_out.copy_(out, non_blocking=True)
+            kw = dict(k_scale=K_SCALE, v_scale=V_SCALE, scale=spec.scale, window=spec.window,
+                      max_q_len=spec.max_q_len, max_seq_len=spec.max_seq_len,
+                      workspace=workspace, h2d_stream=up, d2h_stream=down, chunks=chunks,
+                      dev_status=status)
+            if decode:
+                ink.decode_step_host_fp8(*step_args, **kw)
+            else:
+                ink.prefill_step_host_fp8(*step_args, **kw)
         elif decode:
             ink.decode_step_host(*step_args, scale=spec.scale, window=spec.window,
                                  max_q_len=spec.max_q_len, max_seq_len=spec.max_seq_len,

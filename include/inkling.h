@@ -406,6 +406,40 @@ INKLING_API int inkling_decode_step_host(
     inkling_stream_t d2h_stream);
 
 /*
+ * inkling_prefill_step_host_fp8 / inkling_decode_step_host_fp8 — the same whole steps over
+ * an E4M3 cache (vLLM Day-0 Inkling blog, "Roadmap": FP8 for the global-attention
+ * layers): each group runs inkling_sconv_kv_fp8 (codes written with k_scale / v_scale),
+ * then inkling_rel_attn_prefill_fp8 or inkling_rel_attn_decode_fp8.  Arguments as for the
+ * bf16 forms, plus the scales (positive and finite), max_seq_len, and the workspace of the
+ * FP8 call: for the prefill, inkling_rel_attn_prefill_fp8_workspace_size(B, Hkv,
+ * max_blocks, max_q_len, max_seq_len, window) bytes, into which each group widens the
+ * pages it reads (the groups reuse it one after another on `stream`); for the decode, as
+ * inkling_decode_step_host.  Outputs are bit-identical to the separate FP8 calls.
+ */
+INKLING_API int inkling_prefill_step_host_fp8(
+    const void *q_host, const void *k_raw_host, const void *v_raw_host, void *out_host,
+    void *q_dev, void *k_raw_dev, void *v_raw_dev, void *out_dev, const int32_t *cu_q_lens_host,
+    const float *w_k, const float *w_v, void *sconv_state, const int32_t *cu_q_lens,
+    const int64_t *slot_mapping, void *k_cache, void *v_cache, float k_scale, float v_scale,
+    const int32_t *block_table, int32_t max_blocks, const int32_t *seq_lens, const float *bias,
+    int32_t R, float scale, int32_t window, int32_t out_dtype, float *lse, int32_t B, int32_t T,
+    int32_t Hq, int32_t Hkv, int64_t num_blocks, int32_t max_q_len, int32_t max_seq_len,
+    void *workspace, size_t workspace_bytes, int32_t chunks, int32_t *dev_scratch,
+    int32_t *dev_status, inkling_stream_t stream, inkling_stream_t h2d_stream,
+    inkling_stream_t d2h_stream);
+INKLING_API int inkling_decode_step_host_fp8(
+    const void *q_host, const void *k_raw_host, const void *v_raw_host, void *out_host,
+    void *q_dev, void *k_raw_dev, void *v_raw_dev, void *out_dev, const int32_t *cu_q_lens_host,
+    const float *w_k, const float *w_v, void *sconv_state, const int32_t *cu_q_lens,
+    const int64_t *slot_mapping, void *k_cache, void *v_cache, float k_scale, float v_scale,
+    const int32_t *block_table, int32_t max_blocks, const int32_t *seq_lens, const float *bias,
+    int32_t R, float scale, int32_t window, int32_t out_dtype, float *lse, int32_t B, int32_t T,
+    int32_t Hq, int32_t Hkv, int64_t num_blocks, int32_t max_q_len, int32_t max_seq_len,
+    int32_t num_splits, void *workspace, size_t workspace_bytes, int32_t chunks,
+    int32_t *dev_status, inkling_stream_t stream, inkling_stream_t h2d_stream,
+    inkling_stream_t d2h_stream);
+
+/*
  * inkling_selftest_bounded_wait — checks, on the device, the bounded waits that every
  * pipeline kernel uses (their failure detection).  `ctas` CTAs each wait, with the
  * kernels' own wait, on a barrier that nothing arrives on.  mode 0: every wait must give

@@ -116,10 +116,10 @@ def sconv_state_rollback(state_before: torch.Tensor, x0: torch.Tensor,
 
 
 def _attn_common(q, k_cache, v_cache, block_table, cu_q_lens, seq_lens, bias, out, lse,
-                 dev_status):
+                 dev_status, cache_dtype=torch.bfloat16):
     dev = _check_cuda(q, k_cache, v_cache, block_table, cu_q_lens, seq_lens, bias, out, lse,
                       dev_status)
-    assert q.dtype == k_cache.dtype == v_cache.dtype == torch.bfloat16
+    assert q.dtype == torch.bfloat16 and k_cache.dtype == v_cache.dtype == cache_dtype
     assert block_table.dtype == cu_q_lens.dtype == seq_lens.dtype == torch.int32
     assert bias.dtype == torch.float32
     if out.dtype == torch.bfloat16:
@@ -317,14 +317,14 @@ def _check_host(*ts):
 
 def _step_args(q_host, k_raw_host, v_raw_host, out_host, staging, cu_q_lens_host, w_k, w_v,
                sconv_state, cu_q_lens, slot_mapping, k_cache, v_cache, block_table, seq_lens,
-               bias, lse, dev_status):
+               bias, lse, dev_status, cache_dtype=torch.bfloat16):
     q_dev, k_dev, v_dev, out_dev = staging
     _check_host(q_host, k_raw_host, v_raw_host, out_host)
     if cu_q_lens_host.is_cuda or cu_q_lens_host.dtype != torch.int32:
         raise ValueError("cu_q_lens_host must be an int32 CPU tensor")
     cu_host = cu_q_lens_host.contiguous()
     dev, out_dtype = _attn_common(q_dev, k_cache, v_cache, block_table, cu_q_lens, seq_lens,
-                                  bias, out_dev, lse, dev_status)
+                                  bias, out_dev, lse, dev_status, cache_dtype)
     _check_cuda(q_dev, k_dev, v_dev, out_dev, w_k, w_v, sconv_state, cu_q_lens, slot_mapping,
                 k_cache, v_cache, block_table, seq_lens, bias, lse, dev_status)
     for h, d in ((q_host, q_dev), (k_raw_host, k_dev), (v_raw_host, v_dev), (out_host, out_dev)):
@@ -392,6 +392,75 @@ def decode_step_host(q_host, k_raw_host, v_raw_host, out_host, staging, cu_q_len
                   q_dev.shape[0], q_dev.shape[1], hkv, k_cache.shape[0], int(max_q_len),
                   int(max_seq_len), int(num_splits), workspace, ws_bytes, int(chunks),
                   dev_status, _stream(stream), h2d_stream.cuda_stream, d2h_stream.cuda_stream)
+
+
+def prefill_step_host_fp8(q_host, k_raw_host, v_raw_host, out_host, staging, cu_q_lens_host,
+                          w_k, w_v, sconv_state, cu_q_lens, slot_mapping, k_cache, v_cache,
+                          block_table, seq_lens, bias, *, k_scale: float, v_scale: float,
+                          scale: float, window: int, max_q_len: int, max_seq_len: int,
+                          h2d_stream, d2h_stream, chunks: int = 4, split_sequences: bool = True,
+                          scratch: Optional[torch.Tensor] = None,
+                          workspace: Optional[torch.Tensor] = None, lse=None, dev_status=None,
+                          stream=None) -> None:
+    """inkling_prefill_step_host_fp8: sconv_kv_fp8 + rel_attn_prefill_fp8 over host buffers,
+    as prefill_step_host, for E4M3 (uint8) caches.  `workspace` takes the widened pages
+    (prefill_fp8_workspace_size bytes for all B sequences, allocated when omitted)."""
+    dev, out_dtype, cu_host = _step_args(q_host, k_raw_host, v_raw_host, out_host, staging,
+                                         cu_q_lens_host, w_k, w_v, sconv_state, cu_q_lens,
+                                         slot_mapping, k_cache, v_cache, block_table, seq_lens,
+                                         bias, lse, dev_status, torch.uint8)
+    q_dev, k_dev, v_dev, out_dev = staging
+    B = cu_q_lens.shape[0] - 1
+    hkv = k_cache.shape[1]
+    with torch.cuda.device(dev):
+        if split_sequences and scratch is None:
+            scratch = torch.empty(4 * max(int(chunks), 1), dtype=torch.int32, device=dev)
+        if not split_sequences:
+            scratch = None
+        if workspace is None:
+            need = prefill_fp8_workspace_size(B, hkv, block_table.shape[1], max_q_len,
+                                              max_seq_len, window)
+            workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+        ws_bytes = workspace.numel() * workspace.element_size()
+        _lib.call("inkling_prefill_step_host_fp8", q_host, k_raw_host, v_raw_host, out_host,
+                  q_dev, k_dev, v_dev, out_dev, cu_host, w_k, w_v, sconv_state, cu_q_lens,
+                  slot_mapping, k_cache, v_cache, float(k_scale), float(v_scale), block_table,
+                  block_table.shape[1], seq_lens, bias, bias.shape[1], float(scale), int(window),
+                  out_dtype, lse, B, q_dev.shape[0], q_dev.shape[1], hkv, k_cache.shape[0],
+                  int(max_q_len), int(max_seq_len), workspace, ws_bytes, int(chunks), scratch,
+                  dev_status, _stream(stream), h2d_stream.cuda_stream, d2h_stream.cuda_stream)
+
+
+def decode_step_host_fp8(q_host, k_raw_host, v_raw_host, out_host, staging, cu_q_lens_host,
+                         w_k, w_v, sconv_state, cu_q_lens, slot_mapping, k_cache, v_cache,
+                         block_table, seq_lens, bias, *, k_scale: float, v_scale: float,
+                         scale: float, window: int, max_q_len: int, max_seq_len: int,
+                         h2d_stream, d2h_stream, num_splits: int = 0,
+                         workspace: Optional[torch.Tensor] = None, chunks: int = 1, lse=None,
+                         dev_status=None, stream=None) -> None:
+    """inkling_decode_step_host_fp8: sconv_kv_fp8 + rel_attn_decode_fp8 over host buffers,
+    as decode_step_host, for E4M3 (uint8) caches."""
+    dev, out_dtype, cu_host = _step_args(q_host, k_raw_host, v_raw_host, out_host, staging,
+                                         cu_q_lens_host, w_k, w_v, sconv_state, cu_q_lens,
+                                         slot_mapping, k_cache, v_cache, block_table, seq_lens,
+                                         bias, lse, dev_status, torch.uint8)
+    q_dev, k_dev, v_dev, out_dev = staging
+    B = cu_q_lens.shape[0] - 1
+    hkv = k_cache.shape[1]
+    with torch.cuda.device(dev):
+        need = _lib.workspace_size(B, q_dev.shape[1], hkv, int(max_q_len), int(max_seq_len),
+                                   int(window), int(num_splits))
+        if workspace is None and need > 0:
+            workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+        ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+        _lib.call("inkling_decode_step_host_fp8", q_host, k_raw_host, v_raw_host, out_host,
+                  q_dev, k_dev, v_dev, out_dev, cu_host, w_k, w_v, sconv_state, cu_q_lens,
+                  slot_mapping, k_cache, v_cache, float(k_scale), float(v_scale), block_table,
+                  block_table.shape[1], seq_lens, bias, bias.shape[1], float(scale), int(window),
+                  out_dtype, lse, B, q_dev.shape[0], q_dev.shape[1], hkv, k_cache.shape[0],
+                  int(max_q_len), int(max_seq_len), int(num_splits), workspace, ws_bytes,
+                  int(chunks), dev_status, _stream(stream), h2d_stream.cuda_stream,
+                  d2h_stream.cuda_stream)
 
 
 def selftest_bounded_wait(mode: int, ctas: int, dev_status: torch.Tensor,

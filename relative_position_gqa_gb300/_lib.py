@@ -43,6 +43,12 @@ SIGNATURES = {
     "inkling_decode_step_host": [P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, I32, P, P,
                                  I32, F32, I32, I32, P, I32, I32, I32, I32, I64, I32, I32, I32,
                                  P, SZ, I32, P, P, P, P],
+    "inkling_prefill_step_host_fp8": [P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, F32, F32, P,
+                                      I32, P, P, I32, F32, I32, I32, P, I32, I32, I32, I32, I64,
+                                      I32, I32, P, SZ, I32, P, P, P, P, P],
+    "inkling_decode_step_host_fp8": [P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, F32, F32, P,
+                                     I32, P, P, I32, F32, I32, I32, P, I32, I32, I32, I32, I64,
+                                     I32, I32, I32, P, SZ, I32, P, P, P, P],
     "inkling_selftest_bounded_wait": [I32, I32, P, P, P],
     "inkling_status_string": [ctypes.c_int],
     "inkling_version": [],

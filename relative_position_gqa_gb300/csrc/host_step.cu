@@ -6,6 +6,7 @@
 // Host code only: the kernels are the ones the separate calls launch.
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <cstdint>
 #include <vector>
 
@@ -197,6 +198,159 @@ int prepare(const void* q_host, const void* k_raw_host, const void* v_raw_host, 
   return INKLING_OK;
 }
 
+bool scales_ok(float k_scale, float v_scale) {
+  return k_scale > 0.f && v_scale > 0.f && std::isfinite(k_scale) && std::isfinite(v_scale);
+}
+
+// One prefill step over a bf16 cache (fp8 false) or an E4M3 cache (fp8 true: the conv
+// writes E4M3 codes with k_scale / v_scale, and each group's attention widens the pages it
+// reads into `workspace`, which the groups reuse one after another on `stream`).
+int prefill_step(bool fp8, float k_scale, float v_scale, const void* q_host,
+                 const void* k_raw_host, const void* v_raw_host, void* out_host, void* q_dev,
+                 void* k_raw_dev, void* v_raw_dev, void* out_dev, const int32_t* cu_q_lens_host,
+                 const float* w_k, const float* w_v, void* sconv_state, const int32_t* cu_q_lens,
+                 const int64_t* slot_mapping, void* k_cache, void* v_cache,
+                 const int32_t* block_table, int32_t max_blocks, const int32_t* seq_lens,
+                 const float* bias, int32_t R, float scale, int32_t window, int32_t out_dtype,
+                 float* lse, int32_t B, int32_t T, int32_t Hq, int32_t Hkv, int64_t num_blocks,
+                 int32_t max_q_len, int32_t max_seq_len, void* workspace, size_t workspace_bytes,
+                 int32_t chunks, int32_t* dev_scratch, int32_t* dev_status,
+                 inkling_stream_t stream, inkling_stream_t h2d_stream,
+                 inkling_stream_t d2h_stream) {
+  HostRows h;
+  std::vector<Group> groups;
+  int rc = prepare(q_host, k_raw_host, v_raw_host, out_host, q_dev, k_raw_dev, v_raw_dev,
+                   out_dev, cu_q_lens_host, out_dtype, B, T, Hq, Hkv, max_q_len, chunks, stream,
+                   h2d_stream, d2h_stream, &h, &groups);
+  if (rc != INKLING_OK) return rc;
+  if (!w_k || !w_v || !sconv_state || !cu_q_lens || !slot_mapping || !block_table || !seq_lens)
+    return INKLING_ERR_INVALID_ARG;
+  if (fp8 && (!scales_ok(k_scale, v_scale) || max_seq_len < 0)) return INKLING_ERR_INVALID_ARG;
+  if (B == 0 || T == 0) return INKLING_OK;
+  // the widened pages of any group fit in a workspace sized for all B sequences
+  if (fp8 && max_q_len > 0 && max_seq_len > 0 &&
+      (workspace == nullptr ||
+       workspace_bytes < ink::prefill_fp8_workspace_bytes(B, Hkv, max_blocks, max_q_len,
+                                                          max_seq_len, window)))
+    return INKLING_ERR_WORKSPACE;
+  // with scratch for their lengths, long sequences may be cut into pieces
+  if (dev_scratch != nullptr) groups = make_prefill_groups(cu_q_lens_host, B, chunks);
+  const size_t state_seq = (size_t)2 * 3 * Hkv * 128 * 2;  // bytes of one sequence's state
+  const size_t kv_row = (size_t)Hkv * 128 * 2;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  auto conv = [&](const void* k_raw, const void* v_raw, void* state, const int32_t* cu,
+                  const int64_t* slots, int nb, int t, int max_n) {
+    return fp8 ? inkling_sconv_kv_fp8(k_raw, v_raw, w_k, w_v, state, cu, slots, k_cache, v_cache,
+                                      k_scale, v_scale, nb, t, Hkv, num_blocks, max_n, dev_status,
+                                      stream)
+               : inkling_sconv_kv(k_raw, v_raw, w_k, w_v, state, cu, slots, k_cache, v_cache, nb,
+                                  t, Hkv, num_blocks, max_n, dev_status, stream);
+  };
+  auto attn = [&](const void* q, const int32_t* table, const int32_t* cu, const int32_t* lens,
+                  void* out, float* lse_g, int nb, int t, int max_n) {
+    return fp8 ? inkling_rel_attn_prefill_fp8(q, k_cache, v_cache, k_scale, v_scale, table,
+                                              max_blocks, cu, lens, bias, R, scale, window, out,
+                                              out_dtype, lse_g, nb, t, Hq, Hkv, num_blocks, max_n,
+                                              max_seq_len, workspace, workspace_bytes, dev_status,
+                                              stream)
+               : inkling_rel_attn_prefill(q, k_cache, v_cache, table, max_blocks, cu, lens, bias,
+                                          R, scale, window, out, out_dtype, lse_g, nb, t, Hq, Hkv,
+                                          num_blocks, max_n, dev_status, stream);
+  };
+  int piece = 0;
+  auto launch = [&](const Group& g) {
+    if (g.piece) {
+      // one run of sequence b's tokens: pointers start at its first row, and the lengths
+      // come from a scratch slot (cu = {0, rows}, the sequence's length at its last row)
+      int32_t* lens = dev_scratch + 4 * piece++;  // piece < chunks by construction
+      const int b = g.b0;
+      const int rel0 = (int)(g.t0 - cu_q_lens_host[b]), rel1 = (int)(g.t1 - cu_q_lens_host[b]);
+      const int rows = rel1 - rel0;
+      piece_lens_kernel<<<1, 32, 0, st>>>(cu_q_lens, seq_lens, b, rel0, rel1, lens);
+      if (cudaGetLastError() != cudaSuccess) return (int)INKLING_ERR_CUDA;
+      int r = conv(static_cast<uint8_t*>(k_raw_dev) + g.t0 * kv_row,
+                   static_cast<uint8_t*>(v_raw_dev) + g.t0 * kv_row,
+                   static_cast<uint8_t*>(sconv_state) + b * state_seq, lens, slot_mapping + g.t0,
+                   1, rows, rows);
+      if (r != INKLING_OK) return r;
+      return attn(static_cast<uint8_t*>(q_dev) + g.t0 * h.q_row,
+                  block_table + (size_t)b * max_blocks, lens, lens + 2,
+                  static_cast<uint8_t*>(out_dev) + g.t0 * h.out_row,
+                  lse ? lse + g.t0 * Hq : nullptr, 1, rows, rows);
+    }
+    const int nb = g.b1 - g.b0;
+    int r = conv(k_raw_dev, v_raw_dev, static_cast<uint8_t*>(sconv_state) + g.b0 * state_seq,
+                 cu_q_lens + g.b0, slot_mapping, nb, T, g.max_n);
+    if (r != INKLING_OK) return r;
+    return attn(q_dev, block_table + (size_t)g.b0 * max_blocks, cu_q_lens + g.b0,
+                seq_lens + g.b0, out_dev, lse, nb, T, g.max_n);
+  };
+  return run_groups(h, groups, st, reinterpret_cast<cudaStream_t>(h2d_stream),
+                    reinterpret_cast<cudaStream_t>(d2h_stream), launch);
+}
+
+// One decode step over a bf16 cache or (fp8 true) an E4M3 cache.
+int decode_step(bool fp8, float k_scale, float v_scale, const void* q_host,
+                const void* k_raw_host, const void* v_raw_host, void* out_host, void* q_dev,
+                void* k_raw_dev, void* v_raw_dev, void* out_dev, const int32_t* cu_q_lens_host,
+                const float* w_k, const float* w_v, void* sconv_state, const int32_t* cu_q_lens,
+                const int64_t* slot_mapping, void* k_cache, void* v_cache,
+                const int32_t* block_table, int32_t max_blocks, const int32_t* seq_lens,
+                const float* bias, int32_t R, float scale, int32_t window, int32_t out_dtype,
+                float* lse, int32_t B, int32_t T, int32_t Hq, int32_t Hkv, int64_t num_blocks,
+                int32_t max_q_len, int32_t max_seq_len, int32_t num_splits, void* workspace,
+                size_t workspace_bytes, int32_t chunks, int32_t* dev_status,
+                inkling_stream_t stream, inkling_stream_t h2d_stream,
+                inkling_stream_t d2h_stream) {
+  HostRows h;
+  std::vector<Group> groups;
+  int rc = prepare(q_host, k_raw_host, v_raw_host, out_host, q_dev, k_raw_dev, v_raw_dev,
+                   out_dev, cu_q_lens_host, out_dtype, B, T, Hq, Hkv, max_q_len, chunks, stream,
+                   h2d_stream, d2h_stream, &h, &groups);
+  if (rc != INKLING_OK) return rc;
+  if (!w_k || !w_v || !sconv_state || !cu_q_lens || !slot_mapping || !block_table || !seq_lens)
+    return INKLING_ERR_INVALID_ARG;
+  if (max_q_len > INKLING_MAX_DECODE_Q || num_splits < 0 || max_seq_len < 0)
+    return INKLING_ERR_INVALID_ARG;
+  if (fp8 && !scales_ok(k_scale, v_scale)) return INKLING_ERR_INVALID_ARG;
+  if (B == 0 || T == 0) return INKLING_OK;
+  // One split count for every group, the one the whole batch would get: a group's
+  // partials then fit in a workspace sized for all B sequences.
+  if (num_splits == 0 && groups.size() > 1) {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+      return INKLING_ERR_CUDA;
+    num_splits = ink::decode_split(B, Hkv, max_q_len, max_seq_len, window, 0, sms).num_splits;
+  }
+  const size_t state_seq = (size_t)2 * 3 * Hkv * 128 * 2;
+  auto launch = [&](const Group& g) {
+    const int nb = g.b1 - g.b0;
+    void* state = static_cast<uint8_t*>(sconv_state) + g.b0 * state_seq;
+    int r = fp8 ? inkling_sconv_kv_fp8(k_raw_dev, v_raw_dev, w_k, w_v, state, cu_q_lens + g.b0,
+                                       slot_mapping, k_cache, v_cache, k_scale, v_scale, nb, T,
+                                       Hkv, num_blocks, g.max_n, dev_status, stream)
+                : inkling_sconv_kv(k_raw_dev, v_raw_dev, w_k, w_v, state, cu_q_lens + g.b0,
+                                   slot_mapping, k_cache, v_cache, nb, T, Hkv, num_blocks,
+                                   g.max_n, dev_status, stream);
+    if (r != INKLING_OK) return r;
+    const int32_t* table = block_table + (size_t)g.b0 * max_blocks;
+    return fp8 ? inkling_rel_attn_decode_fp8(q_dev, k_cache, v_cache, k_scale, v_scale, table,
+                                             max_blocks, cu_q_lens + g.b0, seq_lens + g.b0, bias,
+                                             R, scale, window, out_dev, out_dtype, lse, nb, T, Hq,
+                                             Hkv, num_blocks, g.max_n, max_seq_len, num_splits,
+                                             workspace, workspace_bytes, dev_status, stream)
+               : inkling_rel_attn_decode(q_dev, k_cache, v_cache, table, max_blocks,
+                                         cu_q_lens + g.b0, seq_lens + g.b0, bias, R, scale,
+                                         window, out_dev, out_dtype, lse, nb, T, Hq, Hkv,
+                                         num_blocks, g.max_n, max_seq_len, num_splits, workspace,
+                                         workspace_bytes, dev_status, stream);
+  };
+  return run_groups(h, groups, reinterpret_cast<cudaStream_t>(stream),
+                    reinterpret_cast<cudaStream_t>(h2d_stream),
+                    reinterpret_cast<cudaStream_t>(d2h_stream), launch);
+}
+
 }  // namespace
 
 extern "C" {
@@ -211,59 +365,31 @@ int inkling_prefill_step_host(
     int32_t Hkv, int64_t num_blocks, int32_t max_q_len, int32_t chunks, int32_t* dev_scratch,
     int32_t* dev_status, inkling_stream_t stream, inkling_stream_t h2d_stream,
     inkling_stream_t d2h_stream) {
-  HostRows h;
-  std::vector<Group> groups;
-  int rc = prepare(q_host, k_raw_host, v_raw_host, out_host, q_dev, k_raw_dev, v_raw_dev,
-                   out_dev, cu_q_lens_host, out_dtype, B, T, Hq, Hkv, max_q_len, chunks, stream,
-                   h2d_stream, d2h_stream, &h, &groups);
-  if (rc != INKLING_OK) return rc;
-  if (!w_k || !w_v || !sconv_state || !cu_q_lens || !slot_mapping || !block_table || !seq_lens)
-    return INKLING_ERR_INVALID_ARG;
-  if (B == 0 || T == 0) return INKLING_OK;
-  // with scratch for their lengths, long sequences may be cut into pieces
-  if (dev_scratch != nullptr) groups = make_prefill_groups(cu_q_lens_host, B, chunks);
-  const size_t state_seq = (size_t)2 * 3 * Hkv * 128 * 2;  // bytes of one sequence's state
-  const size_t kv_row = (size_t)Hkv * 128 * 2;
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  int piece = 0;
-  auto launch = [&](const Group& g) {
-    if (g.piece) {
-      // one run of sequence b's tokens: pointers start at its first row, and the lengths
-      // come from a scratch slot (cu = {0, rows}, the sequence's length at its last row)
-      int32_t* lens = dev_scratch + 4 * piece++;  // piece < chunks by construction
-      const int b = g.b0;
-      const int rel0 = (int)(g.t0 - cu_q_lens_host[b]), rel1 = (int)(g.t1 - cu_q_lens_host[b]);
-      const int rows = rel1 - rel0;
-      piece_lens_kernel<<<1, 32, 0, st>>>(cu_q_lens, seq_lens, b, rel0, rel1, lens);
-      if (cudaGetLastError() != cudaSuccess) return (int)INKLING_ERR_CUDA;
-      int r = inkling_sconv_kv(static_cast<uint8_t*>(k_raw_dev) + g.t0 * kv_row,
-                               static_cast<uint8_t*>(v_raw_dev) + g.t0 * kv_row, w_k, w_v,
-                               static_cast<uint8_t*>(sconv_state) + b * state_seq, lens,
-                               slot_mapping + g.t0, k_cache, v_cache, 1, rows, Hkv, num_blocks,
-                               rows, dev_status, stream);
-      if (r != INKLING_OK) return r;
-      return inkling_rel_attn_prefill(static_cast<uint8_t*>(q_dev) + g.t0 * h.q_row, k_cache,
-                                      v_cache, block_table + (size_t)b * max_blocks, max_blocks,
-                                      lens, lens + 2, bias, R, scale, window,
-                                      static_cast<uint8_t*>(out_dev) + g.t0 * h.out_row,
-                                      out_dtype, lse ? lse + g.t0 * Hq : nullptr, 1, rows, Hq,
-                                      Hkv, num_blocks, rows, dev_status, stream);
-    }
-    const int nb = g.b1 - g.b0;
-    int r = inkling_sconv_kv(k_raw_dev, v_raw_dev, w_k, w_v,
-                             static_cast<uint8_t*>(sconv_state) + g.b0 * state_seq,
-                             cu_q_lens + g.b0, slot_mapping, k_cache, v_cache, nb, T, Hkv,
-                             num_blocks, g.max_n, dev_status, stream);
-    if (r != INKLING_OK) return r;
-    return inkling_rel_attn_prefill(q_dev, k_cache, v_cache,
-                                    block_table + (size_t)g.b0 * max_blocks, max_blocks,
-                                    cu_q_lens + g.b0, seq_lens + g.b0, bias, R, scale, window,
-                                    out_dev, out_dtype, lse, nb, T, Hq, Hkv, num_blocks, g.max_n,
-                                    dev_status, stream);
-  };
-  return run_groups(h, groups, reinterpret_cast<cudaStream_t>(stream),
-                    reinterpret_cast<cudaStream_t>(h2d_stream),
-                    reinterpret_cast<cudaStream_t>(d2h_stream), launch);
+  return prefill_step(false, 1.f, 1.f, q_host, k_raw_host, v_raw_host, out_host, q_dev,
+                      k_raw_dev, v_raw_dev, out_dev, cu_q_lens_host, w_k, w_v, sconv_state,
+                      cu_q_lens, slot_mapping, k_cache, v_cache, block_table, max_blocks,
+                      seq_lens, bias, R, scale, window, out_dtype, lse, B, T, Hq, Hkv, num_blocks,
+                      max_q_len, 0, nullptr, 0, chunks, dev_scratch, dev_status, stream,
+                      h2d_stream, d2h_stream);
+}
+
+int inkling_prefill_step_host_fp8(
+    const void* q_host, const void* k_raw_host, const void* v_raw_host, void* out_host,
+    void* q_dev, void* k_raw_dev, void* v_raw_dev, void* out_dev, const int32_t* cu_q_lens_host,
+    const float* w_k, const float* w_v, void* sconv_state, const int32_t* cu_q_lens,
+    const int64_t* slot_mapping, void* k_cache, void* v_cache, float k_scale, float v_scale,
+    const int32_t* block_table, int32_t max_blocks, const int32_t* seq_lens, const float* bias,
+    int32_t R, float scale, int32_t window, int32_t out_dtype, float* lse, int32_t B, int32_t T,
+    int32_t Hq, int32_t Hkv, int64_t num_blocks, int32_t max_q_len, int32_t max_seq_len,
+    void* workspace, size_t workspace_bytes, int32_t chunks, int32_t* dev_scratch,
+    int32_t* dev_status, inkling_stream_t stream, inkling_stream_t h2d_stream,
+    inkling_stream_t d2h_stream) {
+  return prefill_step(true, k_scale, v_scale, q_host, k_raw_host, v_raw_host, out_host, q_dev,
+                      k_raw_dev, v_raw_dev, out_dev, cu_q_lens_host, w_k, w_v, sconv_state,
+                      cu_q_lens, slot_mapping, k_cache, v_cache, block_table, max_blocks,
+                      seq_lens, bias, R, scale, window, out_dtype, lse, B, T, Hq, Hkv, num_blocks,
+                      max_q_len, max_seq_len, workspace, workspace_bytes, chunks, dev_scratch,
+                      dev_status, stream, h2d_stream, d2h_stream);
 }
 
 int inkling_decode_step_host(
@@ -277,44 +403,31 @@ int inkling_decode_step_host(
     int32_t num_splits, void* workspace, size_t workspace_bytes, int32_t chunks,
     int32_t* dev_status, inkling_stream_t stream, inkling_stream_t h2d_stream,
     inkling_stream_t d2h_stream) {
-  HostRows h;
-  std::vector<Group> groups;
-  int rc = prepare(q_host, k_raw_host, v_raw_host, out_host, q_dev, k_raw_dev, v_raw_dev,
-                   out_dev, cu_q_lens_host, out_dtype, B, T, Hq, Hkv, max_q_len, chunks, stream,
-                   h2d_stream, d2h_stream, &h, &groups);
-  if (rc != INKLING_OK) return rc;
-  if (!w_k || !w_v || !sconv_state || !cu_q_lens || !slot_mapping || !block_table || !seq_lens)
-    return INKLING_ERR_INVALID_ARG;
-  if (max_q_len > INKLING_MAX_DECODE_Q || num_splits < 0 || max_seq_len < 0)
-    return INKLING_ERR_INVALID_ARG;
-  if (B == 0 || T == 0) return INKLING_OK;
-  // One split count for every group, the one the whole batch would get: a group's
-  // partials then fit in a workspace sized for all B sequences.
-  if (num_splits == 0 && groups.size() > 1) {
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
-      return INKLING_ERR_CUDA;
-    num_splits = ink::decode_split(B, Hkv, max_q_len, max_seq_len, window, 0, sms).num_splits;
-  }
-  const size_t state_seq = (size_t)2 * 3 * Hkv * 128 * 2;
-  auto launch = [&](const Group& g) {
-    const int nb = g.b1 - g.b0;
-    int r = inkling_sconv_kv(k_raw_dev, v_raw_dev, w_k, w_v,
-                             static_cast<uint8_t*>(sconv_state) + g.b0 * state_seq,
-                             cu_q_lens + g.b0, slot_mapping, k_cache, v_cache, nb, T, Hkv,
-                             num_blocks, g.max_n, dev_status, stream);
-    if (r != INKLING_OK) return r;
-    return inkling_rel_attn_decode(q_dev, k_cache, v_cache,
-                                   block_table + (size_t)g.b0 * max_blocks, max_blocks,
-                                   cu_q_lens + g.b0, seq_lens + g.b0, bias, R, scale, window,
-                                   out_dev, out_dtype, lse, nb, T, Hq, Hkv, num_blocks, g.max_n,
-                                   max_seq_len, num_splits, workspace, workspace_bytes,
-                                   dev_status, stream);
-  };
-  return run_groups(h, groups, reinterpret_cast<cudaStream_t>(stream),
-                    reinterpret_cast<cudaStream_t>(h2d_stream),
-                    reinterpret_cast<cudaStream_t>(d2h_stream), launch);
+  return decode_step(false, 1.f, 1.f, q_host, k_raw_host, v_raw_host, out_host, q_dev,
+                     k_raw_dev, v_raw_dev, out_dev, cu_q_lens_host, w_k, w_v, sconv_state,
+                     cu_q_lens, slot_mapping, k_cache, v_cache, block_table, max_blocks,
+                     seq_lens, bias, R, scale, window, out_dtype, lse, B, T, Hq, Hkv, num_blocks,
+                     max_q_len, max_seq_len, num_splits, workspace, workspace_bytes, chunks,
+                     dev_status, stream, h2d_stream, d2h_stream);
+}
+
+int inkling_decode_step_host_fp8(
+    const void* q_host, const void* k_raw_host, const void* v_raw_host, void* out_host,
+    void* q_dev, void* k_raw_dev, void* v_raw_dev, void* out_dev, const int32_t* cu_q_lens_host,
+    const float* w_k, const float* w_v, void* sconv_state, const int32_t* cu_q_lens,
+    const int64_t* slot_mapping, void* k_cache, void* v_cache, float k_scale, float v_scale,
+    const int32_t* block_table, int32_t max_blocks, const int32_t* seq_lens, const float* bias,
+    int32_t R, float scale, int32_t window, int32_t out_dtype, float* lse, int32_t B, int32_t T,
+    int32_t Hq, int32_t Hkv, int64_t num_blocks, int32_t max_q_len, int32_t max_seq_len,
+    int32_t num_splits, void* workspace, size_t workspace_bytes, int32_t chunks,
+    int32_t* dev_status, inkling_stream_t stream, inkling_stream_t h2d_stream,
+    inkling_stream_t d2h_stream) {
+  return decode_step(true, k_scale, v_scale, q_host, k_raw_host, v_raw_host, out_host, q_dev,
+                     k_raw_dev, v_raw_dev, out_dev, cu_q_lens_host, w_k, w_v, sconv_state,
+                     cu_q_lens, slot_mapping, k_cache, v_cache, block_table, max_blocks,
+                     seq_lens, bias, R, scale, window, out_dtype, lse, B, T, Hq, Hkv, num_blocks,
+                     max_q_len, max_seq_len, num_splits, workspace, workspace_bytes, chunks,
+                     dev_status, stream, h2d_stream, d2h_stream);
 }
 
 }  // extern "C"

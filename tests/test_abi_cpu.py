@@ -186,6 +186,42 @@ def test_step_host_checks(lib, name, over):
     assert _step(lib, name, **over) == 1
 
 
+def _step_fp8(lib, name, **over):
+    cu = (ctypes.c_int32 * 3)(0, 5, 10)
+    a = dict(qh=FAKE, kh=FAKE, vh=FAKE, oh=FAKE, qd=FAKE, kd=FAKE, vd=FAKE, od=FAKE,
+             cu_h=ctypes.cast(cu, ctypes.c_void_p), wk=FAKE, wv=FAKE, st=FAKE, cu=FAKE,
+             slot=FAKE, kc=FAKE, vc=FAKE, ks=0.5, vs=0.25, bt=FAKE, maxb=4, sl=FAKE, bias=FAKE,
+             R=64, scale=0.1, window=0, odt=0, lse=None, B=2, T=10, Hq=4, Hkv=2, nb=4, mq=5,
+             msl=500)
+    if name == "inkling_decode_step_host_fp8":
+        a.update(ns=0, ws=None, wsb=0, chunks=2)
+    else:
+        a.update(ws=None, wsb=0, chunks=2, scratch=None)
+    a.update(ds=None, s=None, up=0x20000, down=0x30000)
+    a.update(over)
+    rc = getattr(lib, name)(*a.values())
+    del cu
+    return rc
+
+
+@pytest.mark.parametrize("name", ["inkling_prefill_step_host_fp8", "inkling_decode_step_host_fp8"])
+@pytest.mark.parametrize("over", [dict(chunks=0), dict(up=0x30000), dict(qh=None), dict(odt=3),
+                                  dict(mq=4), dict(T=11), dict(wk=None), dict(ks=0.0),
+                                  dict(vs=float("inf")), dict(ks=-1.0), dict(msl=-1)])
+def test_step_host_fp8_checks(lib, name, over):
+    """The FP8 step forms reject what the bf16 forms reject, and scales that are not
+    positive and finite, before enqueueing anything."""
+    assert _step_fp8(lib, name, **over) == 1
+
+
+def test_prefill_step_host_fp8_needs_workspace(lib):
+    """The whole step's widening workspace is checked before any group is enqueued."""
+    need = lib.inkling_rel_attn_prefill_fp8_workspace_size(2, 2, 4, 5, 500, 0)
+    assert need > 0
+    assert _step_fp8(lib, "inkling_prefill_step_host_fp8") == 7          # INKLING_ERR_WORKSPACE
+    assert _step_fp8(lib, "inkling_prefill_step_host_fp8", ws=FAKE, wsb=need - 16) == 7
+
+
 def test_decode_step_host_checks(lib):
     assert _step(lib, "inkling_decode_step_host", mq=10) == 1   # more than 9 tokens
     assert _step(lib, "inkling_decode_step_host", ns=-1) == 1
