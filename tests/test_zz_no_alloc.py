@@ -93,3 +93,43 @@ def test_noalloc_decode_rejects_requests_beyond_capacity(ink):
                                     window=-1, max_q_len=9, max_seq_len=1 << 20, num_splits=2,
                                     out=torch.empty(9 * big_b, 8, 128, device=dev))
     assert e.value.code == 1  # INKLING_ERR_INVALID_ARG
+
+
+def test_noalloc_decode_graph_replay(ink):
+    """Captured into a CUDA graph (no allocation during the capture), the allocation-free
+    decode replays bit-identically to the eager call, and a replay after new Q values are
+    written into the captured buffer gives the eager call's new output."""
+    spec = W.small(q_lens=(9, 9, 3, 1), seq_lens=(500, 700, 129, 1000), hq=8, hkv=1, r=64)
+    c = W.make_case(spec, seed=23, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    gpu_sconv(ink, c, st)
+    out = torch.empty(spec.total_q, spec.hq, 128, device="cuda")
+    lse = torch.empty(spec.total_q, spec.hq, device="cuda")
+
+    def call():
+        ink.rel_attn_decode_noalloc(c.q, c.k_cache, c.v_cache, c.block_table, c.cu_q_lens,
+                                    c.seq_lens, c.bias, scale=spec.scale, window=spec.window,
+                                    max_q_len=spec.max_q_len, max_seq_len=spec.max_seq_len,
+                                    out=out, lse=lse, num_splits=3, dev_status=st)
+    call()
+    torch.cuda.synchronize()
+    ref, ref_lse = out.clone(), lse.clone()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        call()
+    for _ in range(2):
+        out.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        assert torch.equal(out.view(torch.int32), ref.view(torch.int32))
+        assert torch.equal(lse.view(torch.int32), ref_lse.view(torch.int32))
+    gen = torch.Generator(device="cuda").manual_seed(98)
+    c.q.copy_(torch.randn(c.q.shape, generator=gen, device="cuda").to(torch.bfloat16))
+    call()
+    torch.cuda.synchronize()
+    ref2 = out.clone()
+    out.fill_(float("nan"))
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int32), ref2.view(torch.int32))
