@@ -1,7 +1,6 @@
 """GPU parity of inkling_rel_attn_decode: paged KV, up to 9 query tokens per sequence (MTP
 verify, vLLM Day-0 Inkling blog "Model Architecture / MTP"), split over pages and merged
 ("FA4 with sheared bias": num_splits), full or sliding window."""
-import numpy as np
 import pytest
 import torch
 

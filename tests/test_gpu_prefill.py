@@ -1,7 +1,6 @@
 """GPU parity of inkling_rel_attn_prefill (relative-bias GQA over full or sliding windows;
 vLLM Day-0 Inkling blog, "Model Architecture / Attention") against the fp64 oracle, at
 sizes the oracle finishes in seconds that still span several tiles and ragged tails."""
-import numpy as np
 import pytest
 import torch
 

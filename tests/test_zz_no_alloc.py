@@ -5,7 +5,6 @@ static device scratch; its output must match the workspace-based decode call's w
 the parity tolerance, and the fp64 oracle's, on two calls in a row (the second reuses the
 scratch the first left behind).  Collected last on purpose: it also runs after every
 other GPU test."""
-import numpy as np
 import pytest
 import torch
 
