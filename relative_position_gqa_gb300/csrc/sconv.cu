@@ -26,11 +26,14 @@
 namespace ink {
 
 // New tokens per thread, and rows loaded ahead of use, per form (measured on GB300 for
-// 4 x 8192 tokens: the paged K/V conv over 1024 channels wants longer runs so that one
-// wave of CTAs covers the batch, the dense conv over 4096 channels more loads in flight).
+// 4 x 8192 tokens: the paged K/V conv over 1024 channels wants runs long enough that one
+// wave of CTAs covers the batch; the dense conv over 4096 channels wants more loads in
+// flight and runs of 256 tokens, whose 3-row halo adds 1.2% to the reads where runs of
+// 32 added 9% (32 / 64 / 128 / 256 / 512 tokens: 0.092 / 0.091 / 0.090 / 0.089 / 0.116 ms,
+// the last with too few CTAs to keep HBM busy)).
 template <bool kPaged> struct SconvShape;
 template <> struct SconvShape<true> { static constexpr int kChunk = 64, kBatch = 8; };
-template <> struct SconvShape<false> { static constexpr int kChunk = 32, kBatch = 16; };
+template <> struct SconvShape<false> { static constexpr int kChunk = 256, kBatch = 16; };
 constexpr int kVec = 8;       // channels per thread (one 16-byte vector of bf16)
 constexpr int kSconvThreads = 128;
 
